@@ -1,0 +1,328 @@
+"""CPU oracle for the SGMV LoRA delta -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never imports, links or calls it, and this package shares no
+code with the product: not the routing, not the weight preparation, not the
+bf16 conversion.
+
+What it computes, and where the pages define it:
+
+* ``build_routing`` -- sort the batch so same-adapter requests are adjacent and
+  base requests (slot -1) come last, then group consecutive same-adapter
+  requests into ``(lora_ids, grouped_offsets, end)``, truncating at the first
+  base group ("max.pipelines.lora.LoRAManagerV3" API page, sort_lora_batch and
+  get_lora_graph_inputs).  Plain C in ``lora_oracle.c``.
+* ``lora_scale`` -- scale = lora_alpha / r, or lora_alpha / sqrt(r) for rsLoRA
+  ("vLLM LoRA 实现深度解析" section 1, the rsLoRA variant).
+* ``prep_a`` / ``prep_b`` -- the load-time pipeline of the MAX page ("MAX
+  max.pipelines.lora 模块解析", load pipeline: scale pre-multiplied into B, rank
+  padding [r, in] -> [max_rank, in] and [out, r] -> [out, max_rank], dtype
+  unification).  The scale is multiplied in fp32 and the product is rounded
+  once to the storage type; this is what both pages' code does for fp32 and
+  bf16 weights (numpy fp32 times a Python float; torch bf16 times a Python
+  float computes in fp32 and rounds once).
+* ``fuse_qkv_a`` / ``fuse_qkv_b`` -- QKV fusion: A concatenated on the rank
+  dimension, B on the output dimension (same MAX page, QKV fusion).
+* ``sgmv_rows`` -- the delta y_t += B_s . (A_s . x_t) for LoRA-routed rows,
+  per slice, in double ("vLLM LoRA 实现深度解析" sections 1 and 6).  Plain C.
+
+Storage types: ``"f32"`` arrays are numpy float32; ``"bf16"`` arrays are numpy
+uint16 holding the bfloat16 bit pattern (the upper half of an IEEE binary32).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+OK, BAD_ARG, BAD_SLOT, BAD_ROW, BAD_ROUTE = 0, 1, 2, 3, 4
+
+
+class _Slice(ctypes.Structure):
+    _fields_ = [
+        ("A", ctypes.c_void_p),
+        ("A_slot_stride", ctypes.c_longlong),
+        ("B", ctypes.c_void_p),
+        ("B_slot_stride", ctypes.c_longlong),
+        ("out_dim", ctypes.c_int),
+        ("y_in", ctypes.c_void_p),
+        ("y_in_row_stride", ctypes.c_longlong),
+        ("y_out", ctypes.c_void_p),
+        ("y_out_row_stride", ctypes.c_longlong),
+    ]
+
+
+def lib():
+    """Load (building first if needed) the C oracle."""
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i32p = ctypes.POINTER(ctypes.c_int)
+        L.oracle_build_routing.restype = ctypes.c_int
+        L.oracle_build_routing.argtypes = [ctypes.c_int, i32p, i32p, ctypes.c_int, i32p, i32p, i32p,
+                                           i32p, i32p, i32p]
+        L.oracle_sgmv_rows.restype = ctypes.c_int
+        L.oracle_sgmv_rows.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
+                                       ctypes.c_longlong, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p]
+        _LIB = L
+    return _LIB
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p32(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+# --------------------------------------------------------------------------
+# Storage-type conversions (exact decode; round-to-nearest-even encode)
+# --------------------------------------------------------------------------
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float32 (exact: bf16 is the top half of binary32)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f32_to_bf16_bits(f: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bits, IEEE round-to-nearest, ties to even.
+
+    The discarded low 16 bits are compared with one half of the last kept
+    bit; exact halves round to the even neighbour.  NaNs stay NaN (quiet bit
+    set); infinities and overflow to infinity follow from the same rule.
+    """
+    a = np.ascontiguousarray(np.asarray(f, dtype=np.float32))
+    u = a.view(np.uint32).astype(np.uint64)
+    hi = u >> np.uint64(16)
+    lo = u & np.uint64(0xFFFF)
+    round_up = (lo > 0x8000) | ((lo == 0x8000) & ((hi & np.uint64(1)) == 1))
+    out = (hi + round_up.astype(np.uint64)).astype(np.uint64)
+    nan = np.isnan(a)
+    out = np.where(nan, (hi | np.uint64(0x0040)), out)
+    return out.astype(np.uint16)
+
+
+def to_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact conversion of stored values to double."""
+    if dtype == "bf16":
+        return bf16_bits_to_f32(arr).astype(np.float64)
+    if dtype == "f32":
+        return np.asarray(arr, dtype=np.float32).astype(np.float64)
+    raise ValueError("unknown storage dtype %r" % (dtype,))
+
+
+def from_f32(arr32: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values -> storage type (one RNE rounding for bf16)."""
+    if dtype == "bf16":
+        return f32_to_bf16_bits(arr32)
+    if dtype == "f32":
+        return np.asarray(arr32, dtype=np.float32).copy()
+    raise ValueError("unknown storage dtype %r" % (dtype,))
+
+
+# --------------------------------------------------------------------------
+# Routing
+# --------------------------------------------------------------------------
+
+def build_routing(req_slot, req_len, max_num_loras: int) -> dict:
+    """Sort + group into the routing triple (plain C; see lora_oracle.c)."""
+    L = lib()
+    slots = _i32(req_slot)
+    lens = _i32(req_len)
+    n = int(slots.size)
+    S = int(max_num_loras)
+    perm = np.zeros(max(n, 1), dtype=np.int32)
+    ids = np.zeros(max(S, 1), dtype=np.int32)
+    offs = np.zeros(S + 1, dtype=np.int32)
+    G = ctypes.c_int(0)
+    end = ctypes.c_int(0)
+    T = ctypes.c_int(0)
+    rc = L.oracle_build_routing(n, _p32(slots), _p32(lens), S, _p32(perm), _p32(ids), _p32(offs),
+                                ctypes.byref(G), ctypes.byref(end), ctypes.byref(T))
+    if rc != OK:
+        return {"status": rc}
+    g = G.value
+    return {"status": OK, "perm": perm[:n].copy(), "lora_ids": ids[:g].copy(),
+            "grouped_offsets": offs[:g + 1].copy(), "num_groups": g, "end": end.value,
+            "total_tokens": T.value}
+
+
+# --------------------------------------------------------------------------
+# Load-time preparation (scale folding, rank padding, QKV fusion)
+# --------------------------------------------------------------------------
+
+def lora_scale(lora_alpha: float, r: int, use_rslora: bool) -> np.float32:
+    """alpha / r, or alpha / sqrt(r) for rsLoRA; computed in double, kept as fp32."""
+    if r <= 0:
+        raise ValueError("rank must be positive")
+    s = float(lora_alpha) / (math.sqrt(r) if use_rslora else float(r))
+    return np.float32(s)
+
+
+def prep_a(A_raw: np.ndarray, max_rank: int, dtype: str) -> np.ndarray:
+    """[r, in] fp32 -> [max_rank, in] storage: rows >= r are zero."""
+    A_raw = np.asarray(A_raw, dtype=np.float32)
+    r, k = A_raw.shape
+    if r > max_rank:
+        raise ValueError("adapter rank %d exceeds max_lora_rank %d" % (r, max_rank))
+    out = np.zeros((max_rank, k), dtype=np.float32)
+    out[:r, :] = A_raw
+    return from_f32(out, dtype)
+
+
+def prep_b(B_raw: np.ndarray, max_rank: int, scale: np.float32, dtype: str) -> np.ndarray:
+    """[out, r] fp32 -> scale folded in fp32 -> [out, max_rank] storage (cols >= r zero)."""
+    B_raw = np.asarray(B_raw, dtype=np.float32)
+    d, r = B_raw.shape
+    if r > max_rank:
+        raise ValueError("adapter rank %d exceeds max_lora_rank %d" % (r, max_rank))
+    folded = (B_raw * np.float32(scale)).astype(np.float32)  # fp32 multiply, one rounding
+    out = np.zeros((d, max_rank), dtype=np.float32)
+    out[:, :r] = folded
+    return from_f32(out, dtype)
+
+
+def fuse_qkv_a(a_list):
+    """Concatenate per-projection [R, in] A blocks on the rank dimension -> [n*R, in]."""
+    return np.concatenate(list(a_list), axis=0)
+
+
+def fuse_qkv_b(b_list):
+    """Concatenate per-projection [out_j, R] B blocks on the output dimension -> [O, R]."""
+    return np.concatenate(list(b_list), axis=0)
+
+
+def lora_memory_bytes(num_lora_layers: int, in_features: int, out_features: int, rank: int,
+                      dtype_bytes: int, max_loras: int) -> int:
+    """GPU memory of the stacked A/B buffers ("vLLM LoRA 实现深度解析" section 9 formula)."""
+    return num_lora_layers * (in_features * rank + out_features * rank) * dtype_bytes * max_loras
+
+
+# --------------------------------------------------------------------------
+# The delta
+# --------------------------------------------------------------------------
+
+def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim: int, R: int,
+              max_num_loras: int):
+    """Delta for the listed rows, in double.
+
+    rows           int array, batch row index of each listed row (< end)
+    x_rows         float64 [n_rows, in_dim], the listed rows of x
+    slices         list of dicts, one per projection slice:
+                     A  float64 [S, >= R rows, in_dim] stack, or a flat view with
+                        "A_slot_stride" (elements); rank row k of slot s at
+                        A[s*A_slot_stride + k*in_dim : +in_dim]
+                     B  float64 stack; element (s, o, k) at B[s*B_slot_stride + o*R + k]
+                     out_dim, y_in float64 [n_rows, out_dim] (listed rows)
+    Returns (u [n_rows, n*R] float64, [y_out_j [n_rows, out_j] float64]).
+    """
+    L = lib()
+    rows = _i32(rows)
+    n = int(rows.size)
+    x_rows = np.ascontiguousarray(x_rows, dtype=np.float64)
+    assert x_rows.shape == (n, in_dim)
+    ns = len(slices)
+    keep = []
+    arr = (_Slice * ns)()
+    outs = []
+    for j, sl in enumerate(slices):
+        A = np.ascontiguousarray(sl["A"], dtype=np.float64)
+        B = np.ascontiguousarray(sl["B"], dtype=np.float64)
+        yi = np.ascontiguousarray(sl["y_in"], dtype=np.float64)
+        od = int(sl["out_dim"])
+        assert yi.shape == (n, od)
+        yo = np.empty((n, od), dtype=np.float64)
+        keep += [A, B, yi, yo]
+        base_a = A.ctypes.data + 8 * int(sl.get("A_offset", 0))
+        base_b = B.ctypes.data + 8 * int(sl.get("B_offset", 0))
+        arr[j] = _Slice(base_a, int(sl["A_slot_stride"]), base_b, int(sl["B_slot_stride"]), od,
+                        yi.ctypes.data, od, yo.ctypes.data, od)
+        outs.append(yo)
+    ids = _i32(lora_ids)
+    offs = _i32(grouped_offsets)
+    G = int(ids.size)
+    assert offs.size == G + 1 or (G == 0 and offs.size >= 1)
+    u = np.empty((n, ns * R), dtype=np.float64)
+    rc = L.oracle_sgmv_rows(n, _p32(rows), int(in_dim), int(R), int(max_num_loras), ns, arr,
+                            x_rows.ctypes.data, int(in_dim), _p32(ids), _p32(offs), G, int(end),
+                            u.ctypes.data)
+    if rc != OK:
+        raise ValueError("oracle_sgmv_rows failed with code %d" % rc)
+    return u, outs
+
+
+def problem_rows(prob, rows):
+    """Run ``sgmv_rows`` on a prepared problem (see ``prepare_problem``) for the given rows."""
+    rows = _i32(rows)
+    dt = prob["dtype"]
+    x_rows = to_f64(prob["x"][rows], dt)
+    slices = []
+    for sl in prob["slices"]:
+        d = dict(sl)
+        d["y_in"] = to_f64(sl["y"][rows][:, sl["y_col0"]:sl["y_col0"] + sl["out_dim"]], dt)
+        slices.append(d)
+    return sgmv_rows(rows, x_rows, slices, prob["lora_ids"], prob["grouped_offsets"], prob["end"],
+                     prob["in_dim"], prob["R"], prob["S"])
+
+
+def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
+    """Oracle-side preparation of one projection problem from raw synthetic inputs.
+
+    ``raw`` is a workload drawn by ``workloads.synthetic`` (raw fp32 adapter
+    matrices per slot and projection, ranks, alphas, rsLoRA flags, request
+    list, x and y in storage type).  ``proj`` is "qkv" or "o".  Returns the
+    routing (oracle's own), the stacked storage buffers and fp64 views.
+    """
+    dt = raw["dtype"]
+    S, R = raw["max_num_loras"], raw["max_lora_rank"]
+    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    route = build_routing(raw["req_slot"], raw["req_len"], S)
+    in_dim = raw["x_" + proj].shape[1]
+    outs = [raw["out_dims"][nm] for nm in names]
+    stacks_a, stacks_b = [], []
+    for nm in names:
+        a_s, b_s = [], []
+        for s in range(S):
+            r = int(raw["rank"][s])
+            sc = lora_scale(raw["alpha"][s], r, bool(raw["rslora"][s]))
+            a_s.append(prep_a(raw["A"][nm][s], R, dt))
+            b_s.append(prep_b(raw["B"][nm][s], R, sc, dt))
+        stacks_a.append(np.stack(a_s))
+        stacks_b.append(np.stack(b_s))
+    slices = []
+    y = raw["y_" + proj]
+    if fused and len(names) > 1:
+        A_st = np.stack([fuse_qkv_a([stacks_a[j][s] for j in range(len(names))]) for s in range(S)])
+        B_st = np.stack([fuse_qkv_b([stacks_b[j][s] for j in range(len(names))]) for s in range(S)])
+        A64, B64 = to_f64(A_st, dt), to_f64(B_st, dt)
+        O = sum(outs)
+        off = 0
+        for j, od in enumerate(outs):
+            slices.append({"A": A64, "A_offset": j * R * in_dim, "A_slot_stride": len(names) * R * in_dim,
+                           "B": B64, "B_offset": off * R, "B_slot_stride": O * R, "out_dim": od,
+                           "y": y, "y_col0": off})
+            off += od
+        stored = {"A": A_st, "B": B_st}
+    else:
+        off = 0
+        for j, od in enumerate(outs):
+            slices.append({"A": to_f64(stacks_a[j], dt), "A_offset": 0, "A_slot_stride": R * in_dim,
+                           "B": to_f64(stacks_b[j], dt), "B_offset": 0, "B_slot_stride": od * R,
+                           "out_dim": od, "y": y, "y_col0": off})
+            off += od
+        stored = {"A": stacks_a, "B": stacks_b}
+    return {"dtype": dt, "S": S, "R": R, "in_dim": in_dim, "x": raw["x_" + proj], "slices": slices,
+            "lora_ids": route["lora_ids"], "grouped_offsets": route["grouped_offsets"],
+            "end": route["end"], "route": route, "stored": stored, "out_dims": outs}

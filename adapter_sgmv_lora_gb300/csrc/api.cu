@@ -1,0 +1,201 @@
+// api.cu -- the extern "C" entry points of liblora_sgmv.so: argument
+// validation, problem descriptors, kernel dispatch and the device status word.
+// The routing builder (lora_build_routing) lives in routing.cpp.
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace lora {
+
+// Device status word: an OR of LORA_DEV_* flags raised by the kernels.
+__device__ unsigned g_status_word;
+
+namespace {
+
+unsigned* status_ptr() {
+  static unsigned* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+lora_status_t validate_problem(const lora_problem_t* p) {
+  if (!p) return LORA_ERR_NULL;
+  if (p->dtype != LORA_DTYPE_F32 && p->dtype != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (p->num_tokens < 0 || p->in_dim < 1 || p->max_num_loras < 1 || p->max_lora_rank < 1 ||
+      p->max_lora_rank > 1024)
+    return LORA_ERR_SHAPE;
+  if (p->num_slices < 1 || p->num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
+  if (!p->x) return LORA_ERR_NULL;
+  if (p->x_row_stride < p->in_dim) return LORA_ERR_SHAPE;
+  const long long R = p->max_lora_rank;
+  for (int j = 0; j < p->num_slices; ++j) {
+    const lora_slice_t& s = p->slices[j];
+    if (!s.A || !s.B || !s.y) return LORA_ERR_NULL;
+    if (s.out_dim < 1) return LORA_ERR_SHAPE;
+    if (s.A_slot_stride < R * p->in_dim) return LORA_ERR_SHAPE;
+    if (s.B_slot_stride < R * s.out_dim) return LORA_ERR_SHAPE;
+    if (s.y_row_stride < s.out_dim) return LORA_ERR_SHAPE;
+  }
+  return LORA_OK;
+}
+
+lora_status_t validate_routing(const lora_problem_t* p, const lora_routing_t* r) {
+  if (!r) return LORA_ERR_NULL;
+  if (r->num_groups < 0 || r->num_groups > p->max_num_loras) return LORA_ERR_ROUTING;
+  if (r->end < 0 || r->end > p->num_tokens) return LORA_ERR_ROUTING;
+  if (r->num_groups == 0 && r->end != 0) return LORA_ERR_ROUTING;
+  if (r->num_groups > 0 && (!r->lora_ids || !r->grouped_offsets)) return LORA_ERR_NULL;
+  return LORA_OK;
+}
+
+ProblemDesc make_desc(const lora_problem_t* p, const lora_routing_t* r) {
+  ProblemDesc d{};
+  d.dtype = p->dtype;
+  d.num_tokens = p->num_tokens;
+  d.in_dim = p->in_dim;
+  d.S = p->max_num_loras;
+  d.R = p->max_lora_rank;
+  d.n_slices = p->num_slices;
+  d.x = p->x;
+  d.x_row_stride = p->x_row_stride;
+  for (int j = 0; j < p->num_slices; ++j) {
+    const lora_slice_t& s = p->slices[j];
+    d.sl[j] = SliceDesc{s.A, (long long)s.A_slot_stride, s.B, (long long)s.B_slot_stride,
+                        s.out_dim, s.y, (long long)s.y_row_stride};
+  }
+  if (r) {
+    d.lora_ids = r->lora_ids;
+    d.offs = r->grouped_offsets;
+    d.G = r->num_groups;
+    d.end = r->end;
+  }
+  d.status = status_ptr();
+  return d;
+}
+
+lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+bool is_noop(const lora_routing_t* r) { return r->num_groups == 0 || r->end == 0; }
+
+size_t ws_bytes(const lora_problem_t* p, int32_t end) {
+  const size_t raw = (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices * (size_t)p->max_lora_rank * 4;
+  return (raw + 255) & ~(size_t)255;
+}
+
+}  // namespace
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" lora_status_t lora_set_slot(const lora_problem_t* problem, int32_t slice, int32_t slot,
+                                       int32_t r, double lora_alpha, int32_t use_rslora,
+                                       const void* A_raw, const void* B_raw,
+                                       lora_dtype_t raw_dtype, lora_stream_t stream) {
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if (slice < 0 || slice >= problem->num_slices) return LORA_ERR_SHAPE;
+  if (slot < 0 || slot >= problem->max_num_loras) return LORA_ERR_SLOT_RANGE;
+  if (r < 0 || r > problem->max_lora_rank) return LORA_ERR_RANK;
+  if (raw_dtype != LORA_DTYPE_F32 && raw_dtype != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (r > 0 && (!A_raw || !B_raw)) return LORA_ERR_NULL;
+  float scale = 0.f;
+  if (r > 0) {
+    const double denom = use_rslora ? std::sqrt((double)r) : (double)r;
+    scale = (float)(lora_alpha / denom);
+  }
+  ProblemDesc d = make_desc(problem, nullptr);
+  return cuda_status(launch_set_slot(d, slice, slot, r, scale, A_raw, B_raw, raw_dtype,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" lora_status_t lora_shrink(const lora_problem_t* problem, const lora_routing_t* routing,
+                                     float* u, lora_stream_t stream) {
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
+  if (is_noop(routing)) return LORA_OK;
+  if (!u) return LORA_ERR_NULL;
+  ProblemDesc d = make_desc(problem, routing);
+  if (!d.status) return LORA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fast_path_ok(d, u)) return cuda_status(launch_shrink_bf16(d, u, s));
+  return cuda_status(launch_shrink_simple(d, u, s));
+}
+
+extern "C" lora_status_t lora_expand(const lora_problem_t* problem, const lora_routing_t* routing,
+                                     const float* u, lora_stream_t stream) {
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
+  if (is_noop(routing)) return LORA_OK;
+  if (!u) return LORA_ERR_NULL;
+  ProblemDesc d = make_desc(problem, routing);
+  if (!d.status) return LORA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fast_path_ok(d, u)) return cuda_status(launch_expand_bf16(d, u, s, false));
+  return cuda_status(launch_expand_simple(d, u, s, false));
+}
+
+extern "C" size_t lora_workspace_bytes(const lora_problem_t* problem, int32_t end) {
+  if (!problem || problem->num_slices < 1 || problem->max_lora_rank < 1) return 0;
+  return ws_bytes(problem, end);
+}
+
+extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_t* routing,
+                                         void* workspace, size_t workspace_bytes,
+                                         lora_stream_t stream) {
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
+  if (is_noop(routing)) return LORA_OK;
+  if (!workspace || workspace_bytes < ws_bytes(problem, routing->end)) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return LORA_ERR_ALIGN;
+  ProblemDesc d = make_desc(problem, routing);
+  if (!d.status) return LORA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* u = static_cast<float*>(workspace);
+  if (fast_path_ok(d, u)) {
+    if ((st = cuda_status(launch_shrink_bf16(d, u, s))) != LORA_OK) return st;
+    return cuda_status(launch_expand_bf16(d, u, s, true));
+  }
+  if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
+  return cuda_status(launch_expand_simple(d, u, s, true));
+}
+
+extern "C" lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* flags) {
+  if (!flags) return LORA_ERR_NULL;
+  unsigned* p = status_ptr();
+  if (!p) return LORA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return LORA_ERR_CUDA;
+  *flags = v;
+  return LORA_OK;
+}
+
+extern "C" const char* lora_status_string(lora_status_t status) {
+  switch (status) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_NULL: return "LORA_ERR_NULL: a required pointer is NULL";
+    case LORA_ERR_SHAPE: return "LORA_ERR_SHAPE: a count, size or stride is out of range";
+    case LORA_ERR_RANK: return "LORA_ERR_RANK: adapter rank exceeds max_lora_rank";
+    case LORA_ERR_SLOT_RANGE: return "LORA_ERR_SLOT_RANGE: slot id out of range";
+    case LORA_ERR_ROUTING: return "LORA_ERR_ROUTING: routing triple inconsistent";
+    case LORA_ERR_DTYPE: return "LORA_ERR_DTYPE: unknown storage type";
+    case LORA_ERR_ALIGN: return "LORA_ERR_ALIGN: pointer or stride misaligned";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing or too small";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA: a CUDA call failed";
+    case LORA_ERR_DEVICE_CHECK: return "LORA_ERR_DEVICE_CHECK: device-side routing check failed";
+  }
+  return "unknown lora_status_t";
+}

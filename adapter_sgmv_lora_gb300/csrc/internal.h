@@ -1,0 +1,56 @@
+// internal.h -- descriptors and launcher declarations shared by the
+// library's translation units (not part of the public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/lora_sgmv.h"
+
+namespace lora {
+
+// One slice, as the kernels see it (same meaning as lora_slice_t).
+struct SliceDesc {
+  const void* A;
+  long long A_slot_stride;
+  const void* B;
+  long long B_slot_stride;
+  int out_dim;
+  void* y;
+  long long y_row_stride;
+};
+
+// A validated problem plus its routing, passed by value to every kernel.
+struct ProblemDesc {
+  int dtype;  // lora_dtype_t
+  int num_tokens;
+  int in_dim;
+  int S;  // max_num_loras
+  int R;  // max_lora_rank
+  int n_slices;
+  const void* x;
+  long long x_row_stride;
+  SliceDesc sl[LORA_MAX_SLICES];
+  const int* lora_ids;  // device [G]
+  const int* offs;      // device [G + 1]
+  int G;
+  int end;
+  unsigned* status;  // device status word (LORA_DEV_* flags)
+};
+
+// Token rows per tile of the bf16 SGMV kernels.
+constexpr int kTileRows = 64;
+
+// Host launchers (return a cudaError_t from the launch).
+cudaError_t launch_shrink_simple(const ProblemDesc& p, float* u, cudaStream_t s);
+cudaError_t launch_expand_simple(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl);
+cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, float scale,
+                            const void* A_raw, const void* B_raw, int raw_dtype, cudaStream_t s);
+
+// bf16 fast path (tensor cores + bulk copies + clusters).  `fast_path_ok`
+// tells whether a problem meets its alignment / size preconditions.
+bool fast_path_ok(const ProblemDesc& p, const void* u);
+cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
+cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl);
+
+}  // namespace lora

@@ -1,0 +1,507 @@
+// sgmv_bf16.cu -- bf16 SGMV shrink and boundary-aware expand for sm_103a.
+//
+// Shrink  u[t, j*R+k] = sum_i A_j[s, k, i] x[t, i]       (rank-R intermediate)
+// Expand  y_j[t, o]   = rn(y_j[t, o] + sum_k B_j[s, o, k] u[t, j*R+k])
+// for every routed row t < end of group g with slot s = lora_ids[g]
+// ("vLLM LoRA 实现深度解析" sections 1 and 6; routing triple of the
+// "max.pipelines.lora.LoRAManagerV3" page, get_lora_graph_inputs).
+//
+// Work decomposition.  The routed rows are cut into 64-row tiles per group
+// (tiles.cuh).  The shrink gives each (tile, rank-column block) to a
+// thread-block cluster of C CTAs that split the input dimension; every CTA
+// streams its K range of the tile's x rows and of the slot's A rows into
+// shared memory with bulk (TMA engine) copies, one copy per row segment so
+// that no byte outside the group is fetched, and multiplies on the tensor
+// cores (mma.sync m16n8k16, fp32 accumulate).  The C partial tiles are summed
+// through distributed shared memory in a fixed order (deterministic) and
+// written once to u.  The expand gives each (tile, slice, 2R..256-column
+// output block) to one CTA: it loads the y block and the slot's B block, then
+// waits (programmatic dependent launch) for the shrink grid, loads u, splits
+// it into hi + lo bf16 terms, multiplies with the y block as the initial
+// accumulator, rounds once and bulk-stores exactly the routed rows back.
+// Rows at or past `end` are never read or written.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tiles.cuh"
+
+namespace lora {
+
+namespace {
+
+constexpr int MT = kTileRows;       // token rows per tile
+constexpr int KS = 64;              // input elements per shrink stage
+constexpr int XPITCH = KS * 2 + 16; // bytes per staged row (padding: conflict-free ldmatrix)
+constexpr int NSTAGE = 4;           // shrink pipeline depth
+
+template <int NB>
+struct ShrinkCfg {
+  static constexpr int STAGE_BYTES = (MT + NB) * XPITCH;
+  static constexpr int PPITCH = NB + 4;  // floats per partial row
+  static constexpr int SMEM = NSTAGE * STAGE_BYTES;
+  static_assert(MT * PPITCH * 4 <= SMEM, "partial tile must fit in the stage ring");
+};
+
+__device__ __forceinline__ void record(const ProblemDesc& p, unsigned flag) { atomicOr(p.status, flag); }
+
+}  // namespace
+
+// grid.x = C * nblk * n_tiles_max, cluster (C,1,1) when C > 1.
+template <int NB>
+__global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_constant__ ProblemDesc p,
+                                                               float* __restrict__ u, int C,
+                                                               int nblk, int Kc) {
+  using Cfg = ShrinkCfg<NB>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[NSTAGE];
+  __shared__ Tile s_tile;
+  __shared__ int s_ok;
+
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = (int)(blockIdx.x % (unsigned)C);
+  const int rest = (int)(blockIdx.x / (unsigned)C);
+  const int nb = rest % nblk;
+  const long long tile = rest / nblk;
+
+  if (warp == 0) {
+    Tile t{};
+    const bool ok = warp_locate_tile(p, MT, tile, t);
+    if (lane == 0) {
+      s_tile = t;
+      s_ok = ok;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!s_ok) return;  // the whole cluster sees the same tile and verdict
+  const Tile t = s_tile;
+
+  const int R = p.R;
+  const int nR = p.n_slices * R;
+  const int n0 = nb * NB;
+  const int nvalid = min(NB, nR - n0);
+  const int k0 = crank * Kc;
+  const int nst = Kc / KS;
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+
+  auto issue = [&](int s) {
+    const int slot = s % NSTAGE;
+    uint8_t* xs = smem + slot * Cfg::STAGE_BYTES;
+    uint8_t* as = xs + MT * XPITCH;
+    const long long kk = (long long)k0 + (long long)s * KS;
+    if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(t.rows + nvalid) * (KS * 2));
+    __syncwarp();
+    for (int r = lane; r < t.rows; r += 32)
+      bulk_g2s(xs + r * XPITCH, xg + (long long)(t.row0 + r) * p.x_row_stride + kk, KS * 2, &full[slot]);
+    for (int n = lane; n < nvalid; n += 32) {
+      const int col = n0 + n;
+      const int j = col / R, k = col - (col / R) * R;
+      const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(p.sl[j].A) +
+                               (long long)t.slot * p.sl[j].A_slot_stride + (long long)k * p.in_dim + kk;
+      bulk_g2s(as + n * XPITCH, a, KS * 2, &full[slot]);
+    }
+  };
+
+  if (warp == 0)
+    for (int s = 0; s < min(NSTAGE, nst); ++s) issue(s);
+
+  float acc[NB / 8][4];
+#pragma unroll
+  for (int i = 0; i < NB / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  const bool active = warp * 16 < t.rows;  // warp-uniform: this warp's 16 rows hold data
+  bool timed_out = false;
+  for (int s = 0; s < nst; ++s) {
+    const int slot = s % NSTAGE;
+    if (!timed_out && !mbar_wait(&full[slot], (uint32_t)((s / NSTAGE) & 1))) timed_out = true;
+    if (active && !timed_out) {
+      const uint32_t xs = smem_addr(smem + slot * Cfg::STAGE_BYTES);
+      const uint32_t as = xs + MT * XPITCH;
+#pragma unroll
+      for (int ks = 0; ks < KS / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(xs + (warp * 16 + (lane & 15)) * XPITCH + (ks * 16 + (lane >> 4) * 8) * 2, a[0], a[1],
+                a[2], a[3]);
+#pragma unroll
+        for (int np = 0; np < NB / 16; ++np) {
+          uint32_t b0, b1, b2, b3;
+          const int nrow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int kcol = ks * 16 + ((lane >> 3) & 1) * 8;
+          ldsm_x4(as + nrow * XPITCH + kcol * 2, b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * np], a, b0, b1);
+          mma_bf16_16816(acc[2 * np + 1], a, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+    if (warp == 0 && s + NSTAGE < nst && !timed_out) issue(s + NSTAGE);
+  }
+  if (timed_out) {
+    record(p, LORA_DEV_TIMEOUT);
+    // Give outstanding copies a bounded chance to land before smem is reused.
+    for (int s = 0; s < min(NSTAGE, nst); ++s) (void)mbar_wait(&full[s], 0);
+  }
+
+  // Partial tile -> shared memory (reuses the stage ring: every copy landed).
+  float* P = reinterpret_cast<float*>(smem);
+  if (active) {
+    const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NB / 8; ++nt) {
+      const int row = warp * 16 + g, col = nt * 8 + 2 * tq;
+      P[row * Cfg::PPITCH + col] = acc[nt][0];
+      P[row * Cfg::PPITCH + col + 1] = acc[nt][1];
+      P[(row + 8) * Cfg::PPITCH + col] = acc[nt][2];
+      P[(row + 8) * Cfg::PPITCH + col + 1] = acc[nt][3];
+    }
+  }
+  if (C > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+
+  // Each CTA of the cluster sums its share of rows over all C partials, in
+  // rank order, and writes them to u.
+  const int rpc = MT / C;
+  const int r_lo = crank * rpc;
+  const int r_hi = min(r_lo + rpc, t.rows);
+  const int cnt = (r_hi - r_lo) * nvalid;
+  for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+    const int r = r_lo + e / nvalid, c = e % nvalid;
+    float v;
+    if (C == 1) {
+      v = P[r * Cfg::PPITCH + c];
+    } else {
+      const uint32_t la = smem_addr(&P[r * Cfg::PPITCH + c]);
+      v = 0.f;
+      for (int q = 0; q < C; ++q) v += ld_shared_cluster_f32(map_shared_rank(la, (uint32_t)q));
+    }
+    u[(long long)(t.row0 + r) * nR + n0 + c] = v;
+  }
+  if (C > 1) cluster_sync();  // keep this CTA's partial alive for its peers
+}
+
+// ------------------------------------------------------------------ expand
+
+template <int R, int OB>
+struct ExpandCfg {
+  static constexpr int YPITCH = OB * 2 + 16;  // bytes per staged y row
+  static constexpr int UPITCH = 4 * R + 16;   // bytes per hi|lo row (2R bf16)
+  static constexpr int Y_OFF = 0;
+  static constexpr int B_OFF = MT * YPITCH;
+  static constexpr int U_OFF = B_OFF + OB * R * 2;
+  static constexpr int H_OFF = U_OFF + MT * R * 4;
+  static constexpr int SMEM = H_OFF + MT * UPITCH;
+};
+
+struct ExpandMap {
+  int n_ob_total;                   // output blocks per tile, all slices
+  int ob_begin[LORA_MAX_SLICES + 1];  // first output block of each slice
+};
+
+template <int R, int OB>
+__global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
+                                                               const float* __restrict__ u,
+                                                               const ExpandMap map) {
+  using Cfg = ExpandCfg<R, OB>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar_yb, bar_u;
+  __shared__ Tile s_tile;
+  __shared__ int s_ok;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long tile = blockIdx.x / (unsigned)map.n_ob_total;
+  const int obg = (int)(blockIdx.x % (unsigned)map.n_ob_total);
+  int j = 0;
+  while (j + 1 < p.n_slices && obg >= map.ob_begin[j + 1]) ++j;
+  const int o0 = (obg - map.ob_begin[j]) * OB;
+  const SliceDesc& sl = p.sl[j];
+  const int ovalid = min(OB, sl.out_dim - o0);
+  const int nR = p.n_slices * R;
+
+  if (warp == 0) {
+    Tile t{};
+    const bool ok = warp_locate_tile(p, MT, tile, t);
+    if (lane == 0) {
+      s_tile = t;
+      s_ok = ok;
+    }
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_yb, 1);
+    mbar_init(&bar_u, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!s_ok) {
+    pdl_wait();
+    return;
+  }
+  const Tile t = s_tile;
+
+  uint8_t* Ys = smem + Cfg::Y_OFF;
+  uint8_t* Bs = smem + Cfg::B_OFF;
+  float* Us = reinterpret_cast<float*>(smem + Cfg::U_OFF);
+  uint8_t* Hs = smem + Cfg::H_OFF;
+  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(sl.y);
+
+  // y block and B block do not depend on the shrink: fetch them first.
+  if (warp == 0) {
+    if (lane == 0)
+      mbar_arrive_expect_tx(&bar_yb, (uint32_t)t.rows * ovalid * 2 + (uint32_t)ovalid * R * 2);
+    __syncwarp();
+    if (lane == 0)
+      bulk_g2s(Bs,
+               static_cast<const __nv_bfloat16*>(sl.B) + (long long)t.slot * sl.B_slot_stride +
+                   (long long)o0 * R,
+               (uint32_t)ovalid * R * 2, &bar_yb);
+    for (int r = lane; r < t.rows; r += 32)
+      bulk_g2s(Ys + r * Cfg::YPITCH, yg + (long long)(t.row0 + r) * sl.y_row_stride + o0,
+               (uint32_t)ovalid * 2, &bar_yb);
+  }
+
+  pdl_wait();  // the shrink grid (if any) has finished and its u is visible
+
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(&bar_u, (uint32_t)t.rows * R * 4);
+    __syncwarp();
+    for (int r = lane; r < t.rows; r += 32)
+      bulk_g2s(Us + r * R, u + (long long)(t.row0 + r) * nR + (long long)j * R, R * 4, &bar_u);
+  }
+  bool ok = mbar_wait(&bar_u, 0);
+  // u -> hi + lo bf16 (u = hi + lo to 16 significant bits; the subtraction is exact).
+  if (ok) {
+    for (int e = threadIdx.x; e < t.rows * R; e += blockDim.x) {
+      const int r = e / R, k = e % R;
+      const float v = Us[r * R + k];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
+      hrow[k] = hi;
+      hrow[R + k] = lo;
+    }
+  }
+  ok = mbar_wait(&bar_yb, 0) && ok;
+  __syncthreads();
+  const int any_fail = __syncthreads_or(!ok);
+  if (any_fail) {
+    if (threadIdx.x == 0) record(p, LORA_DEV_TIMEOUT);
+    (void)mbar_wait(&bar_yb, 0);
+    (void)mbar_wait(&bar_u, 0);
+    return;
+  }
+
+  const int m = warp & 3, nh = warp >> 2;
+  constexpr int NT = OB / 16;  // n8 tiles per warp
+  const int g = lane >> 2, tq = lane & 3;
+  const bool active = m * 16 < t.rows;
+  if (active) {
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = nh * (OB / 2) + nt * 8 + 2 * tq;
+      const __nv_bfloat162 v0 =
+          *reinterpret_cast<const __nv_bfloat162*>(Ys + (m * 16 + g) * Cfg::YPITCH + col * 2);
+      const __nv_bfloat162 v1 =
+          *reinterpret_cast<const __nv_bfloat162*>(Ys + (m * 16 + g + 8) * Cfg::YPITCH + col * 2);
+      acc[nt][0] = __low2float(v0);
+      acc[nt][1] = __high2float(v0);
+      acc[nt][2] = __low2float(v1);
+      acc[nt][3] = __high2float(v1);
+    }
+    const uint32_t hs = smem_addr(Hs), bs = smem_addr(Bs);
+#pragma unroll
+    for (int kk = 0; kk < (2 * R) / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(hs + (m * 16 + (lane & 15)) * Cfg::UPITCH + (kk * 16 + (lane >> 4) * 8) * 2, a[0], a[1],
+              a[2], a[3]);
+      const int kb = (kk * 16) % R;
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        const int nrow = nh * (OB / 2) + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int kcol = kb + ((lane >> 3) & 1) * 8;
+        ldsm_x4(bs + nrow * (R * 2) + kcol * 2, b0, b1, b2, b3);
+        mma_bf16_16816(acc[2 * np], a, b0, b1);
+        mma_bf16_16816(acc[2 * np + 1], a, b2, b3);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = nh * (OB / 2) + nt * 8 + 2 * tq;
+      *reinterpret_cast<__nv_bfloat162*>(Ys + (m * 16 + g) * Cfg::YPITCH + col * 2) =
+          __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<__nv_bfloat162*>(Ys + (m * 16 + g + 8) * Cfg::YPITCH + col * 2) =
+          __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 0) {
+    for (int r = lane; r < t.rows; r += 32)
+      bulk_s2g(yg + (long long)(t.row0 + r) * sl.y_row_stride + o0, Ys + r * Cfg::YPITCH,
+               (uint32_t)ovalid * 2);
+    bulk_commit();
+    bulk_wait_all();
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pick_nb(int nR, int* nblk) {
+  static const int choices[] = {16, 32, 48, 64, 96, 128};
+  const int nb_count = (nR + 127) / 128;
+  const int need = (nR + nb_count - 1) / nb_count;
+  for (int c : choices)
+    if (c >= need) {
+      *nblk = (nR + c - 1) / c;
+      return c;
+    }
+  *nblk = nb_count;
+  return 128;
+}
+
+std::mutex g_attr_mu;
+
+// Raise a kernel's dynamic shared-memory limit once per device.  `done` is
+// the caller's per-instantiation bitmask of devices already configured.
+template <typename K>
+cudaError_t ensure_smem(K kernel, int bytes, unsigned long long* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (*done & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) *done |= bit;
+  return e;
+}
+
+int num_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 152;
+  }
+  return sms[dev];
+}
+
+template <int NB>
+cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk) {
+  auto kernel = sgmv_shrink_bf16_kernel<NB>;
+  const int smem = ShrinkCfg<NB>::SMEM;
+  static unsigned long long done = 0;
+  cudaError_t e = ensure_smem(kernel, smem, &done);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)p.G + p.end / MT;
+  // Split the input dimension over a cluster until the grid covers the GPU.
+  const int ksteps = p.in_dim / KS;
+  int C = 1;
+  const long long target = 2LL * num_sms();
+  while (C < 8 && tiles * nblk * C * 2 <= target && ksteps % (C * 2) == 0) C *= 2;
+  const int Kc = p.in_dim / C;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * nblk * C));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (C > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc);
+}
+
+template <int R, int OB>
+cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl) {
+  auto kernel = sgmv_expand_bf16_kernel<R, OB>;
+  const int smem = ExpandCfg<R, OB>::SMEM;
+  static unsigned long long done = 0;
+  cudaError_t e = ensure_smem(kernel, smem, &done);
+  if (e != cudaSuccess) return e;
+  ExpandMap map{};
+  int acc = 0;
+  for (int j = 0; j < p.n_slices; ++j) {
+    map.ob_begin[j] = acc;
+    acc += (p.sl[j].out_dim + OB - 1) / OB;
+  }
+  map.ob_begin[p.n_slices] = acc;
+  map.n_ob_total = acc;
+  const long long tiles = (long long)p.G + p.end / MT;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * acc));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, p, u, map);
+}
+
+}  // namespace
+
+bool fast_path_ok(const ProblemDesc& p, const void* u) {
+  if (p.dtype != LORA_DTYPE_BF16) return false;
+  if (p.R != 16 && p.R != 32 && p.R != 64 && p.R != 128) return false;
+  if (p.in_dim % KS != 0) return false;
+  if (!aligned16(p.x) || p.x_row_stride % 8 != 0) return false;
+  if (u && !aligned16(u)) return false;
+  for (int j = 0; j < p.n_slices; ++j) {
+    const SliceDesc& sl = p.sl[j];
+    if (!aligned16(sl.A) || !aligned16(sl.B) || !aligned16(sl.y)) return false;
+    if (sl.A_slot_stride % 8 != 0 || sl.B_slot_stride % 8 != 0) return false;
+    if (sl.out_dim % 8 != 0 || sl.y_row_stride % 8 != 0) return false;
+  }
+  return true;
+}
+
+cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s) {
+  int nblk = 1;
+  const int nb = pick_nb(p.n_slices * p.R, &nblk);
+  switch (nb) {
+    case 16: return launch_shrink_nb<16>(p, u, s, nblk);
+    case 32: return launch_shrink_nb<32>(p, u, s, nblk);
+    case 48: return launch_shrink_nb<48>(p, u, s, nblk);
+    case 64: return launch_shrink_nb<64>(p, u, s, nblk);
+    case 96: return launch_shrink_nb<96>(p, u, s, nblk);
+    default: return launch_shrink_nb<128>(p, u, s, nblk);
+  }
+}
+
+cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl) {
+  switch (p.R) {
+    case 16: return launch_expand_r<16, 256>(p, u, s, pdl);
+    case 32: return launch_expand_r<32, 256>(p, u, s, pdl);
+    case 64: return launch_expand_r<64, 128>(p, u, s, pdl);
+    default: return launch_expand_r<128, 64>(p, u, s, pdl);
+  }
+}
+
+}  // namespace lora

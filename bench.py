@@ -1,0 +1,493 @@
+"""SGMV LoRA benchmark: LoRA-routed tokens/s and HBM GB/s vs roofline.
+
+One step = one batch through the whole path: routing (sort + group, built
+per batch on the host), then the SGMV delta on the fused q/k/v projection and
+on o_proj (shrink + boundary-aware expand each).  The default workload is the
+Llama-3-8B-shaped decode batch: hidden 4096, 32 heads, 8 KV heads, head_dim
+128 (fused qkv out 6144, o 4096 -> 4096), 8 adapter slots, max rank 16 (ranks
+8/16), 256 one-token requests, 25% base.
+
+value: device-resident inputs (x, y, stacks, routing triple in HBM); K steps
+       replayed from CUDA graphs over NSETS independent input sets (each set is
+       one layer: its own x, y and A/B stacks) whose total footprint exceeds
+       4x L2, so every step streams from HBM.
+e2e:   the same steps through the Python API with host buffers: per step the
+       host routing build, pinned-host -> device copies of x, y and the triple,
+       the two applies and a device -> host read of both y outputs.
+roofline: the fused-qkv apply (shrink + expand, chained with programmatic
+       dependent launch) timed alone with CUDA events over the rotated sets.
+cpu_baseline / --impl reference: the CPU oracle (plain C, double, one thread)
+       on a bounded sample of the same workload.
+
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+     [--workload decode8b|many64|prefill8b|mixed70b]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-routed tokens/sec for SGMV shrink+expand; achieved HBM GB/s vs roofline"
+
+WORKLOAD_DESC = {
+    "decode8b": "decode, Llama-3-8B attention (hidden 4096, 32/8 heads, hd 128; fused qkv 6144 + o 4096), "
+                "8 slots, max rank 16, 256 x 1-token requests, 25% base, bf16",
+    "many64": "many-adapter decode, 8B shapes, 64 slots, rank 16, 1024 x 1-token requests, Zipf(1.1), 10% base, "
+              "per-projection q/k/v + o, bf16",
+    "prefill8b": "ragged prefill, 8B shapes, 4 slots + base, max rank 64, 16 requests of 128-2048 tokens, bf16",
+    "mixed70b": "mixed prefill+decode, Llama-3-70B attention (hidden 8192, 64/8 heads; fused qkv 10240 + o 8192), "
+                "16 slots, max rank 128, 8192 tokens, 20% base, bf16",
+}
+
+
+def _env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(route_host, raw, proj, e=2):
+    """Per-apply algorithmic bytes: routed x rows + touched A/B slots (padded) + y read+write."""
+    E = route_host["end"]
+    touched = len(set(int(s) for s in route_host["lora_ids"]))
+    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    n = len(names)
+    O = sum(raw["out_dims"][nm] for nm in names)
+    R = raw["max_lora_rank"]
+    k = raw["in_dims"][names[0]]
+    return E * k * e + touched * n * R * k * e + touched * O * R * e + 2 * E * O * e
+
+
+def algorithmic_flops(route_host, raw, proj):
+    E = route_host["end"]
+    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    O = sum(raw["out_dims"][nm] for nm in names)
+    R = raw["max_lora_rank"]
+    k = raw["in_dims"][names[0]]
+    return E * (2 * len(names) * R * k + 2 * R * O)
+
+
+class ClockSampler:
+    """nvidia-smi clocks + throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [v.strip() for v in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle --
+
+def oracle_step_sampler(workload, seed, target_s, max_rows=None):
+    """Prepared oracle problems and a callable running the oracle on a sample
+    of routed rows.  Returns (run(rows_per_proj) -> routed rows done, full_rows)."""
+    import oracle
+    from workloads import synthetic as sy
+
+    raw = sy.draw(workload, seed)
+    fused = sy.SPECS[workload].fused_qkv
+    probs = [oracle.prepare_problem(raw, "qkv", fused=fused), oracle.prepare_problem(raw, "o", fused=True)]
+    end = probs[0]["end"]
+    # pre-convert the rows the oracle will read (conversion is not timed)
+    cache = {}
+
+    def run(nrows):
+        rows = np.arange(min(nrows, end), dtype=np.int32)
+        for p in probs:
+            key = (id(p), rows.size)
+            if key not in cache:
+                x_rows = oracle.to_f64(p["x"][rows], p["dtype"])
+                sl = []
+                for s in p["slices"]:
+                    d = dict(s)
+                    d["y_in"] = oracle.to_f64(s["y"][rows][:, s["y_col0"]:s["y_col0"] + s["out_dim"]], p["dtype"])
+                    sl.append(d)
+                cache[key] = (x_rows, sl)
+            x_rows, sl = cache[key]
+            oracle.sgmv_rows(rows, x_rows, sl, p["lora_ids"], p["grouped_offsets"], p["end"], p["in_dim"],
+                             p["R"], p["S"])
+        return rows.size
+
+    return run, end
+
+
+def cpu_baseline(workload, budget_s=12.0):
+    run, end = oracle_step_sampler(workload, 0, budget_s)
+    run(min(end, 8))  # warm (builds the oracle, converts rows)
+    t0 = time.perf_counter()
+    run(min(end, 8))
+    per_row = max((time.perf_counter() - t0) / min(end, 8), 1e-7)
+    nrows = int(max(1, min(end, budget_s / 3 / per_row)))
+    run(nrows)  # convert
+    reps, done, t0 = 0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and reps < 1000:
+        done += run(nrows)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d routed rows of one %s batch (qkv + o), %d repetitions, %.1f s, "
+                      "single-threaded C in double" % (nrows, end, workload, reps, dt)}
+
+
+def run_reference(args):
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return 0
+    run, end = oracle_step_sampler(args.workload, 0, 0)
+    run(min(end, 4))
+    t0 = time.perf_counter()
+    run(min(end, 4))
+    per_row = max((time.perf_counter() - t0) / min(end, 4), 1e-7)
+    steps_total = args.steps + args.warmup
+    nrows = int(max(1, min(end, 150.0 / steps_total / per_row)))
+    run(nrows)
+    for _ in range(args.warmup):
+        run(nrows)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += run(nrows)
+    dt = time.perf_counter() - t0
+    val = done / dt
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload]},
+           "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                            "sample": "%d of %d routed rows per step (qkv + o), single-threaded C in double"
+                                      % (nrows, end)},
+           "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
+
+
+# -------------------------------------------------------------- GPU arm --
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = _env_rank()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev_idx = torch.cuda.current_device()
+    import __graft_entry__ as ge
+    ge.build()
+    import adapter_sgmv_lora_gb300 as lk
+    from workloads import device, synthetic as sy
+
+    spec = sy.SPECS[args.workload]
+    props = torch.cuda.get_device_properties(dev_idx)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20)
+
+    # ---- input sets (one per simulated layer), sized to exceed 4x L2
+    sets = []
+    foot = 0
+    max_sets = args.sets or 64
+    seed0 = 1000 * rank
+    while len(sets) < max_sets:
+        raw = sy.draw(spec, seed0 + len(sets))
+        qkv = device.prepare(raw, "qkv", fused=spec.fused_qkv)
+        o = device.prepare(raw, "o")
+        b = algorithmic_bytes(qkv["route_host"], raw, "qkv") + algorithmic_bytes(o["route_host"], raw, "o")
+        sets.append({"raw": raw, "qkv": qkv, "o": o, "bytes": b, "E": qkv["route_host"]["end"]})
+        foot += b
+        if not args.sets and foot >= 4 * l2 and len(sets) >= 2:
+            break
+    NS = len(sets)
+    for s in sets:
+        s["call_qkv"] = lk.CallBuilder(s["qkv"]["problem"], s["qkv"]["routing"], s["qkv"]["workspace"])
+        s["call_o"] = lk.CallBuilder(s["o"]["problem"], s["o"]["routing"], s["o"]["workspace"])
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step(i, st):
+        s = sets[i % NS]
+        s["call_qkv"].apply(st)
+        s["call_o"].apply(st)
+
+    # ---- CUDA graphs: one over all NS sets, plus one per set for remainders
+    with torch.cuda.stream(stream):
+        for i in range(NS):  # eager warm (first-launch attribute setup)
+            step(i, stream)
+    stream.synchronize()
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for i in range(NS):
+            step(i, torch.cuda.current_stream())
+    g_one = []
+    for i in range(NS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(i, torch.cuda.current_stream())
+        g_one.append(g)
+    g_qkv = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_qkv, stream=stream):
+        for i in range(NS):
+            sets[i]["call_qkv"].apply(torch.cuda.current_stream())
+
+    def run_steps(k, start=0):
+        i = 0
+        while k - i >= NS and (start + i) % NS == 0:
+            g_all.replay()
+            i += NS
+        while i < k:
+            g_one[(start + i) % NS].replay()
+            i += 1
+
+    with torch.cuda.stream(stream):
+        run_steps(max(args.warmup, 3))
+    stream.synchronize()
+
+    # ---- timed region
+    sampler = ClockSampler(dev_idx) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    tokens = sum(sets[i % NS]["E"] for i in range(args.steps))
+    bytes_steps = sum(sets[i % NS]["bytes"] for i in range(args.steps))
+
+    # ---- roofline unit: fused-qkv apply alone, over the rotated sets
+    reps = max(1, (args.steps + NS - 1) // NS)
+    with torch.cuda.stream(stream):
+        g_qkv.replay()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(reps):
+            g_qkv.replay()
+        r1.record(stream)
+    torch.cuda.synchronize()
+    qkv_ms = r0.elapsed_time(r1) / (reps * NS)
+    qkv_bytes = statistics.mean(algorithmic_bytes(s["qkv"]["route_host"], s["raw"], "qkv") for s in sets)
+    clocks = sampler.stop() if sampler else None
+
+    if dist:
+        t = torch.tensor([ms, qkv_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, qkv_ms = float(t[0]), float(t[1])
+        tk = torch.tensor([float(tokens)], device="cuda")
+        dist.all_reduce(tk)
+        tokens = float(tk[0])
+
+    # ---- e2e through the public API with host buffers
+    e2e = run_e2e(args, sets, lk, torch, stream, dist)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = _peaks()
+    achieved = qkv_bytes / (qkv_ms * 1e-3) / 1e9
+    traffic = _profiled_traffic(args.workload)
+    out = {
+        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random adapters, activations and base outputs)",
+        "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload], "input_sets": NS,
+                   "footprint_MB": round(foot / 1e6, 1), "l2_MB": round(l2 / 2 ** 20, 1),
+                   "l2_policy": "inputs larger than L2: %d rotated input sets, %.0f MB > 4x L2" % (NS, foot / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "hbm_GBps_step": round(bytes_steps / (ms * 1e-3) / 1e9, 1),
+                   "routed_tokens_per_step": tokens / args.steps / max(world, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "fused-qkv SGMV apply (shrink + expand, PDL-chained)",
+                     "peak_source": "%s HBM copy bandwidth (MEASURED_PEAKS.json)" % peak_kind
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": int(qkv_bytes), "avg_launch_us": round(qkv_ms * 1e3, 3)},
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def _profiled_traffic(workload):
+    """DRAM bytes per fused-qkv apply from the committed ncu summary, if present."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.json" % workload)
+    if os.path.exists(path):
+        try:
+            return json.load(open(path)).get("dram_bytes_per_qkv_apply")
+        except (OSError, ValueError):
+            return None
+    return None
+
+
+def run_e2e(args, sets, lk, torch, stream, dist):
+    """Host buffers -> device -> apply (qkv, o) -> host, through the Python API."""
+    n = min(len(sets), max(4, min(args.steps, 32)))
+    host = []
+    for s in sets[:n]:
+        raw = s["raw"]
+        h = {}
+        for key in ("x_qkv", "x_o", "y_qkv", "y_o"):
+            arr = np.ascontiguousarray(raw[key]).view(np.int16)
+            t = torch.from_numpy(arr).view(torch.bfloat16).pin_memory()
+            h[key] = t
+        h["out_qkv"] = torch.empty_like(h["y_qkv"]).pin_memory()
+        h["out_o"] = torch.empty_like(h["y_o"]).pin_memory()
+        h["ids"] = torch.empty(raw["max_num_loras"], dtype=torch.int32).pin_memory()
+        h["offs"] = torch.empty(raw["max_num_loras"] + 1, dtype=torch.int32).pin_memory()
+        h["ev"] = torch.cuda.Event()
+        h["ev"].record()
+        host.append(h)
+    h2d = d2h = 0
+
+    def one(i, st):
+        nonlocal h2d, d2h
+        s, h = sets[i], host[i]
+        raw = s["raw"]
+        rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], raw["max_num_loras"])
+        G = rt["num_groups"]
+        h["ev"].synchronize()  # the previous copy out of these pinned buffers has finished
+        h["ids"][:G].copy_(torch.from_numpy(rt["lora_ids"]))
+        h["offs"][:G + 1].copy_(torch.from_numpy(rt["grouped_offsets"]))
+        for proj in ("qkv", "o"):
+            d = s[proj]
+            d["x"].copy_(h["x_" + proj], non_blocking=True)
+            d["y_all"].copy_(h["y_" + proj], non_blocking=True)
+            d["routing"].lora_ids[:G].copy_(h["ids"][:G], non_blocking=True)
+            d["routing"].grouped_offsets[:G + 1].copy_(h["offs"][:G + 1], non_blocking=True)
+            h2d += 2 * h["x_" + proj].numel() + 2 * h["y_" + proj].numel() + 4 * (2 * G + 1)
+            lk.lora_sgmv_apply(d["problem"], lk.Routing(d["routing"].lora_ids, d["routing"].grouped_offsets,
+                                                        G, rt["end"]), d["workspace"], st)
+        for proj in ("qkv", "o"):
+            h["out_" + proj].copy_(s[proj]["y_all"], non_blocking=True)
+            d2h += 2 * h["out_" + proj].numel()
+        h["ev"].record(st)
+        return rt["end"]
+
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            one(i, stream)
+    stream.synchronize()
+    h2d = d2h = 0
+    k = max(args.steps // 4, n)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    toks = 0
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(k):
+            toks += one(i % n, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+        tk = torch.tensor([float(toks)], device="cuda")
+        dist.all_reduce(tk)
+        toks = float(tk[0])
+    return {"value": toks / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d // k,
+            "d2h_bytes_per_step": d2h // k, "steps": k,
+            "note": "per step: host routing build, pinned H2D of x/y/triple for qkv and o, two "
+                    "lora_sgmv_apply calls, D2H of both y"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=640)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode8b", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 4x L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+/*
+ * lora_sgmv.h -- C ABI of the GB300 (sm_103a) segmented gather matrix-vector
+ * (SGMV) LoRA library.
+ *
+ * The library adds, for every token row t routed to an adapter slot s,
+ *     y_t += B_s . (A_s . x_t)
+ * to a projection's base output y ("vLLM LoRA 实现深度解析", section 1: the
+ * forward pass h = W0 x + (alpha/r) B A x with the scale folded into B;
+ * section 6: output += lora_b_stacked[slot] . lora_a_stacked[slot] . x).
+ *
+ * Routing follows the triple of the "max.pipelines.lora.LoRAManagerV3" API
+ * page (get_lora_graph_inputs): lora_ids and grouped_offsets live on the
+ * device, end on the host.  Rows at or past `end` (base requests, which the
+ * sort puts last) are never read or written.
+ *
+ * Conventions for every entry point:
+ *   - Every buffer is owned by the caller.  No entry point allocates or frees
+ *     device memory, and none keeps a pointer after it returns.
+ *   - Device work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and is asynchronous; host arrays passed in may be reused
+ *     as soon as the call returns.
+ *   - Arguments are validated on the host before anything is launched; on any
+ *     error nothing is launched and the error code is returned.
+ *   - The device-side routing arrays are checked by the kernels themselves
+ *     (slot range, monotone offsets, first offset 0, last offset == end).  A
+ *     violation makes that launch skip ALL of its work, leaves y untouched and
+ *     records a flag that lora_get_device_status() returns.
+ *   - A CUDA launch failure returns LORA_ERR_CUDA.
+ *   - Entry points are thread-safe as far as CUDA itself is; two calls that
+ *     write the same y concurrently on different streams race.
+ */
+#ifndef LORA_SGMV_H
+#define LORA_SGMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, without pulling in the CUDA headers. */
+typedef struct CUstream_st* lora_stream_t;
+
+typedef enum {
+  LORA_OK = 0,
+  LORA_ERR_NULL = 1,          /* a required pointer is NULL */
+  LORA_ERR_SHAPE = 2,         /* a count, size or stride is out of range */
+  LORA_ERR_RANK = 3,          /* adapter rank r > max_lora_rank, or r < 0 */
+  LORA_ERR_SLOT_RANGE = 4,    /* a slot id < -1 (requests) or >= max_num_loras */
+  LORA_ERR_ROUTING = 5,       /* routing triple inconsistent (num_groups, end) */
+  LORA_ERR_DTYPE = 6,         /* unknown storage type */
+  LORA_ERR_ALIGN = 7,         /* pointer/stride alignment required by the call */
+  LORA_ERR_WORKSPACE = 8,     /* workspace NULL or smaller than lora_workspace_bytes() */
+  LORA_ERR_CUDA = 9,          /* a CUDA runtime call or kernel launch failed */
+  LORA_ERR_DEVICE_CHECK = 10  /* reserved: returned by no call; see lora_get_device_status */
+} lora_status_t;
+
+/* Storage type of x, y and the A/B stacks of one problem. */
+typedef enum { LORA_DTYPE_F32 = 0, LORA_DTYPE_BF16 = 1 } lora_dtype_t;
+
+/* Flags of the device status word (lora_get_device_status). */
+#define LORA_DEV_BAD_SLOT 1u     /* lora_ids[g] outside [0, max_num_loras) */
+#define LORA_DEV_BAD_OFFSETS 2u  /* grouped_offsets[0] != 0 or a decreasing offset */
+#define LORA_DEV_BAD_END 4u      /* grouped_offsets[num_groups] != end */
+#define LORA_DEV_TIMEOUT 8u      /* a kernel gave up waiting for its own copies */
+
+#define LORA_MAX_SLICES 3
+
+/*
+ * One projection slice of a problem.  A and B are the per-slot stacks of the
+ * "vLLM LoRA 实现深度解析" page, section 9 (memory layout):
+ *   A: slot s block at A + s*A_slot_stride, shape [max_lora_rank, in_dim],
+ *      row-major, row stride in_dim (elements).
+ *   B: slot s block at B + s*B_slot_stride, shape [out_dim, max_lora_rank],
+ *      row-major, row stride max_lora_rank.
+ *   y: row t of this slice's output at y + t*y_row_stride, out_dim elements.
+ * Strides are in elements.  Fused q/k/v ("MAX max.pipelines.lora 模块解析",
+ * load pipeline, QKV fusion: A concatenated on the rank dimension, B on the
+ * output dimension) is pure pointer arithmetic on one fused stack:
+ *   slice j: A = A_fused + j*R*in_dim, A_slot_stride = n*R*in_dim,
+ *            B = B_fused + off_j*R,   B_slot_stride = O*R,
+ *            y = y_fused + off_j,      y_row_stride  = O,
+ * so slice j's B multiplies only rank columns [jR, (j+1)R) of the
+ * intermediate.  Per-projection (unfused) q/k/v is three slices with their
+ * own stacks.
+ */
+typedef struct {
+  const void* A;
+  int64_t A_slot_stride;
+  const void* B;
+  int64_t B_slot_stride;
+  int32_t out_dim;
+  void* y;
+  int64_t y_row_stride;
+} lora_slice_t;
+
+/*
+ * One LoRA problem: a projection input x[num_tokens, in_dim] (row stride
+ * x_row_stride elements, rows in sorted-batch order) and 1..3 slices sharing
+ * it.  max_num_loras (S) and max_lora_rank (R) are the stack sizes.
+ */
+typedef struct {
+  lora_dtype_t dtype;
+  int32_t num_tokens;
+  int32_t in_dim;
+  int32_t max_num_loras;
+  int32_t max_lora_rank;
+  const void* x;
+  int64_t x_row_stride;
+  int32_t num_slices;
+  lora_slice_t slices[LORA_MAX_SLICES];
+} lora_problem_t;
+
+/*
+ * The routing triple ("max.pipelines.lora.LoRAManagerV3",
+ * get_lora_graph_inputs): lora_ids[num_groups] and
+ * grouped_offsets[num_groups + 1] are DEVICE int32 arrays; num_groups and end
+ * are host values.  Group g covers sorted-batch rows
+ * [grouped_offsets[g], grouped_offsets[g+1]) and uses slot lora_ids[g].
+ * num_groups == 0 or end == 0 is a valid no-op.
+ */
+typedef struct {
+  const int32_t* lora_ids;
+  const int32_t* grouped_offsets;
+  int32_t num_groups;
+  int32_t end;
+} lora_routing_t;
+
+/*
+ * lora_build_routing -- HOST ONLY.  Sort + group ("max.pipelines.lora.
+ * LoRAManagerV3", sort_lora_batch and get_lora_graph_inputs).
+ *
+ * Input: num_requests requests in arrival order, request i on slot
+ * req_slot[i] (-1 = base model, else 0..max_num_loras-1) with
+ * req_num_tokens[i] >= 0 token rows.
+ * Output (caller-allocated host arrays):
+ *   perm[num_requests]               sorted order: perm[i] is the arrival index
+ *                                    of the i-th request of the sorted batch.
+ *                                    Ascending slot, stable, base last.
+ *   lora_ids[max_num_loras]          slot of each group (first *num_groups used)
+ *   grouped_offsets[max_num_loras+1] first row of each group; entry
+ *                                    [*num_groups] equals *end
+ *   *num_groups, *end (LoRA-routed rows), *total_tokens (all rows).
+ * Consecutive same-slot requests form one group; the walk stops at the first
+ * base request.  A zero-token request still opens its slot's group.
+ * Errors: LORA_ERR_SHAPE (num_requests < 0, max_num_loras < 1, a negative
+ * token count, total rows > INT32_MAX), LORA_ERR_SLOT_RANGE, LORA_ERR_NULL.
+ * Outputs are unspecified on error.
+ */
+lora_status_t lora_build_routing(int32_t num_requests, const int32_t* req_slot,
+                                 const int32_t* req_num_tokens, int32_t max_num_loras,
+                                 int32_t* perm, int32_t* lora_ids, int32_t* grouped_offsets,
+                                 int32_t* num_groups, int32_t* end, int32_t* total_tokens);
+
+/*
+ * lora_set_slot -- load-time preparation of one adapter slot for one slice
+ * ("MAX max.pipelines.lora 模块解析", load pipeline: scale pre-multiplied into
+ * B, rank padding, dtype unification; "vLLM LoRA 实现深度解析" section 1,
+ * scale alpha/r or alpha/sqrt(r) with rsLoRA, and section 5.3 set_lora).
+ *
+ * Writes slot `slot` of slice `slice` of the stacks described by `problem`
+ * (the stacks must be writable device memory):
+ *   A[slot, k, i] = A_raw[k, i]                        for k < r, else 0
+ *   B[slot, o, k] = rne(fp32(B_raw[o, k]) * scale)     for k < r, else 0
+ * where scale = fp32(lora_alpha / r), or fp32(lora_alpha / sqrt(r)) when
+ * use_rslora != 0, computed in double on the host; the product is formed in
+ * fp32 and rounded once (round to nearest even) to problem->dtype.
+ * A_raw [r, in_dim] and B_raw [out_dim, r] are contiguous DEVICE arrays of
+ * raw_dtype (fp32 or bf16).  r == 0 zeroes the slot (A_raw/B_raw may be NULL).
+ * Errors: LORA_ERR_RANK (r < 0 or r > max_lora_rank), LORA_ERR_SLOT_RANGE,
+ * LORA_ERR_SHAPE (slice out of range, bad dims), LORA_ERR_NULL, LORA_ERR_DTYPE.
+ */
+lora_status_t lora_set_slot(const lora_problem_t* problem, int32_t slice, int32_t slot, int32_t r,
+                            double lora_alpha, int32_t use_rslora, const void* A_raw,
+                            const void* B_raw, lora_dtype_t raw_dtype, lora_stream_t stream);
+
+/*
+ * lora_shrink -- u[t, j*R + k] = sum_i A_j[lora_ids[g], k, i] * x[t, i] for
+ * every routed row t < end (group g), slice j, k < R.  u is a DEVICE fp32
+ * array [end, num_slices*R] (row stride num_slices*R), fully overwritten.
+ * Products of the stored values are exact; sums are fp32.
+ */
+lora_status_t lora_shrink(const lora_problem_t* problem, const lora_routing_t* routing, float* u,
+                          lora_stream_t stream);
+
+/*
+ * lora_expand -- boundary-aware expand: y_j[t, o] = rn(y_j[t, o] +
+ * sum_k B_j[lora_ids[g], o, k] * u[t, j*R + k]) for routed rows t < end only,
+ * with one rounding to the storage type.  u as produced by lora_shrink.
+ * Accumulation is fp32.  On the bf16 tensor-core path u enters the product as
+ * two bf16 terms (u = hi + lo, 16 significant bits, the split is exact);
+ * elsewhere it enters as fp32.
+ */
+lora_status_t lora_expand(const lora_problem_t* problem, const lora_routing_t* routing,
+                          const float* u, lora_stream_t stream);
+
+/* Bytes of device workspace lora_sgmv_apply needs for `end` routed rows. */
+size_t lora_workspace_bytes(const lora_problem_t* problem, int32_t end);
+
+/*
+ * lora_sgmv_apply -- shrink then expand in one call; the fp32 intermediate
+ * lives in `workspace` (DEVICE, >= lora_workspace_bytes(problem, end) bytes,
+ * 16-byte aligned, contents on entry ignored).  The expand is launched as a
+ * programmatic dependent of the shrink, so its weight and y loads overlap the
+ * shrink.
+ */
+lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_t* routing,
+                              void* workspace, size_t workspace_bytes, lora_stream_t stream);
+
+/*
+ * lora_get_device_status -- synchronizes `stream`, then reads and clears the
+ * device status word of the current device (an OR of LORA_DEV_* flags from
+ * every launch since the last read).  Returns LORA_ERR_CUDA if the
+ * synchronization or copy fails.
+ */
+lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* flags);
+
+/* Static, human-readable name of a status code. */
+const char* lora_status_string(lora_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_SGMV_H */

@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.
+
+Bars: routing bit-exact; slot preparation bit-exact; u within
+1e-3 (1 + |ref|); y within 2e-2 (1 + |ref|) for bf16 and 1e-3 (1 + |ref|)
+for fp32; rows at or past `end` bit-identical (NaN-payload sentinels).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import synthetic as sy
+
+pytestmark = pytest.mark.gpu
+
+TOL_U = 1e-3
+TOL_Y = {"bf16": 2e-2, "f32": 1e-3}
+SENTINEL = {"bf16": 0x7FC1, "f32": 0x7FC00001}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as ge
+    ge.build()
+
+
+def _lk():
+    import adapter_sgmv_lora_gb300 as lk
+    return lk
+
+
+def _dev():
+    from workloads import device
+    return device
+
+
+def _plant_sentinels(dev, end):
+    dt = dev["dtype"]
+    bits = SENTINEL[dt]
+    for y in dev["ys"] if dev["separate_y"] else [dev["y_all"]]:
+        if y.shape[0] > end:
+            if dt == "bf16":
+                y[end:].view(torch.int16).fill_(bits - 0x10000 if bits > 0x7FFF else bits)
+            else:
+                y[end:].view(torch.int32).fill_(bits)
+
+
+def _sample_rows(offs, end, rng, extra=48):
+    rows = set()
+    for g in range(len(offs) - 1):
+        a, b = int(offs[g]), int(offs[g + 1])
+        if b <= a:
+            continue
+        for t in (a, a + 1, b - 2, b - 1):
+            if a <= t < b:
+                rows.add(t)
+        for base in range(a + 63, b, 64):  # around every 64-row tile boundary
+            for t in (base, base + 1):
+                if a <= t < b:
+                    rows.add(t)
+    if end > 0:
+        rows.update(int(v) for v in rng.integers(0, end, size=min(extra, end)))
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0):
+    """Prepare on the device, run, compare with the oracle.  Returns the device dict."""
+    lk, device = _lk(), _dev()
+    dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y)
+    ref = oracle.prepare_problem(raw, proj, fused=fused)
+    dt = raw["dtype"]
+    # routing: library == oracle, bit-exact
+    rt = dev["route_host"]
+    assert np.array_equal(rt["lora_ids"], ref["route"]["lora_ids"])
+    assert np.array_equal(rt["grouped_offsets"], ref["route"]["grouped_offsets"])
+    assert np.array_equal(rt["perm"], ref["route"]["perm"])
+    end = rt["end"]
+    # stacks: lora_set_slot == oracle preparation, bit-exact
+    if fused or len(dev["names"]) == 1:
+        assert np.array_equal(device.torch_to_storage(dev["stacks"]["A"], dt), ref["stored"]["A"])
+        assert np.array_equal(device.torch_to_storage(dev["stacks"]["B"], dt), ref["stored"]["B"])
+    else:
+        for j in range(len(dev["names"])):
+            assert np.array_equal(device.torch_to_storage(dev["stacks"]["A"][j], dt), ref["stored"]["A"][j])
+            assert np.array_equal(device.torch_to_storage(dev["stacks"]["B"][j], dt), ref["stored"]["B"][j])
+    _plant_sentinels(dev, end)
+    y_before = device.y_host(dev)
+    prob, routing = dev["problem"], dev["routing"]
+    u = None
+    if mode == "apply":
+        lk.lora_sgmv_apply(prob, routing, dev["workspace"])
+    else:
+        nR = len(dev["names"]) * raw["max_lora_rank"]
+        u = torch.full((max(end, 1), nR), float("nan"), dtype=torch.float32, device="cuda")
+        lk.lora_shrink(prob, routing, u)
+        lk.lora_expand(prob, routing, u)
+    torch.cuda.synchronize()
+    assert lk.lora_get_device_status() == 0
+    y_after = device.y_host(dev)
+    # rows >= end: bit-identical
+    assert np.array_equal(y_after[end:], y_before[end:])
+    if end == 0:
+        return dev
+    rng = np.random.default_rng(seed)
+    rr = np.arange(end, dtype=np.int32) if rows == "all" else _sample_rows(rt["grouped_offsets"], end, rng)
+    u_ref, ys_ref = oracle.problem_rows(ref, rr)
+    got = oracle.to_f64(y_after[rr], dt)
+    col = 0
+    for yj in ys_ref:
+        g = got[:, col:col + yj.shape[1]]
+        err = np.abs(g - yj) / (1.0 + np.abs(yj))
+        assert err.max() <= TOL_Y[dt], ("y", float(err.max()), int(np.argmax(err.max(axis=1))))
+        col += yj.shape[1]
+    if u is not None:
+        ug = u.cpu().numpy().astype(np.float64)[rr]
+        err = np.abs(ug - u_ref) / (1.0 + np.abs(u_ref))
+        assert err.max() <= TOL_U, ("u", float(err.max()))
+    return dev
+
+
+# ------------------------------------------------------------ workloads --
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_tiny_fp32(proj, mode):
+    run_case(sy.draw("tiny", 0), proj, mode=mode)
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_decode8b_full(proj, mode):
+    run_case(sy.draw("decode8b", 0), proj, mode=mode)
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_many64_unfused_full(proj):
+    run_case(sy.draw("many64", 0), proj, fused=False, mode="split")
+
+
+def test_many64_separate_outputs():
+    run_case(sy.draw("many64", 1), "qkv", fused=False, separate_y=True)
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_prefill8b_sampled(proj):
+    run_case(sy.draw("prefill8b", 0), proj, mode="split", rows="sample")
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_mixed70b_sampled(proj):
+    run_case(sy.draw("mixed70b", 0), proj, rows="sample")
+
+
+# ------------------------------------------------------------ edge cases --
+
+def _spec(**kw):
+    return sy.custom_spec(**kw)
+
+
+@pytest.mark.parametrize("R", [16, 32, 64, 128])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_rank_variants_ragged_tiles(R, mode):
+    """Group lengths straddling 64-row tiles: 1, 63, 64, 65, 127, 130, 200."""
+    spec = _spec(max_num_loras=7, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
+                 fixed_slots=(0, 1, 2, 3, 4, 5, 6, -1), fixed_lens=(1, 63, 64, 65, 127, 130, 200, 9),
+                 hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
+    run_case(sy.draw(spec, 3), "qkv", mode=mode)
+    run_case(sy.draw(spec, 4), "o", mode=mode)
+
+
+def test_all_base_is_noop():
+    spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(3, 4))
+    dev = run_case(sy.draw(spec, 0), "qkv")
+    assert dev["route_host"]["end"] == 0
+
+
+def test_zero_length_groups_and_unsorted_arrivals():
+    spec = _spec(max_num_loras=5, kind="fixed", fixed_slots=(3, -1, 0, 4, 0, 2, 1, -1),
+                 fixed_lens=(5, 2, 0, 0, 7, 66, 0, 3), hidden=128)
+    run_case(sy.draw(spec, 0), "qkv", mode="split")
+
+
+def test_unaligned_shapes_take_generic_path():
+    """in_dim not a multiple of 64 and outputs not multiples of 8: generic kernels."""
+    spec = _spec(hidden=72, n_heads=3, n_kv_heads=1, head_dim=12, max_lora_rank=16, n_requests=40)
+    run_case(sy.draw(spec, 0), "qkv", mode="split")
+    run_case(sy.draw(spec, 1), "qkv", mode="apply")
+
+
+def test_rank_not_in_fast_set():
+    spec = _spec(max_lora_rank=8, rank_choices=(4, 8), n_requests=30)
+    run_case(sy.draw(spec, 0), "qkv", mode="split")
+
+
+def test_fp32_larger():
+    spec = _spec(dtype="f32", hidden=512, n_heads=8, n_kv_heads=2, head_dim=64, max_lora_rank=32,
+                 rank_choices=(16, 32), kind="prefill", n_requests=6, len_range=(1, 150),
+                 slot_dist="uniform+base")
+    run_case(sy.draw(spec, 0), "qkv", mode="split")
+
+
+def test_deterministic():
+    lk, device = _lk(), _dev()
+    raw = sy.draw("decode8b", 2)
+    outs = []
+    for _ in range(2):
+        dev = device.prepare(raw, "qkv")
+        lk.lora_sgmv_apply(dev["problem"], dev["routing"], dev["workspace"])
+        torch.cuda.synchronize()
+        outs.append(device.y_host(dev))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_pages_base_only_fallback_leaves_y_unchanged():
+    """The MAX page's base-only fallback: an all-zero adapter in slot 0 with
+    every token routed to it is a no-op in value."""
+    lk, device = _lk(), _dev()
+    spec = _spec(max_num_loras=2, kind="fixed", fixed_slots=(0,), fixed_lens=(50,), rank_choices=(16,))
+    raw = sy.draw(spec, 0)
+    for p in sy.PROJS:
+        raw["B"][p][0] = np.zeros_like(raw["B"][p][0])
+    dev = device.prepare(raw, "qkv")
+    before = device.y_host(dev)
+    lk.lora_sgmv_apply(dev["problem"], dev["routing"], dev["workspace"])
+    torch.cuda.synchronize()
+    after = device.y_host(dev)
+    a = oracle.to_f64(before, "bf16")
+    b = oracle.to_f64(after, "bf16")
+    assert np.array_equal(a, b)  # equal in value (+0 / -0 allowed)
+
+
+@pytest.mark.parametrize("bad", ["slot", "offsets", "end"])
+def test_invalid_device_routing_is_flagged_and_skipped(bad):
+    lk, device = _lk(), _dev()
+    raw = sy.draw("decode8b", 0)
+    dev = device.prepare(raw, "qkv")
+    rt = dev["route_host"]
+    ids = rt["lora_ids"].copy()
+    offs = rt["grouped_offsets"].copy()
+    if bad == "slot":
+        ids[1] = raw["max_num_loras"] + 3
+        flag = lk.DEV_BAD_SLOT
+    elif bad == "offsets":
+        offs[2], offs[3] = offs[3], offs[2]
+        flag = lk.DEV_BAD_OFFSETS
+    else:
+        offs[-1] -= 1
+        flag = lk.DEV_BAD_END
+    routing = lk.Routing(torch.from_numpy(ids).cuda(), torch.from_numpy(offs).cuda(), rt["num_groups"],
+                         rt["end"])
+    assert lk.lora_get_device_status() == 0
+    before = device.y_host(dev)
+    lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
+    assert lk.lora_get_device_status() & flag
+    assert np.array_equal(device.y_host(dev), before)
+    assert lk.lora_get_device_status() == 0  # read-and-clear
+
+
+def test_workspace_too_small_is_rejected():
+    lk, device = _lk(), _dev()
+    dev = device.prepare(sy.draw("decode8b", 0), "o")
+    with pytest.raises(lk.LoraError) as e:
+        lk.lora_sgmv_apply(dev["problem"], dev["routing"], dev["workspace"][:10])
+    assert e.value.status == 8

@@ -322,7 +322,7 @@ def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
                            "B": to_f64(stacks_b[j], dt), "B_offset": 0, "B_slot_stride": od * R,
                            "out_dim": od, "y": y, "y_col0": off})
             off += od
-        stored = {"A": stacks_a, "B": stacks_b}
+        stored = {"A": stacks_a, "B": stacks_b} if len(names) > 1 else {"A": stacks_a[0], "B": stacks_b[0]}
     return {"dtype": dt, "S": S, "R": R, "in_dim": in_dim, "x": raw["x_" + proj], "slices": slices,
             "lora_ids": route["lora_ids"], "grouped_offsets": route["grouped_offsets"],
             "end": route["end"], "route": route, "stored": stored, "out_dims": outs}

@@ -10,16 +10,21 @@
 // (tiles.cuh).  The shrink gives each (tile, rank-column block) to a
 // thread-block cluster of C CTAs that split the input dimension; every CTA
 // streams its K range of the tile's x rows and of the slot's A rows into
-// shared memory with bulk (TMA engine) copies, one copy per row segment so
-// that no byte outside the group is fetched, and multiplies on the tensor
-// cores (mma.sync m16n8k16, fp32 accumulate).  The C partial tiles are summed
-// through distributed shared memory in a fixed order (deterministic) and
-// written once to u.  The expand gives each (tile, slice, 2R..256-column
-// output block) to one CTA: it loads the y block and the slot's B block, then
-// waits (programmatic dependent launch) for the shrink grid, loads u, splits
-// it into hi + lo bf16 terms, multiplies with the y block as the initial
-// accumulator, rounds once and bulk-stores exactly the routed rows back.
-// Rows at or past `end` are never read or written.
+// shared memory through a multistage ring of 16-byte asynchronous copies
+// issued by all threads (exactly the group's own rows: nothing outside the
+// group is fetched), and multiplies on the tensor cores (mma.sync m16n8k16,
+// fp32 accumulate).  The C partial tiles are summed through distributed
+// shared memory in a fixed order (deterministic) and written once to u.  The
+// expand gives each (tile, slice, output block) to one CTA: it starts the
+// loads of the y block and of the slot's B block, waits (programmatic
+// dependent launch) for the shrink grid, loads u, splits it into hi + lo
+// bf16 terms, multiplies with the y block as the initial accumulator, rounds
+// once and writes exactly the routed rows back with 16-byte stores.  Rows at
+// or past `end` are never read or written.
+//
+// Row gathers use per-thread 16-byte copies rather than one bulk (TMA)
+// request per row: a tile is tens of short row segments, and per-request
+// bulk-copy issue cost dominated (measured: 30 us for a 4.8 MB shrink).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -33,20 +38,18 @@ namespace lora {
 
 namespace {
 
-constexpr int MT = kTileRows;       // token rows per tile
-constexpr int KS = 64;              // input elements per shrink stage
-constexpr int XPITCH = KS * 2 + 16; // bytes per staged row (padding: conflict-free ldmatrix)
-constexpr int NSTAGE = 4;           // shrink pipeline depth
+constexpr int MT = kTileRows;        // token rows per tile
+constexpr int KS = 64;               // input elements per shrink stage
+constexpr int XPITCH = KS * 2 + 16;  // bytes per staged row (padding: conflict-free ldmatrix)
 
 template <int NB>
 struct ShrinkCfg {
+  static constexpr int NSTAGE = NB <= 48 ? 8 : (NB <= 64 ? 6 : 4);
   static constexpr int STAGE_BYTES = (MT + NB) * XPITCH;
-  static constexpr int PPITCH = NB + 4;  // floats per partial row
+  static constexpr int PPITCH = NB + 4;  // floats per partial row (16-byte aligned rows)
   static constexpr int SMEM = NSTAGE * STAGE_BYTES;
   static_assert(MT * PPITCH * 4 <= SMEM, "partial tile must fit in the stage ring");
 };
-
-__device__ __forceinline__ void record(const ProblemDesc& p, unsigned flag) { atomicOr(p.status, flag); }
 
 }  // namespace
 
@@ -56,8 +59,8 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
                                                                float* __restrict__ u, int C,
                                                                int nblk, int Kc) {
   using Cfg = ShrinkCfg<NB>;
+  constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[NSTAGE];
   __shared__ Tile s_tile;
   __shared__ int s_ok;
 
@@ -77,10 +80,6 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
       s_ok = ok;
     }
   }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NSTAGE; ++i) mbar_init(&full[i], 1);
-    fence_mbar_init();
-  }
   __syncthreads();
   if (!s_ok) return;  // the whole cluster sees the same tile and verdict
   const Tile t = s_tile;
@@ -92,39 +91,50 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   const int k0 = crank * Kc;
   const int nst = Kc / KS;
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+  const int chunks = (t.rows + nvalid) * (KS / 8);  // 16-byte chunks per stage
 
   auto issue = [&](int s) {
-    const int slot = s % NSTAGE;
-    uint8_t* xs = smem + slot * Cfg::STAGE_BYTES;
-    uint8_t* as = xs + MT * XPITCH;
+    uint8_t* xs = smem + (s % NSTAGE) * Cfg::STAGE_BYTES;
     const long long kk = (long long)k0 + (long long)s * KS;
-    if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(t.rows + nvalid) * (KS * 2));
-    __syncwarp();
-    for (int r = lane; r < t.rows; r += 32)
-      bulk_g2s(xs + r * XPITCH, xg + (long long)(t.row0 + r) * p.x_row_stride + kk, KS * 2, &full[slot]);
-    for (int n = lane; n < nvalid; n += 32) {
-      const int col = n0 + n;
-      const int j = col / R, k = col - (col / R) * R;
-      const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(p.sl[j].A) +
-                               (long long)t.slot * p.sl[j].A_slot_stride + (long long)k * p.in_dim + kk;
-      bulk_g2s(as + n * XPITCH, a, KS * 2, &full[slot]);
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const int row = c >> 3, ch = c & 7;
+      const __nv_bfloat16* src;
+      int drow;  // x rows occupy [0, MT) of the stage, A rows [MT, MT + NB)
+      if (row < t.rows) {
+        src = xg + (long long)(t.row0 + row) * p.x_row_stride + kk + ch * 8;
+        drow = row;
+      } else {
+        const int col = n0 + row - t.rows;
+        const int j = col / R, k = col - j * R;
+        src = static_cast<const __nv_bfloat16*>(p.sl[j].A) + (long long)t.slot * p.sl[j].A_slot_stride +
+              (long long)k * p.in_dim + kk + ch * 8;
+        drow = MT + (row - t.rows);
+      }
+      cp_async16(xs + drow * XPITCH + ch * 16, src);
     }
   };
 
-  if (warp == 0)
-    for (int s = 0; s < min(NSTAGE, nst); ++s) issue(s);
+#pragma unroll 1
+  for (int s = 0; s < NSTAGE - 1; ++s) {
+    if (s < nst) issue(s);
+    cp_async_commit();
+  }
 
   float acc[NB / 8][4];
 #pragma unroll
   for (int i = 0; i < NB / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
   const bool active = warp * 16 < t.rows;  // warp-uniform: this warp's 16 rows hold data
-  bool timed_out = false;
+#pragma unroll 1
   for (int s = 0; s < nst; ++s) {
-    const int slot = s % NSTAGE;
-    if (!timed_out && !mbar_wait(&full[slot], (uint32_t)((s / NSTAGE) & 1))) timed_out = true;
-    if (active && !timed_out) {
-      const uint32_t xs = smem_addr(smem + slot * Cfg::STAGE_BYTES);
+    // Refill the slot consumed in the previous iteration (all threads passed
+    // the barrier that ended it), then wait for stage s.
+    if (s + NSTAGE - 1 < nst) issue(s + NSTAGE - 1);
+    cp_async_commit();
+    cp_async_wait<NSTAGE - 1>();
+    __syncthreads();
+    if (active) {
+      const uint32_t xs = smem_addr(smem + (s % NSTAGE) * Cfg::STAGE_BYTES);
       const uint32_t as = xs + MT * XPITCH;
 #pragma unroll
       for (int ks = 0; ks < KS / 16; ++ks) {
@@ -143,13 +153,9 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
       }
     }
     __syncthreads();
-    if (warp == 0 && s + NSTAGE < nst && !timed_out) issue(s + NSTAGE);
   }
-  if (timed_out) {
-    record(p, LORA_DEV_TIMEOUT);
-    // Give outstanding copies a bounded chance to land before smem is reused.
-    for (int s = 0; s < min(NSTAGE, nst); ++s) (void)mbar_wait(&full[s], 0);
-  }
+  cp_async_wait<0>();
+  __syncthreads();
 
   // Partial tile -> shared memory (reuses the stage ring: every copy landed).
   float* P = reinterpret_cast<float*>(smem);
@@ -158,10 +164,8 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
 #pragma unroll
     for (int nt = 0; nt < NB / 8; ++nt) {
       const int row = warp * 16 + g, col = nt * 8 + 2 * tq;
-      P[row * Cfg::PPITCH + col] = acc[nt][0];
-      P[row * Cfg::PPITCH + col + 1] = acc[nt][1];
-      P[(row + 8) * Cfg::PPITCH + col] = acc[nt][2];
-      P[(row + 8) * Cfg::PPITCH + col + 1] = acc[nt][3];
+      *reinterpret_cast<float2*>(&P[row * Cfg::PPITCH + col]) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2*>(&P[(row + 8) * Cfg::PPITCH + col]) = make_float2(acc[nt][2], acc[nt][3]);
     }
   }
   if (C > 1)
@@ -170,22 +174,35 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     __syncthreads();
 
   // Each CTA of the cluster sums its share of rows over all C partials, in
-  // rank order, and writes them to u.
+  // rank order, and writes them to u, four columns per step (nvalid is a
+  // multiple of 16).  The C remote loads of a step are issued back to back.
   const int rpc = MT / C;
   const int r_lo = crank * rpc;
   const int r_hi = min(r_lo + rpc, t.rows);
-  const int cnt = (r_hi - r_lo) * nvalid;
+  const int q4 = nvalid / 4;
+  const int cnt = (r_hi - r_lo) * q4;
   for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-    const int r = r_lo + e / nvalid, c = e % nvalid;
-    float v;
+    const int r = r_lo + e / q4, c = (e % q4) * 4;
+    float4 v;
     if (C == 1) {
-      v = P[r * Cfg::PPITCH + c];
+      v = *reinterpret_cast<const float4*>(&P[r * Cfg::PPITCH + c]);
     } else {
       const uint32_t la = smem_addr(&P[r * Cfg::PPITCH + c]);
-      v = 0.f;
-      for (int q = 0; q < C; ++q) v += ld_shared_cluster_f32(map_shared_rank(la, (uint32_t)q));
+      float4 part[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < C) part[q] = ld_shared_cluster_f32x4(map_shared_rank(la, (uint32_t)q));
+      v = part[0];
+#pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < C) {
+          v.x += part[q].x;
+          v.y += part[q].y;
+          v.z += part[q].z;
+          v.w += part[q].w;
+        }
     }
-    u[(long long)(t.row0 + r) * nR + n0 + c] = v;
+    *reinterpret_cast<float4*>(&u[(long long)(t.row0 + r) * nR + n0 + c]) = v;
   }
   if (C > 1) cluster_sync();  // keep this CTA's partial alive for its peers
 }
@@ -195,16 +212,17 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
 template <int R, int OB>
 struct ExpandCfg {
   static constexpr int YPITCH = OB * 2 + 16;  // bytes per staged y row
+  static constexpr int BPITCH = R * 2 + 16;   // bytes per staged B row (conflict-free ldmatrix)
   static constexpr int UPITCH = 4 * R + 16;   // bytes per hi|lo row (2R bf16)
   static constexpr int Y_OFF = 0;
   static constexpr int B_OFF = MT * YPITCH;
-  static constexpr int U_OFF = B_OFF + OB * R * 2;
+  static constexpr int U_OFF = B_OFF + OB * BPITCH;
   static constexpr int H_OFF = U_OFF + MT * R * 4;
   static constexpr int SMEM = H_OFF + MT * UPITCH;
 };
 
 struct ExpandMap {
-  int n_ob_total;                   // output blocks per tile, all slices
+  int n_ob_total;                     // output blocks per tile, all slices
   int ob_begin[LORA_MAX_SLICES + 1];  // first output block of each slice
 };
 
@@ -214,7 +232,6 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
                                                                const ExpandMap map) {
   using Cfg = ExpandCfg<R, OB>;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar_yb, bar_u;
   __shared__ Tile s_tile;
   __shared__ int s_ok;
 
@@ -236,16 +253,8 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
       s_ok = ok;
     }
   }
-  if (threadIdx.x == 0) {
-    mbar_init(&bar_yb, 1);
-    mbar_init(&bar_u, 1);
-    fence_mbar_init();
-  }
   __syncthreads();
-  if (!s_ok) {
-    pdl_wait();
-    return;
-  }
+  if (!s_ok) return;
   const Tile t = s_tile;
 
   uint8_t* Ys = smem + Cfg::Y_OFF;
@@ -253,58 +262,56 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   float* Us = reinterpret_cast<float*>(smem + Cfg::U_OFF);
   uint8_t* Hs = smem + Cfg::H_OFF;
   __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(sl.y);
+  const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(sl.B) + (long long)t.slot * sl.B_slot_stride +
+                            (long long)o0 * R;
 
   // y block and B block do not depend on the shrink: fetch them first.
-  if (warp == 0) {
-    if (lane == 0)
-      mbar_arrive_expect_tx(&bar_yb, (uint32_t)t.rows * ovalid * 2 + (uint32_t)ovalid * R * 2);
-    __syncwarp();
-    if (lane == 0)
-      bulk_g2s(Bs,
-               static_cast<const __nv_bfloat16*>(sl.B) + (long long)t.slot * sl.B_slot_stride +
-                   (long long)o0 * R,
-               (uint32_t)ovalid * R * 2, &bar_yb);
-    for (int r = lane; r < t.rows; r += 32)
-      bulk_g2s(Ys + r * Cfg::YPITCH, yg + (long long)(t.row0 + r) * sl.y_row_stride + o0,
-               (uint32_t)ovalid * 2, &bar_yb);
+  {
+    const int ych = ovalid / 8;  // 16-byte chunks per y row
+    const int ny = t.rows * ych;
+    constexpr int BCH = R / 8;   // chunks per B row
+    const int nbc = ovalid * BCH;
+    for (int c = threadIdx.x; c < ny + nbc; c += blockDim.x) {
+      if (c < ny) {
+        const int r = c / ych, ch = c - r * ych;
+        cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8);
+      } else {
+        const int e = c - ny;
+        const int o = e / BCH, ch = e - o * BCH;
+        cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
+      }
+    }
+    cp_async_commit();
   }
 
   pdl_wait();  // the shrink grid (if any) has finished and its u is visible
 
-  if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(&bar_u, (uint32_t)t.rows * R * 4);
-    __syncwarp();
-    for (int r = lane; r < t.rows; r += 32)
-      bulk_g2s(Us + r * R, u + (long long)(t.row0 + r) * nR + (long long)j * R, R * 4, &bar_u);
-  }
-  bool ok = mbar_wait(&bar_u, 0);
-  // u -> hi + lo bf16 (u = hi + lo to 16 significant bits; the subtraction is exact).
-  if (ok) {
-    for (int e = threadIdx.x; e < t.rows * R; e += blockDim.x) {
-      const int r = e / R, k = e % R;
-      const float v = Us[r * R + k];
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-      __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
-      hrow[k] = hi;
-      hrow[R + k] = lo;
+  {
+    constexpr int UCH = R / 4;  // 16-byte chunks per u row slice
+    for (int c = threadIdx.x; c < t.rows * UCH; c += blockDim.x) {
+      const int r = c / UCH, ch = c - r * UCH;
+      cp_async16(Us + r * R + ch * 4, u + (long long)(t.row0 + r) * nR + (long long)j * R + ch * 4);
     }
+    cp_async_commit();
   }
-  ok = mbar_wait(&bar_yb, 0) && ok;
+  cp_async_wait<0>();
   __syncthreads();
-  const int any_fail = __syncthreads_or(!ok);
-  if (any_fail) {
-    if (threadIdx.x == 0) record(p, LORA_DEV_TIMEOUT);
-    (void)mbar_wait(&bar_yb, 0);
-    (void)mbar_wait(&bar_u, 0);
-    return;
+  // u -> hi + lo bf16 (u = hi + lo to 16 significant bits; the subtraction is exact).
+  for (int e = threadIdx.x; e < t.rows * R; e += blockDim.x) {
+    const int r = e / R, k = e % R;
+    const float v = Us[r * R + k];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
+    hrow[k] = hi;
+    hrow[R + k] = lo;
   }
+  __syncthreads();
 
   const int m = warp & 3, nh = warp >> 2;
   constexpr int NT = OB / 16;  // n8 tiles per warp
   const int g = lane >> 2, tq = lane & 3;
-  const bool active = m * 16 < t.rows;
-  if (active) {
+  if (m * 16 < t.rows) {
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
         uint32_t b0, b1, b2, b3;
         const int nrow = nh * (OB / 2) + np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int kcol = kb + ((lane >> 3) & 1) * 8;
-        ldsm_x4(bs + nrow * (R * 2) + kcol * 2, b0, b1, b2, b3);
+        ldsm_x4(bs + nrow * Cfg::BPITCH + kcol * 2, b0, b1, b2, b3);
         mma_bf16_16816(acc[2 * np], a, b0, b1);
         mma_bf16_16816(acc[2 * np + 1], a, b2, b3);
       }
@@ -344,14 +351,13 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
           __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
     }
   }
-  fence_proxy_async_smem();
   __syncthreads();
-  if (warp == 0) {
-    for (int r = lane; r < t.rows; r += 32)
-      bulk_s2g(yg + (long long)(t.row0 + r) * sl.y_row_stride + o0, Ys + r * Cfg::YPITCH,
-               (uint32_t)ovalid * 2);
-    bulk_commit();
-    bulk_wait_all();
+  // Routed rows of the block back to y, 16 bytes per thread per step.
+  const int ych = ovalid / 8;
+  for (int c = threadIdx.x; c < t.rows * ych; c += blockDim.x) {
+    const int r = c / ych, ch = c - r * ych;
+    *reinterpret_cast<uint4*>(yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8) =
+        *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
   }
 }
 

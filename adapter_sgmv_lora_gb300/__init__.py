@@ -8,7 +8,8 @@ library cannot be loaded, every call raises.
 
 Names follow the C ABI: ``lora_build_routing``, ``lora_set_slot``,
 ``lora_shrink``, ``lora_expand``, ``lora_workspace_bytes``,
-``lora_sgmv_apply``, ``lora_get_device_status``, ``lora_status_string``.
+``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_get_device_status``,
+``lora_status_string``.
 """
 from __future__ import annotations
 
@@ -90,6 +91,8 @@ def lib():
     L.lora_sgmv_apply.restype = ctypes.c_int
     L.lora_sgmv_apply.argtypes = [ctypes.POINTER(_Problem), ctypes.POINTER(_Routing), vp,
                                   ctypes.c_size_t, vp]
+    L.lora_sgmv_apply_noalloc.restype = ctypes.c_int
+    L.lora_sgmv_apply_noalloc.argtypes = [ctypes.POINTER(_Problem), ctypes.POINTER(_Routing), vp]
     L.lora_get_device_status.restype = ctypes.c_int
     L.lora_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.lora_status_string.restype = ctypes.c_char_p
@@ -275,6 +278,19 @@ def lora_sgmv_apply(problem: Problem, routing: Routing, workspace, stream=None) 
     _check(L.lora_sgmv_apply(ctypes.byref(c), ctypes.byref(rr),
                              workspace.data_ptr() if workspace is not None else None, nbytes,
                              _stream_handle(stream)), "lora_sgmv_apply")
+
+
+NOALLOC_MAX_WORKSPACE_BYTES = 16 * 1024 * 1024
+
+
+def lora_sgmv_apply_noalloc(problem: Problem, routing: Routing, stream=None) -> None:
+    """lora_sgmv_apply without a workspace argument, for callers that cannot
+    allocate device memory: the intermediate lives in a fixed 16 MiB array
+    inside the library.  Calls whose GPU work overlaps race on that array."""
+    L = lib()
+    c, rr = problem._c(), routing._c()
+    _check(L.lora_sgmv_apply_noalloc(ctypes.byref(c), ctypes.byref(rr), _stream_handle(stream)),
+           "lora_sgmv_apply_noalloc")
 
 
 def lora_get_device_status(stream=None) -> int:

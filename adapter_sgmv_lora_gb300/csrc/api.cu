@@ -3,6 +3,7 @@
 // The routing builder (lora_build_routing) lives in routing.cpp.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
@@ -198,4 +199,68 @@ extern "C" const char* lora_status_string(lora_status_t status) {
     case LORA_ERR_DEVICE_CHECK: return "LORA_ERR_DEVICE_CHECK: device-side routing check failed";
   }
   return "unknown lora_status_t";
+}
+
+// ---------------------------------------------------------------------------
+// lora_sgmv_apply_noalloc: the same shrink + expand as lora_sgmv_apply, with
+// the fp32 intermediate held in a fixed array compiled into the library
+// instead of a caller-provided workspace.  For callers that cannot allocate
+// device memory at all (see the header).
+//
+// The array is a file-scope __device__ variable: every GPU that loads this
+// library holds it until the process exits.  Its name in host code is only a
+// host-side stand-in, so the device address is looked up once per device
+// with cudaGetSymbolAddress (with that device current) and cached.
+// ---------------------------------------------------------------------------
+namespace lora {
+namespace {
+
+constexpr size_t kStaticWorkspaceFloats = LORA_NOALLOC_MAX_WORKSPACE_BYTES / sizeof(float);
+static_assert(kStaticWorkspaceFloats * sizeof(float) == LORA_NOALLOC_MAX_WORKSPACE_BYTES,
+              "the limit must be a whole number of floats");
+
+static __device__ __align__(256) float g_static_workspace[kStaticWorkspaceFloats];
+
+std::mutex g_static_mu;
+float* g_static_ptr[64] = {nullptr};
+
+// Device address of the static workspace on the current device (nullptr on
+// failure).  First call per device does the lookup.
+float* static_workspace_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return nullptr;
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  return g_static_ptr[dev];
+}
+
+}  // namespace
+}  // namespace lora
+
+extern "C" lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem,
+                                                 const lora_routing_t* routing,
+                                                 lora_stream_t stream) {
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
+  if (is_noop(routing)) return LORA_OK;
+  // Every byte of the intermediate that the expand reads is written by the
+  // shrink of the same call, so nothing in the array has to start at zero.
+  if (ws_bytes(problem, routing->end) > lora::kStaticWorkspaceFloats * sizeof(float))
+    return LORA_ERR_WORKSPACE;
+  float* u = static_workspace_ptr();
+  if (!u) return LORA_ERR_CUDA;
+  ProblemDesc d = make_desc(problem, routing);
+  if (!d.status) return LORA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fast_path_ok(d, u)) {
+    if ((st = cuda_status(launch_shrink_bf16(d, u, s))) != LORA_OK) return st;
+    return cuda_status(launch_expand_bf16(d, u, s, true));
+  }
+  if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
+  return cuda_status(launch_expand_simple(d, u, s, true));
 }

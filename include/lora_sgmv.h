@@ -209,6 +209,34 @@ lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_
                               void* workspace, size_t workspace_bytes, lora_stream_t stream);
 
 /*
+ * lora_sgmv_apply_noalloc -- lora_sgmv_apply for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point.
+ *
+ * Some callers cannot call cudaMalloc: plug-ins living inside a host
+ * framework that owns every device allocation (and gives them none), or
+ * latency-critical loops where an allocation could stall or fail.  This call
+ * takes no workspace argument and allocates nothing; the fp32 intermediate
+ * lives in a fixed array of LORA_NOALLOC_MAX_WORKSPACE_BYTES compiled into the
+ * library (every GPU that loads the library holds it until the process exits).
+ *
+ * Same problem, routing, results and errors as lora_sgmv_apply, plus:
+ *   - LORA_ERR_WORKSPACE if lora_workspace_bytes(problem, end) exceeds
+ *     LORA_NOALLOC_MAX_WORKSPACE_BYTES (use lora_sgmv_apply with your own
+ *     workspace for such batches).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; LORA_ERR_CUDA if the lookup fails.
+ *     Make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its own
+ *     intermediate in it.  Nothing has to start at zero (each call writes
+ *     every value it later reads), but calls whose GPU work overlaps -- on
+ *     different streams, or from different threads -- race on the array.
+ *     Serialize them (one stream, or events).
+ */
+#define LORA_NOALLOC_MAX_WORKSPACE_BYTES (16u * 1024u * 1024u)
+lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem, const lora_routing_t* routing,
+                                      lora_stream_t stream);
+
+/*
  * lora_get_device_status -- synchronizes `stream`, then reads and clears the
  * device status word of the current device (an OR of LORA_DEV_* flags from
  * every launch since the last read).  Returns LORA_ERR_CUDA if the

@@ -91,27 +91,39 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   const int k0 = crank * Kc;
   const int nst = Kc / KS;
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
-  const int chunks = (t.rows + nvalid) * (KS / 8);  // 16-byte chunks per stage
+  // Staged rows: the tile's x rows, then the slot's nvalid A rows.  Thread
+  // `tid` always copies 16-byte column `tid % 8` of rows tid/8, tid/8 + 16,
+  // ... so its source pointers and destinations are fixed for every stage
+  // and only advance by the stage's K offset: computed once, here.
+  constexpr int MAXR = (MT + NB + 15) / 16;  // rows per thread
+  const int nrows_total = t.rows + nvalid;
+  const int ch = threadIdx.x & 7;
+  const __nv_bfloat16* srcs[MAXR];
+  uint32_t dsts[MAXR];
+#pragma unroll
+  for (int i = 0; i < MAXR; ++i) {
+    const int row = (threadIdx.x >> 3) + 16 * i;
+    srcs[i] = nullptr;
+    dsts[i] = 0;
+    if (row < t.rows) {
+      srcs[i] = xg + (long long)(t.row0 + row) * p.x_row_stride + k0 + ch * 8;
+      dsts[i] = row * XPITCH + ch * 16;
+    } else if (row < nrows_total) {
+      const int col = n0 + row - t.rows;
+      const int j = col / R, k = col - j * R;
+      srcs[i] = static_cast<const __nv_bfloat16*>(p.sl[j].A) + (long long)t.slot * p.sl[j].A_slot_stride +
+                (long long)k * p.in_dim + k0 + ch * 8;
+      dsts[i] = (MT + row - t.rows) * XPITCH + ch * 16;
+    }
+  }
+  (void)warp;
 
   auto issue = [&](int s) {
     uint8_t* xs = smem + (s % NSTAGE) * Cfg::STAGE_BYTES;
-    const long long kk = (long long)k0 + (long long)s * KS;
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-      const int row = c >> 3, ch = c & 7;
-      const __nv_bfloat16* src;
-      int drow;  // x rows occupy [0, MT) of the stage, A rows [MT, MT + NB)
-      if (row < t.rows) {
-        src = xg + (long long)(t.row0 + row) * p.x_row_stride + kk + ch * 8;
-        drow = row;
-      } else {
-        const int col = n0 + row - t.rows;
-        const int j = col / R, k = col - j * R;
-        src = static_cast<const __nv_bfloat16*>(p.sl[j].A) + (long long)t.slot * p.sl[j].A_slot_stride +
-              (long long)k * p.in_dim + kk + ch * 8;
-        drow = MT + (row - t.rows);
-      }
-      cp_async16(xs + drow * XPITCH + ch * 16, src);
-    }
+    const int kk = s * KS;
+#pragma unroll
+    for (int i = 0; i < MAXR; ++i)
+      if (srcs[i]) cp_async16(xs + dsts[i], srcs[i] + kk);
   };
 
 #pragma unroll 1

@@ -277,32 +277,32 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(sl.B) + (long long)t.slot * sl.B_slot_stride +
                             (long long)o0 * R;
 
-  // y block and B block do not depend on the shrink: fetch them first.
-  {
-    const int ych = ovalid / 8;  // 16-byte chunks per y row
-    const int ny = t.rows * ych;
-    constexpr int BCH = R / 8;   // chunks per B row
-    const int nbc = ovalid * BCH;
-    for (int c = threadIdx.x; c < ny + nbc; c += blockDim.x) {
-      if (c < ny) {
-        const int r = c / ych, ch = c - r * ych;
-        cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8);
-      } else {
-        const int e = c - ny;
-        const int o = e / BCH, ch = e - o * BCH;
-        cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
-      }
-    }
-    cp_async_commit();
+  // y block and B block do not depend on the shrink: fetch them first.  All
+  // chunk loops run over compile-time row widths (OB/8 chunks per y row, R/8
+  // per B row) so the row/column split is a shift; chunks past a partial
+  // block's width are skipped.
+  constexpr int YW = OB / 8;  // 16-byte chunks per full y row
+  constexpr int BW = R / 8;   // chunks per B row
+  const int ych = ovalid / 8;
+  for (int c = threadIdx.x; c < t.rows * YW; c += blockDim.x) {
+    const int r = c / YW, ch = c % YW;
+    if (ch < ych)
+      cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8);
   }
+  for (int c = threadIdx.x; c < ovalid * BW; c += blockDim.x) {
+    const int o = c / BW, ch = c % BW;
+    cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
+  }
+  cp_async_commit();
 
   pdl_wait();  // the shrink grid (if any) has finished and its u is visible
 
   {
     constexpr int UCH = R / 4;  // 16-byte chunks per u row slice
+    const float* ug = u + (long long)t.row0 * nR + (long long)j * R;
     for (int c = threadIdx.x; c < t.rows * UCH; c += blockDim.x) {
-      const int r = c / UCH, ch = c - r * UCH;
-      cp_async16(Us + r * R + ch * 4, u + (long long)(t.row0 + r) * nR + (long long)j * R + ch * 4);
+      const int r = c / UCH, ch = c % UCH;
+      cp_async16(Us + r * R + ch * 4, ug + (long long)r * nR + ch * 4);
     }
     cp_async_commit();
   }
@@ -365,11 +365,11 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   }
   __syncthreads();
   // Routed rows of the block back to y, 16 bytes per thread per step.
-  const int ych = ovalid / 8;
-  for (int c = threadIdx.x; c < t.rows * ych; c += blockDim.x) {
-    const int r = c / ych, ch = c - r * ych;
-    *reinterpret_cast<uint4*>(yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8) =
-        *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
+  for (int c = threadIdx.x; c < t.rows * YW; c += blockDim.x) {
+    const int r = c / YW, ch = c % YW;
+    if (ch < ych)
+      *reinterpret_cast<uint4*>(yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8) =
+          *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
   }
 }
 

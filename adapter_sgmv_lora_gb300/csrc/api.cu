@@ -85,8 +85,18 @@ lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : L
 
 bool is_noop(const lora_routing_t* r) { return r->num_groups == 0 || r->end == 0; }
 
-size_t ws_bytes(const lora_problem_t* p, int32_t end) {
+// One fp32 plane of the intermediate u [end, n*R].
+size_t plane_bytes(const lora_problem_t* p, int32_t end) {
   const size_t raw = (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices * (size_t)p->max_lora_rank * 4;
+  return (raw + 255) & ~(size_t)255;
+}
+
+// lora_sgmv_apply's workspace: its shrink may split the input dimension into
+// up to 8 partial planes (apply_splits), summed by the expand.
+size_t ws_bytes(const lora_problem_t* p, int32_t end) {
+  const int splits = apply_splits(end, p->in_dim, p->num_slices * p->max_lora_rank);
+  const size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
+                     (size_t)p->max_lora_rank * 4;
   return (raw + 255) & ~(size_t)255;
 }
 
@@ -140,7 +150,7 @@ extern "C" lora_status_t lora_expand(const lora_problem_t* problem, const lora_r
   ProblemDesc d = make_desc(problem, routing);
   if (!d.status) return LORA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fast_path_ok(d, u)) return cuda_status(launch_expand_bf16(d, u, s, false));
+  if (fast_path_ok(d, u)) return cuda_status(launch_expand_bf16(d, u, s, false, 1));
   return cuda_status(launch_expand_simple(d, u, s, false));
 }
 
@@ -163,8 +173,9 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* u = static_cast<float*>(workspace);
   if (fast_path_ok(d, u)) {
-    if ((st = cuda_status(launch_shrink_bf16(d, u, s))) != LORA_OK) return st;
-    return cuda_status(launch_expand_bf16(d, u, s, true));
+    const int splits = apply_splits(d.end, d.in_dim, d.n_slices * d.R);
+    if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s))) != LORA_OK) return st;
+    return cuda_status(launch_expand_bf16(d, u, s, true, splits));
   }
   if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
   return cuda_status(launch_expand_simple(d, u, s, true));
@@ -250,7 +261,7 @@ extern "C" lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem,
   if (is_noop(routing)) return LORA_OK;
   // Every byte of the intermediate that the expand reads is written by the
   // shrink of the same call, so nothing in the array has to start at zero.
-  if (ws_bytes(problem, routing->end) > lora::kStaticWorkspaceFloats * sizeof(float))
+  if (plane_bytes(problem, routing->end) > lora::kStaticWorkspaceFloats * sizeof(float))
     return LORA_ERR_WORKSPACE;
   float* u = static_workspace_ptr();
   if (!u) return LORA_ERR_CUDA;
@@ -259,7 +270,7 @@ extern "C" lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (fast_path_ok(d, u)) {
     if ((st = cuda_status(launch_shrink_bf16(d, u, s))) != LORA_OK) return st;
-    return cuda_status(launch_expand_bf16(d, u, s, true));
+    return cuda_status(launch_expand_bf16(d, u, s, true, 1));
   }
   if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
   return cuda_status(launch_expand_simple(d, u, s, true));

@@ -50,7 +50,13 @@ cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, fl
 // bf16 fast path (tensor cores + bulk copies + clusters).  `fast_path_ok`
 // tells whether a problem meets its alignment / size preconditions.
 bool fast_path_ok(const ProblemDesc& p, const void* u);
+// launch_shrink_bf16 writes the final u (cluster reduction);
+// launch_shrink_partial_bf16 writes apply_splits(...) partial planes of u,
+// plane c at u + c * end * n * R, which launch_expand_bf16 sums (nsplit).
 cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
-cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl);
+cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
+cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit);
+// Partial planes the apply's shrink uses for this shape (1..8); shapes only.
+int apply_splits(int end, int in_dim, int nR);
 
 }  // namespace lora

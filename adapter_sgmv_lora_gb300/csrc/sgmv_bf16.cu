@@ -53,11 +53,14 @@ struct ShrinkCfg {
 
 }  // namespace
 
-// grid.x = C * nblk * n_tiles_max, cluster (C,1,1) when C > 1.
+// grid.x = C * nblk * n_tiles_max.  plane_stride == 0: cluster (C,1,1), the
+// C partials are reduced through distributed shared memory into u.
+// plane_stride > 0: no cluster; K-split rank c stores its partial tile into
+// plane c (u + c * plane_stride) and the expand sums the planes.
 template <int NB>
 __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                float* __restrict__ u, int C,
-                                                               int nblk, int Kc) {
+                                                               int nblk, int Kc, long long plane_stride) {
   using Cfg = ShrinkCfg<NB>;
   constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -180,6 +183,17 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
       *reinterpret_cast<float2*>(&P[(row + 8) * Cfg::PPITCH + col]) = make_float2(acc[nt][2], acc[nt][3]);
     }
   }
+  const int q4 = nvalid / 4;
+  if (plane_stride > 0) {
+    __syncthreads();
+    float* up = u + crank * plane_stride;
+    for (int e = threadIdx.x; e < t.rows * q4; e += blockDim.x) {
+      const int r = e / q4, c = (e % q4) * 4;
+      *reinterpret_cast<float4*>(&up[(long long)(t.row0 + r) * nR + n0 + c]) =
+          *reinterpret_cast<const float4*>(&P[r * Cfg::PPITCH + c]);
+    }
+    return;
+  }
   if (C > 1)
     cluster_sync();
   else
@@ -191,7 +205,6 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   const int rpc = MT / C;
   const int r_lo = crank * rpc;
   const int r_hi = min(r_lo + rpc, t.rows);
-  const int q4 = nvalid / 4;
   const int cnt = (r_hi - r_lo) * q4;
   for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
     const int r = r_lo + e / q4, c = (e % q4) * 4;
@@ -228,20 +241,21 @@ struct ExpandCfg {
   static constexpr int UPITCH = 4 * R + 16;   // bytes per hi|lo row (2R bf16)
   static constexpr int Y_OFF = 0;
   static constexpr int B_OFF = MT * YPITCH;
-  static constexpr int U_OFF = B_OFF + OB * BPITCH;
-  static constexpr int H_OFF = U_OFF + MT * R * 4;
+  static constexpr int H_OFF = B_OFF + OB * BPITCH;
   static constexpr int SMEM = H_OFF + MT * UPITCH;
 };
 
 struct ExpandMap {
   int n_ob_total;                     // output blocks per tile, all slices
   int ob_begin[LORA_MAX_SLICES + 1];  // first output block of each slice
+  int nsplit;                         // partial planes of u to sum (1..8)
+  long long plane_stride;             // elements between planes
 };
 
 template <int R, int OB>
 __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                const float* __restrict__ u,
-                                                               const ExpandMap map) {
+                                                               const __grid_constant__ ExpandMap map) {
   using Cfg = ExpandCfg<R, OB>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Tile s_tile;
@@ -271,7 +285,6 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 
   uint8_t* Ys = smem + Cfg::Y_OFF;
   uint8_t* Bs = smem + Cfg::B_OFF;
-  float* Us = reinterpret_cast<float*>(smem + Cfg::U_OFF);
   uint8_t* Hs = smem + Cfg::H_OFF;
   __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(sl.y);
   const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(sl.B) + (long long)t.slot * sl.B_slot_stride +
@@ -297,27 +310,38 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 
   pdl_wait();  // the shrink grid (if any) has finished and its u is visible
 
+  // u (sum of the nsplit planes, in plane order) -> hi + lo bf16: u = hi + lo
+  // to 16 significant bits; the subtraction is exact.  Read through L2 only.
   {
-    constexpr int UCH = R / 4;  // 16-byte chunks per u row slice
-    const float* ug = u + (long long)t.row0 * nR + (long long)j * R;
-    for (int c = threadIdx.x; c < t.rows * UCH; c += blockDim.x) {
-      const int r = c / UCH, ch = c % UCH;
-      cp_async16(Us + r * R + ch * 4, ug + (long long)r * nR + ch * 4);
+    constexpr int R4 = R / 4;
+    const float* ub = u + (long long)t.row0 * nR + (long long)j * R;
+    for (int e = threadIdx.x; e < t.rows * R4; e += blockDim.x) {
+      const int r = e / R4, k = (e % R4) * 4;
+      const float* src = ub + (long long)r * nR + k;
+      float4 part[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < map.nsplit) part[q] = __ldcg(reinterpret_cast<const float4*>(src + q * map.plane_stride));
+      float4 v = part[0];
+#pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < map.nsplit) {
+          v.x += part[q].x;
+          v.y += part[q].y;
+          v.z += part[q].z;
+          v.w += part[q].w;
+        }
+      const float vals[4] = {v.x, v.y, v.z, v.w};
+      __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(vals[i]);
+        hrow[k + i] = hi;
+        hrow[R + k + i] = __float2bfloat16_rn(vals[i] - __bfloat162float(hi));
+      }
     }
-    cp_async_commit();
   }
   cp_async_wait<0>();
-  __syncthreads();
-  // u -> hi + lo bf16 (u = hi + lo to 16 significant bits; the subtraction is exact).
-  for (int e = threadIdx.x; e < t.rows * R; e += blockDim.x) {
-    const int r = e / R, k = e % R;
-    const float v = Us[r * R + k];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-    __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
-    hrow[k] = hi;
-    hrow[R + k] = lo;
-  }
   __syncthreads();
 
   const int m = warp & 3, nh = warp >> 2;
@@ -422,18 +446,24 @@ int num_sms() {
 }
 
 template <int NB>
-cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk) {
+cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
   auto kernel = sgmv_shrink_bf16_kernel<NB>;
   const int smem = ShrinkCfg<NB>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)p.G + p.end / MT;
-  // Split the input dimension over a cluster until the grid covers the GPU.
-  const int ksteps = p.in_dim / KS;
   int C = 1;
-  const long long target = 2LL * num_sms();
-  while (C < 8 && tiles * nblk * C * 2 <= target && ksteps % (C * 2) == 0) C *= 2;
+  long long plane_stride = 0;
+  if (partial) {
+    C = apply_splits(p.end, p.in_dim, p.n_slices * p.R);
+    if (C > 1) plane_stride = (long long)p.end * p.n_slices * p.R;
+  } else {
+    // Split the input dimension over a cluster until the grid covers the GPU.
+    const int ksteps = p.in_dim / KS;
+    const long long target = 2LL * num_sms();
+    while (C < 8 && tiles * nblk * C * 2 <= target && ksteps % (C * 2) == 0) C *= 2;
+  }
   const int Kc = p.in_dim / C;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * nblk * C));
@@ -441,7 +471,7 @@ cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  if (C > 1) {
+  if (C > 1 && !partial) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
@@ -449,11 +479,11 @@ cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc);
+  return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride);
 }
 
 template <int R, int OB>
-cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl) {
+cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
   auto kernel = sgmv_expand_bf16_kernel<R, OB>;
   const int smem = ExpandCfg<R, OB>::SMEM;
   static unsigned long long done = 0;
@@ -467,6 +497,8 @@ cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s
   }
   map.ob_begin[p.n_slices] = acc;
   map.n_ob_total = acc;
+  map.nsplit = nsplit;
+  map.plane_stride = (long long)p.end * p.n_slices * R;
   const long long tiles = (long long)p.G + p.end / MT;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * acc));
@@ -500,25 +532,48 @@ bool fast_path_ok(const ProblemDesc& p, const void* u) {
   return true;
 }
 
-cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s) {
+int apply_splits(int end, int in_dim, int nR) {
+  // Largest power of two <= 8 dividing the input stages such that the
+  // partial-plane shrink grid (a lower bound on its tiles: ceil(end / 64))
+  // stays within 256 CTAs.  Depends on shapes only, so the workspace bound
+  // can be computed without a device.
+  if (end <= 0 || in_dim % KS != 0) return 1;
+  int nblk = 1;
+  (void)pick_nb(nR, &nblk);
+  const long long tiles = (end + MT - 1) / MT;
+  const int ksteps = in_dim / KS;
+  int C = 1;
+  while (C < 8 && tiles * nblk * C * 2 <= 256 && ksteps % (C * 2) == 0) C *= 2;
+  return C;
+}
+
+static cudaError_t dispatch_shrink(const ProblemDesc& p, float* u, cudaStream_t s, bool partial) {
   int nblk = 1;
   const int nb = pick_nb(p.n_slices * p.R, &nblk);
   switch (nb) {
-    case 16: return launch_shrink_nb<16>(p, u, s, nblk);
-    case 32: return launch_shrink_nb<32>(p, u, s, nblk);
-    case 48: return launch_shrink_nb<48>(p, u, s, nblk);
-    case 64: return launch_shrink_nb<64>(p, u, s, nblk);
-    case 96: return launch_shrink_nb<96>(p, u, s, nblk);
-    default: return launch_shrink_nb<128>(p, u, s, nblk);
+    case 16: return launch_shrink_nb<16>(p, u, s, nblk, partial);
+    case 32: return launch_shrink_nb<32>(p, u, s, nblk, partial);
+    case 48: return launch_shrink_nb<48>(p, u, s, nblk, partial);
+    case 64: return launch_shrink_nb<64>(p, u, s, nblk, partial);
+    case 96: return launch_shrink_nb<96>(p, u, s, nblk, partial);
+    default: return launch_shrink_nb<128>(p, u, s, nblk, partial);
   }
 }
 
-cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl) {
+cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s) {
+  return dispatch_shrink(p, u, s, false);
+}
+
+cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s) {
+  return dispatch_shrink(p, u, s, true);
+}
+
+cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
   switch (p.R) {
-    case 16: return launch_expand_r<16, 256>(p, u, s, pdl);
-    case 32: return launch_expand_r<32, 256>(p, u, s, pdl);
-    case 64: return launch_expand_r<64, 128>(p, u, s, pdl);
-    default: return launch_expand_r<128, 64>(p, u, s, pdl);
+    case 16: return launch_expand_r<16, 256>(p, u, s, pdl, nsplit);
+    case 32: return launch_expand_r<32, 256>(p, u, s, pdl, nsplit);
+    case 64: return launch_expand_r<64, 128>(p, u, s, pdl, nsplit);
+    default: return launch_expand_r<128, 64>(p, u, s, pdl, nsplit);
   }
 }
 

@@ -175,6 +175,17 @@ def test_rank_variants_ragged_tiles(R, mode):
     run_case(sy.draw(spec, 4), "o", mode=mode)
 
 
+@pytest.mark.parametrize("R", [16, 32])
+def test_apply_split_planes_ragged_groups(R):
+    """The apply's shrink splits K into partial planes for small batches;
+    groups of 1, 31, 32, 33, 64, 70 and 100 rows, input width 1024."""
+    spec = _spec(max_num_loras=7, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
+                 fixed_slots=(6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 31, 32, 33, 64, 70, 100, 5),
+                 hidden=1024, n_heads=16, n_kv_heads=4, head_dim=64)
+    run_case(sy.draw(spec, 5), "qkv", mode="apply")
+    run_case(sy.draw(spec, 6), "o", mode="apply")
+
+
 def test_all_base_is_noop():
     spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(3, 4))
     dev = run_case(sy.draw(spec, 0), "qkv")

@@ -94,7 +94,9 @@ size_t plane_bytes(const lora_problem_t* p, int32_t end) {
 // lora_sgmv_apply's workspace: its shrink may split the input dimension into
 // up to 8 partial planes (apply_splits), summed by the expand.
 size_t ws_bytes(const lora_problem_t* p, int32_t end) {
-  const int splits = apply_splits(end, p->in_dim, p->num_slices * p->max_lora_rank);
+  int splits = apply_splits(end, p->in_dim, p->num_slices * p->max_lora_rank);
+  const int tc = tc_shrink_splits(end, p->in_dim);
+  if (tc > splits) splits = tc;
   const size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
                      (size_t)p->max_lora_rank * 4;
   return (raw + 255) & ~(size_t)255;
@@ -136,7 +138,13 @@ extern "C" lora_status_t lora_shrink(const lora_problem_t* problem, const lora_r
   ProblemDesc d = make_desc(problem, routing);
   if (!d.status) return LORA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fast_path_ok(d, u)) return cuda_status(launch_shrink_bf16(d, u, s));
+  if (fast_path_ok(d, u)) {
+    if (tc_shrink_ok(d)) {
+      const cudaError_t e = launch_tc_shrink(d, u, s, 1);
+      if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    return cuda_status(launch_shrink_bf16(d, u, s));
+  }
   return cuda_status(launch_shrink_simple(d, u, s));
 }
 
@@ -173,6 +181,14 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* u = static_cast<float*>(workspace);
   if (fast_path_ok(d, u)) {
+    if (tc_shrink_ok(d)) {
+      const int tcs = tc_shrink_splits(d.end, d.in_dim);
+      const cudaError_t e = launch_tc_shrink(d, u, s, tcs);
+      if (e != cudaErrorNotSupported) {
+        if (e != cudaSuccess) return LORA_ERR_CUDA;
+        return cuda_status(launch_expand_bf16(d, u, s, true, tcs));
+      }
+    }
     const int splits = apply_splits(d.end, d.in_dim, d.n_slices * d.R);
     if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s))) != LORA_OK) return st;
     return cuda_status(launch_expand_bf16(d, u, s, true, splits));

@@ -59,4 +59,13 @@ cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_
 // Partial planes the apply's shrink uses for this shape (1..8); shapes only.
 int apply_splits(int end, int in_dim, int nR);
 
+// tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
+// nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says
+// whether the shape and routing suit it; tc_shrink_splits(end, in) is its
+// plane count (shape-only).  Returns cudaErrorNotSupported when the tensor
+// maps cannot be encoded (nothing launched).
+bool tc_shrink_ok(const ProblemDesc& p);
+int tc_shrink_splits(int end, int in_dim);
+cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int nsplit);
+
 }  // namespace lora

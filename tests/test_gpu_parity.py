@@ -149,8 +149,9 @@ def test_many64_separate_outputs():
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
-def test_prefill8b_sampled(proj):
-    run_case(sy.draw("prefill8b", 0), proj, mode="split", rows="sample")
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_prefill8b_sampled(proj, mode):
+    run_case(sy.draw("prefill8b", 0), proj, mode=mode, rows="sample")
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
@@ -184,6 +185,18 @@ def test_apply_split_planes_ragged_groups(R):
                  hidden=1024, n_heads=16, n_kv_heads=4, head_dim=64)
     run_case(sy.draw(spec, 5), "qkv", mode="apply")
     run_case(sy.draw(spec, 6), "o", mode="apply")
+
+
+@pytest.mark.parametrize("R", [16, 32, 64, 128])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_long_groups_tensor_core_shrink(R, mode):
+    """Long groups (the tcgen05 shrink): 128-row tiles with ragged ends,
+    lengths 100, 127, 128, 129, 300 and 1000."""
+    spec = _spec(max_num_loras=6, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
+                 fixed_slots=(5, 4, 3, 2, 1, 0, -1), fixed_lens=(100, 127, 128, 129, 300, 1000, 7),
+                 hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
+    run_case(sy.draw(spec, 7), "qkv", mode=mode)
+    run_case(sy.draw(spec, 8), "o", mode=mode)
 
 
 def test_all_base_is_noop():

@@ -158,7 +158,13 @@ extern "C" lora_status_t lora_expand(const lora_problem_t* problem, const lora_r
   ProblemDesc d = make_desc(problem, routing);
   if (!d.status) return LORA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fast_path_ok(d, u)) return cuda_status(launch_expand_bf16(d, u, s, false, 1));
+  if (fast_path_ok(d, u)) {
+    if (tc_expand_ok(d)) {
+      const cudaError_t e = launch_tc_expand(d, u, s, false, 1);
+      if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    return cuda_status(launch_expand_bf16(d, u, s, false, 1));
+  }
   return cuda_status(launch_expand_simple(d, u, s, false));
 }
 
@@ -186,6 +192,10 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
       const cudaError_t e = launch_tc_shrink(d, u, s, tcs);
       if (e != cudaErrorNotSupported) {
         if (e != cudaSuccess) return LORA_ERR_CUDA;
+        if (tc_expand_ok(d)) {
+          const cudaError_t e2 = launch_tc_expand(d, u, s, true, tcs);
+          if (e2 != cudaErrorNotSupported) return cuda_status(e2);
+        }
         return cuda_status(launch_expand_bf16(d, u, s, true, tcs));
       }
     }

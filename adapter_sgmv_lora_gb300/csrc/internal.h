@@ -67,5 +67,8 @@ int apply_splits(int end, int in_dim, int nR);
 bool tc_shrink_ok(const ProblemDesc& p);
 int tc_shrink_splits(int end, int in_dim);
 cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int nsplit);
+// tcgen05 expand for long groups with R = 64 or 128 (sums nsplit planes of u).
+bool tc_expand_ok(const ProblemDesc& p);
+cudaError_t launch_tc_expand(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit);
 
 }  // namespace lora

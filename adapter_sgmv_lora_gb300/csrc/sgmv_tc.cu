@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   __shared__ int s_ok;
   __shared__ int s_fail;
 
-  pdl_launch_dependents();
   // 1024-byte aligned ring (the 128-byte swizzle repeats every 1024 bytes).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -101,6 +100,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Dependents (the expand) may start only once this CTA holds its TMEM, so
+  // a waiting expand CTA can never hold columns this shrink still needs.
+  pdl_launch_dependents();
   const uint32_t tmem = s_tmem;
   const Tile t = s_tile;
   const bool ok = s_ok != 0;
@@ -291,6 +293,334 @@ cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int
     case 384: return launch_tc_t<384>(p, maps, u, s, nsplit);
   }
   return cudaErrorNotSupported;
+}
+
+}  // namespace lora
+
+// ===========================================================================
+// Expand on tcgen05 for long groups (R = 64 or 128):
+//   y_j[t, o] = rn(y_j[t, o] + sum_k B_j[s, o, k] u[t, j*R+k])
+// One CTA per (128-row tile, slice j, chunk of up to 8 output blocks of 128
+// columns).  Warps 2-5 first sum the u planes of their row and write u as
+// bf16 hi | lo (K = 2R) straight into the 128-byte-swizzled K-major layout
+// the MMA reads; warp 0 streams each block's y (two 64-column boxes) and B
+// (R/64 boxes of 128 rows) through two smem slots with TMA; warp 1 issues
+// tcgen05.mma M=128 N=128 K=2R into one of two TMEM buffers; warps 2-5 add
+// the TMEM delta to the swizzled y block, round once and store the routed
+// rows (16-byte stores; rows past the group are never written).
+// ===========================================================================
+namespace lora {
+
+namespace {
+
+constexpr int XB = 128;     // output columns per block (MMA N)
+constexpr int XCHUNK = 8;   // blocks per CTA
+
+template <int R>
+struct TxCfg {
+  static constexpr int KB = 2 * R / 64;               // 64-wide K blocks of the hi|lo operand
+  static constexpr int U_BYTES = KB * TM * 128;       // A operand (u hi|lo)
+  static constexpr int Y_BYTES = 2 * TM * 128;        // two 64-column y boxes
+  static constexpr int B_BYTES = (R / 64) * XB * 128; // R/64 boxes of 128 rows x 64
+  static constexpr int SLOT = Y_BYTES + B_BYTES;
+  static constexpr int SMEM = U_BYTES + 2 * SLOT + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * XB;
+};
+
+// Byte offset of bf16 element (row r, k) in a K-major operand made of
+// [128 rows x 64] blocks with the 128-byte swizzle (16-byte chunk c of row r
+// stored at chunk c ^ (r % 8)).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
+  const int kb = k >> 6, kk = k & 63;
+  return (uint32_t)(kb * TM * 128 + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + ((kk & 7) << 1));
+}
+
+}  // namespace
+
+struct TxMaps {
+  CUtensorMap y[LORA_MAX_SLICES];  // [T rows, out_j] bf16, box 64 x 128
+  CUtensorMap b[LORA_MAX_SLICES];  // [S, out_j, R] bf16, box 64 x 128 x 1
+};
+
+struct TxWork {
+  int n_chunks;                          // chunks per tile, all slices
+  int chunk_begin[LORA_MAX_SLICES + 1];  // first chunk of each slice
+  int nsplit;                            // partial planes of u
+  long long plane_stride;
+};
+
+template <int R>
+__global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __grid_constant__ ProblemDesc p,
+                                                                    const __grid_constant__ TxMaps maps,
+                                                                    const __grid_constant__ TxWork w,
+                                                                    const float* __restrict__ u) {
+  using Cfg = TxCfg<R>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[2], empty[2], tfull[2], tempty[2], uready;
+  __shared__ uint32_t s_tmem;
+  __shared__ Tile s_tile;
+  __shared__ int s_ok, s_fail;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ua = smem;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long tile = blockIdx.x / (unsigned)w.n_chunks;
+  const int cg = (int)(blockIdx.x % (unsigned)w.n_chunks);
+  int j = 0;
+  while (j + 1 < p.n_slices && cg >= w.chunk_begin[j + 1]) ++j;
+  const SliceDesc& sl = p.sl[j];
+  const int b_first = (cg - w.chunk_begin[j]) * XCHUNK;
+  const int nblocks_slice = (sl.out_dim + XB - 1) / XB;
+  const int nblk = min(XCHUNK, nblocks_slice - b_first);
+
+  if (warp == 0) {
+    Tile t{};
+    const bool ok = warp_locate_tile(p, TM, tile, t);
+    if (lane == 0) {
+      s_tile = t;
+      s_ok = ok;
+      s_fail = 0;
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&full[i], 1);
+        mbar_init(&empty[i], 4);
+        mbar_init(&tfull[i], 1);
+        mbar_init(&tempty[i], 4);
+      }
+      mbar_init(&uready, 4 * 32);
+      fence_mbar_init();
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  const Tile t = s_tile;
+  const bool ok = s_ok != 0;
+
+  if (ok && warp == 0 && lane == 0) {
+    // ---- producer: y and B of block i into slot i % 2 (independent of the
+    // shrink, so it starts before the dependency wait).
+    for (int i = 0; i < nblk; ++i) {
+      const int slot = i & 1;
+      if (i >= 2 && !mbar_wait(&empty[slot], (uint32_t)(((i >> 1) - 1) & 1))) {
+        atomicOr(&s_fail, 1);
+        break;
+      }
+      uint8_t* ys = smem + Cfg::U_BYTES + slot * Cfg::SLOT;
+      uint8_t* bs = ys + Cfg::Y_BYTES;
+      const int o0 = (b_first + i) * XB;
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + Cfg::B_BYTES));
+      tma_load_2d(ys, &maps.y[j], o0, t.row0, &full[slot]);
+      tma_load_2d(ys + TM * 128, &maps.y[j], o0 + 64, t.row0, &full[slot]);
+      for (int kb = 0; kb < R / 64; ++kb) tma_load_3d(bs + kb * XB * 128, &maps.b[j], kb * 64, o0, t.slot, &full[slot]);
+    }
+  } else if (ok && warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(TM, XB);
+    const bool ready = mbar_wait(&uready, 0);
+    if (!ready) atomicOr(&s_fail, 1);
+    for (int i = 0; ready && i < nblk; ++i) {
+      const int slot = i & 1;
+      if (!mbar_wait(&full[slot], (uint32_t)((i >> 1) & 1)) ||
+          (i >= 2 && !mbar_wait(&tempty[slot], (uint32_t)(((i >> 1) - 1) & 1)))) {
+        atomicOr(&s_fail, 1);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t ua = smem_addr(Ua);
+      const uint32_t bs = smem_addr(smem + Cfg::U_BYTES + slot * Cfg::SLOT + Cfg::Y_BYTES);
+#pragma unroll
+      for (int ks = 0; ks < 2 * R / 16; ++ks) {
+        const uint64_t adesc = sw128_desc(ua + (ks >> 2) * TM * 128 + (ks & 3) * 32);
+        const int kbk = (ks * 16) % R;  // the lo half reuses B's K columns
+        const uint64_t bdesc = sw128_desc(bs + (kbk >> 6) * XB * 128 + ((kbk & 63) >> 4) * 32);
+        tc_mma_bf16(tmem + slot * XB, adesc, bdesc, idesc, ks > 0 ? 1u : 0u);
+      }
+      tc_commit(&tfull[slot]);
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue warps: thread = one tile row = one TMEM lane
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int nR = p.n_slices * R;
+    if (ok) {
+      pdl_wait();  // u comes from the shrink grid
+      // u row (sum of planes, plane order) -> bf16 hi | lo, swizzled K-major.
+      const bool live = row < t.rows;
+      const float* ur = u + (long long)(t.row0 + (live ? row : 0)) * nR + (long long)j * R;
+      for (int k = 0; k < R; k += 8) {
+        float v[8];
+        if (live) {
+          float4 a0 = __ldcg(reinterpret_cast<const float4*>(ur + k));
+          float4 a1 = __ldcg(reinterpret_cast<const float4*>(ur + k + 4));
+          for (int s = 1; s < w.nsplit; ++s) {
+            const float4 b0 = __ldcg(reinterpret_cast<const float4*>(ur + s * w.plane_stride + k));
+            const float4 b1 = __ldcg(reinterpret_cast<const float4*>(ur + s * w.plane_stride + k + 4));
+            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+          }
+          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+          v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+          hi[i] = pack_bf16x2(h0, h1);
+          lo[i] = pack_bf16x2(__float2bfloat16_rn(v[2 * i] - __bfloat162float(h0)),
+                              __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1)));
+        }
+        *reinterpret_cast<uint4*>(Ua + sw128_offset(row, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(Ua + sw128_offset(row, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();  // generic writes -> visible to the tensor cores
+      mbar_arrive(&uready);
+
+      __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(sl.y) + (long long)(t.row0 + row) * sl.y_row_stride;
+      for (int i = 0; i < nblk; ++i) {
+        const int slot = i & 1;
+        if (!mbar_wait(&tfull[slot], (uint32_t)((i >> 1) & 1))) {
+          atomicOr(&s_fail, 1);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint8_t* ys = smem + Cfg::U_BYTES + slot * Cfg::SLOT;
+        const int o0 = (b_first + i) * XB;
+        const int ovalid = min(XB, sl.out_dim - o0);
+        for (int c16 = 0; c16 < XB / 16; ++c16) {
+          float d[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * XB + c16 * 16), d);
+          if (live && c16 * 16 < ovalid) {
+            uint32_t out[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int cch = c16 * 2 + h;  // 16-byte chunk of the 128-column block
+              const uint4 yv = *reinterpret_cast<const uint4*>(ys + (cch >> 3) * TM * 128 + row * 128 +
+                                                               (((cch & 7) ^ (row & 7)) << 4));
+              const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xFFFF0000u);
+                out[h * 4 + e] = pack_bf16x2(__float2bfloat16_rn(y0 + d[h * 8 + 2 * e]),
+                                             __float2bfloat16_rn(y1 + d[h * 8 + 2 * e + 1]));
+              }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(yrow + o0 + c16 * 16);
+            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            if (c16 * 16 + 8 < ovalid) dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[slot]);
+          mbar_arrive(&empty[slot]);
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    if (s_fail) {
+      for (int i = 0; i < 2; ++i) (void)mbar_wait(&tfull[i], 0);
+      if (lane == 0) atomicOr(p.status, LORA_DEV_TIMEOUT);
+    }
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+namespace {
+
+bool encode_tx_maps(const ProblemDesc& p, TxMaps* m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  for (int j = 0; j < p.n_slices; ++j) {
+    const SliceDesc& sl = p.sl[j];
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)sl.out_dim, (cuuint64_t)p.num_tokens};
+      const cuuint64_t strides[1] = {(cuuint64_t)sl.y_row_stride * 2};
+      const cuuint32_t box[2] = {64, (cuuint32_t)TM};
+      if (enc(&m->y[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, sl.y, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    }
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)p.R, (cuuint64_t)sl.out_dim, (cuuint64_t)p.S};
+      const cuuint64_t strides[2] = {(cuuint64_t)p.R * 2, (cuuint64_t)sl.B_slot_stride * 2};
+      const cuuint32_t box[3] = {64, (cuuint32_t)XB, 1};
+      if (enc(&m->b[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(sl.B), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    }
+  }
+  return true;
+}
+
+template <int R>
+cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& w, const float* u,
+                        cudaStream_t s, bool pdl) {
+  auto kernel = sgmv_tc_expand_kernel<R>;
+  static unsigned long long done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(g_tc_mu);
+    if (!(done & (1ull << (dev & 63)))) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TxCfg<R>::SMEM);
+      if (e != cudaSuccess) return e;
+      done |= 1ull << (dev & 63);
+    }
+  }
+  const long long tiles = (long long)p.G + p.end / TM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * w.n_chunks));
+  cfg.blockDim = dim3(TTHREADS);
+  cfg.dynamicSmemBytes = TxCfg<R>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, p, maps, w, u);
+}
+
+}  // namespace
+
+bool tc_expand_ok(const ProblemDesc& p) {
+  return (p.R == 64 || p.R == 128) && tc_shrink_ok(p);
+}
+
+cudaError_t launch_tc_expand(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
+  TxMaps maps;
+  if (!encode_tx_maps(p, &maps)) return cudaErrorNotSupported;
+  TxWork w{};
+  int acc = 0;
+  for (int j = 0; j < p.n_slices; ++j) {
+    w.chunk_begin[j] = acc;
+    acc += ((p.sl[j].out_dim + XB - 1) / XB + XCHUNK - 1) / XCHUNK;
+  }
+  w.chunk_begin[p.n_slices] = acc;
+  w.n_chunks = acc;
+  w.nsplit = nsplit;
+  w.plane_stride = (long long)p.end * p.n_slices * p.R;
+  if (p.R == 64) return launch_tx_t<64>(p, maps, w, u, s, pdl);
+  return launch_tx_t<128>(p, maps, w, u, s, pdl);
 }
 
 }  // namespace lora

@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   const int nst = kc / TK;
 
   if (ok && warp == 0 && lane == 0) {
-    // ---- producer
+    // ---- producer (x streams through L2 once; the slot's A rows are re-read
+    // by every tile of the group, so they are kept)
+    const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
     for (int s = 0; s < nst; ++s) {
       const int slot = s % NSTAGE;
       if (s >= NSTAGE && !mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1))) {
@@ -123,8 +125,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
       uint8_t* as = xs + Cfg::X_BYTES;
       mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::X_BYTES + p.n_slices * R * TK * 2));
       const int kk = k0 + s * TK;
-      tma_load_2d(xs, &maps.x, kk, t.row0, &full[slot]);
-      for (int j = 0; j < p.n_slices; ++j) tma_load_3d(as + j * R * TK * 2, &maps.a[j], kk, 0, t.slot, &full[slot]);
+      tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
+      for (int j = 0; j < p.n_slices; ++j)
+        tma_load_3d_hint(as + j * R * TK * 2, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
     }
   } else if (ok && warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -323,7 +326,8 @@ struct TxCfg {
   static constexpr int Y_BYTES = 2 * TM * 128;        // two 64-column y boxes
   static constexpr int B_BYTES = (R / 64) * XB * 128; // R/64 boxes of 128 rows x 64
   static constexpr int SLOT = Y_BYTES + B_BYTES;
-  static constexpr int SMEM = U_BYTES + 2 * SLOT + 1024;
+  static constexpr int NSLOT = (U_BYTES + 3 * SLOT + 1024 <= 220 * 1024) ? 3 : 2;  // y/B pipeline depth
+  static constexpr int SMEM = U_BYTES + NSLOT * SLOT + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * XB;
 };
 
@@ -355,8 +359,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
                                                                     const __grid_constant__ TxWork w,
                                                                     const float* __restrict__ u) {
   using Cfg = TxCfg<R>;
+  constexpr int NSLOT = Cfg::NSLOT;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[2], empty[2], tfull[2], tempty[2], uready;
+  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], tfull[2], tempty[2], uready;
   __shared__ uint32_t s_tmem;
   __shared__ Tile s_tile;
   __shared__ int s_ok, s_fail;
@@ -380,9 +385,11 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       s_tile = t;
       s_ok = ok;
       s_fail = 0;
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < NSLOT; ++i) {
         mbar_init(&full[i], 1);
         mbar_init(&empty[i], 4);
+      }
+      for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull[i], 1);
         mbar_init(&tempty[i], 4);
       }
@@ -404,9 +411,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
   if (ok && warp == 0 && lane == 0) {
     // ---- producer: y and B of block i into slot i % 2 (independent of the
     // shrink, so it starts before the dependency wait).
+    const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
     for (int i = 0; i < nblk; ++i) {
-      const int slot = i & 1;
-      if (i >= 2 && !mbar_wait(&empty[slot], (uint32_t)(((i >> 1) - 1) & 1))) {
+      const int slot = i % NSLOT;
+      if (i >= NSLOT && !mbar_wait(&empty[slot], (uint32_t)(((i / NSLOT) - 1) & 1))) {
         atomicOr(&s_fail, 1);
         break;
       }
@@ -414,9 +422,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       uint8_t* bs = ys + Cfg::Y_BYTES;
       const int o0 = (b_first + i) * XB;
       mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + Cfg::B_BYTES));
-      tma_load_2d(ys, &maps.y[j], o0, t.row0, &full[slot]);
-      tma_load_2d(ys + TM * 128, &maps.y[j], o0 + 64, t.row0, &full[slot]);
-      for (int kb = 0; kb < R / 64; ++kb) tma_load_3d(bs + kb * XB * 128, &maps.b[j], kb * 64, o0, t.slot, &full[slot]);
+      tma_load_2d_hint(ys, &maps.y[j], o0, t.row0, &full[slot], pol_stream);
+      tma_load_2d_hint(ys + TM * 128, &maps.y[j], o0 + 64, t.row0, &full[slot], pol_stream);
+      for (int kb = 0; kb < R / 64; ++kb)
+        tma_load_3d_hint(bs + kb * XB * 128, &maps.b[j], kb * 64, o0, t.slot, &full[slot], pol_keep);
     }
   } else if (ok && warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -424,9 +433,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
     const bool ready = mbar_wait(&uready, 0);
     if (!ready) atomicOr(&s_fail, 1);
     for (int i = 0; ready && i < nblk; ++i) {
-      const int slot = i & 1;
-      if (!mbar_wait(&full[slot], (uint32_t)((i >> 1) & 1)) ||
-          (i >= 2 && !mbar_wait(&tempty[slot], (uint32_t)(((i >> 1) - 1) & 1)))) {
+      const int slot = i % NSLOT, buf = i & 1;
+      if (!mbar_wait(&full[slot], (uint32_t)((i / NSLOT) & 1)) ||
+          (i >= 2 && !mbar_wait(&tempty[buf], (uint32_t)(((i >> 1) - 1) & 1)))) {
         atomicOr(&s_fail, 1);
         break;
       }
@@ -438,9 +447,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const uint64_t adesc = sw128_desc(ua + (ks >> 2) * TM * 128 + (ks & 3) * 32);
         const int kbk = (ks * 16) % R;  // the lo half reuses B's K columns
         const uint64_t bdesc = sw128_desc(bs + (kbk >> 6) * XB * 128 + ((kbk & 63) >> 4) * 32);
-        tc_mma_bf16(tmem + slot * XB, adesc, bdesc, idesc, ks > 0 ? 1u : 0u);
+        tc_mma_bf16(tmem + buf * XB, adesc, bdesc, idesc, ks > 0 ? 1u : 0u);
       }
-      tc_commit(&tfull[slot]);
+      tc_commit(&tfull[buf]);
     }
   } else if (warp >= 2) {
     // ---- epilogue warps: thread = one tile row = one TMEM lane
@@ -452,41 +461,52 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       // u row (sum of planes, plane order) -> bf16 hi | lo, swizzled K-major.
       const bool live = row < t.rows;
       const float* ur = u + (long long)(t.row0 + (live ? row : 0)) * nR + (long long)j * R;
-      for (int k = 0; k < R; k += 8) {
-        float v[8];
-        if (live) {
-          float4 a0 = __ldcg(reinterpret_cast<const float4*>(ur + k));
-          float4 a1 = __ldcg(reinterpret_cast<const float4*>(ur + k + 4));
-          for (int s = 1; s < w.nsplit; ++s) {
-            const float4 b0 = __ldcg(reinterpret_cast<const float4*>(ur + s * w.plane_stride + k));
-            const float4 b1 = __ldcg(reinterpret_cast<const float4*>(ur + s * w.plane_stride + k + 4));
-            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
-            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+      // 32 columns per batch: all loads of a batch (every plane) are issued
+      // before any is consumed, so a batch costs one L2 round trip.
+      for (int k0 = 0; k0 < R; k0 += 32) {
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          a[i] = live ? __ldcg(reinterpret_cast<const float4*>(ur + k0 + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 1; sp < w.nsplit; ++sp) {
+          float4 b[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            b[i] = live ? __ldcg(reinterpret_cast<const float4*>(ur + sp * w.plane_stride + k0 + 4 * i))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            a[i].x += b[i].x;
+            a[i].y += b[i].y;
+            a[i].z += b[i].z;
+            a[i].w += b[i].w;
           }
-          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-          v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = 0.f;
         }
-        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-          hi[i] = pack_bf16x2(h0, h1);
-          lo[i] = pack_bf16x2(__float2bfloat16_rn(v[2 * i] - __bfloat162float(h0)),
-                              __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1)));
+        for (int c = 0; c < 4; ++c) {  // 8 columns -> one 16-byte hi chunk and one lo chunk
+          const float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w,
+                              a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z, a[2 * c + 1].w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+            hi[i] = pack_bf16x2(h0, h1);
+            lo[i] = pack_bf16x2(__float2bfloat16_rn(v[2 * i] - __bfloat162float(h0)),
+                                __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1)));
+          }
+          const int k = k0 + 8 * c;
+          *reinterpret_cast<uint4*>(Ua + sw128_offset(row, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(Ua + sw128_offset(row, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        *reinterpret_cast<uint4*>(Ua + sw128_offset(row, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(Ua + sw128_offset(row, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_smem();  // generic writes -> visible to the tensor cores
       mbar_arrive(&uready);
 
       __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(sl.y) + (long long)(t.row0 + row) * sl.y_row_stride;
+      const uint64_t pol_stream = policy_evict_first();
       for (int i = 0; i < nblk; ++i) {
-        const int slot = i & 1;
-        if (!mbar_wait(&tfull[slot], (uint32_t)((i >> 1) & 1))) {
+        const int slot = i % NSLOT, buf = i & 1;
+        if (!mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
           atomicOr(&s_fail, 1);
           break;
         }
@@ -496,7 +516,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const int ovalid = min(XB, sl.out_dim - o0);
         for (int c16 = 0; c16 < XB / 16; ++c16) {
           float d[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * XB + c16 * 16), d);
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
           if (live && c16 * 16 < ovalid) {
             uint32_t out[8];
 #pragma unroll
@@ -513,14 +533,14 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
               }
             }
             uint4* dst = reinterpret_cast<uint4*>(yrow + o0 + c16 * 16);
-            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-            if (c16 * 16 + 8 < ovalid) dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            st_global_v4_hint(dst, make_uint4(out[0], out[1], out[2], out[3]), pol_stream);
+            if (c16 * 16 + 8 < ovalid) st_global_v4_hint(dst + 1, make_uint4(out[4], out[5], out[6], out[7]), pol_stream);
           }
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&tempty[slot]);
+          mbar_arrive(&tempty[buf]);
           mbar_arrive(&empty[slot]);
         }
       }

@@ -56,6 +56,24 @@ def _env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def reduce_across_ranks(max_values, sum_values, dist=None, device="cpu"):
+    """Whole-job figures across replicas: the slowest rank's times (max) and
+    the routed tokens of all ranks (sum).  Single process: unchanged."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(max_values), list(sum_values)
+    import torch
+    mx = torch.tensor([float(v) for v in max_values], dtype=torch.float64, device=device)
+    sm = torch.tensor([float(v) for v in sum_values], dtype=torch.float64, device=device)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return mx.tolist(), sm.tolist()
+
+
+def rank_seed(rank: int, index: int) -> int:
+    """Seed of input set `index` on replica `rank` (replicas draw disjoint batches)."""
+    return 1000 * rank + index
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -251,9 +269,8 @@ def run_ours(args):
     sets = []
     foot = 0
     max_sets = args.sets or 64
-    seed0 = 1000 * rank
     while len(sets) < max_sets:
-        raw = sy.draw(spec, seed0 + len(sets))
+        raw = sy.draw(spec, rank_seed(rank, len(sets)))
         qkv = device.prepare(raw, "qkv", fused=spec.fused_qkv)
         o = device.prepare(raw, "o")
         b = algorithmic_bytes(qkv["route_host"], raw, "qkv") + algorithmic_bytes(o["route_host"], raw, "o")
@@ -340,13 +357,7 @@ def run_ours(args):
     qkv_bytes = statistics.mean(algorithmic_bytes(s["qkv"]["route_host"], s["raw"], "qkv") for s in sets)
     clocks = sampler.stop() if sampler else None
 
-    if dist:
-        t = torch.tensor([ms, qkv_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, qkv_ms = float(t[0]), float(t[1])
-        tk = torch.tensor([float(tokens)], device="cuda")
-        dist.all_reduce(tk)
-        tokens = float(tk[0])
+    (ms, qkv_ms), (tokens,) = reduce_across_ranks([ms, qkv_ms], [tokens], dist, "cuda")
 
     # ---- e2e through the public API with host buffers
     e2e = run_e2e(args, sets, lk, torch, stream, dist)
@@ -460,13 +471,7 @@ def run_e2e(args, sets, lk, torch, stream, dist):
         e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-        tk = torch.tensor([float(toks)], device="cuda")
-        dist.all_reduce(tk)
-        toks = float(tk[0])
+    (ms,), (toks,) = reduce_across_ranks([ms], [toks], dist, "cuda")
     return {"value": toks / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d // k,
             "d2h_bytes_per_step": d2h // k, "steps": k,
             "note": "per step: host routing build, pinned H2D of x/y/triple for qkv and o, two "

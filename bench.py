@@ -48,6 +48,8 @@ WORKLOAD_DESC = {
     "prefill8b": "ragged prefill, 8B shapes, 4 slots + base, max rank 64, 16 requests of 128-2048 tokens, bf16",
     "mixed70b": "mixed prefill+decode, Llama-3-70B attention (hidden 8192, 64/8 heads; fused qkv 10240 + o 8192), "
                 "16 slots, max rank 128, 8192 tokens, 20% base, bf16",
+    "mlp8b": "decode, Llama-3-8B MLP (hidden 4096, intermediate 14336; fused gate+up 28672 + down 4096), "
+             "8 slots, max rank 16, 256 x 1-token requests, 25% base, bf16",
 }
 
 
@@ -82,11 +84,16 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _names(proj):
+    from workloads.synthetic import PROBLEMS
+    return list(PROBLEMS[proj])
+
+
 def algorithmic_bytes(route_host, raw, proj, e=2):
     """Per-apply algorithmic bytes: routed x rows + touched A/B slots (padded) + y read+write."""
     E = route_host["end"]
     touched = len(set(int(s) for s in route_host["lora_ids"]))
-    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    names = _names(proj)
     n = len(names)
     O = sum(raw["out_dims"][nm] for nm in names)
     R = raw["max_lora_rank"]
@@ -96,7 +103,7 @@ def algorithmic_bytes(route_host, raw, proj, e=2):
 
 def algorithmic_flops(route_host, raw, proj):
     E = route_host["end"]
-    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    names = _names(proj)
     O = sum(raw["out_dims"][nm] for nm in names)
     R = raw["max_lora_rank"]
     k = raw["in_dims"][names[0]]
@@ -166,8 +173,9 @@ def oracle_step_sampler(workload, seed, target_s, max_rows=None):
     from workloads import synthetic as sy
 
     raw = sy.draw(workload, seed)
-    fused = sy.SPECS[workload].fused_qkv
-    probs = [oracle.prepare_problem(raw, "qkv", fused=fused), oracle.prepare_problem(raw, "o", fused=True)]
+    spec = sy.SPECS[workload]
+    p0, p1 = spec.problems
+    probs = [oracle.prepare_problem(raw, p0, fused=spec.fused_qkv), oracle.prepare_problem(raw, p1, fused=True)]
     end = probs[0]["end"]
     # pre-convert the rows the oracle will read (conversion is not timed)
     cache = {}
@@ -262,6 +270,7 @@ def run_ours(args):
     from workloads import device, synthetic as sy
 
     spec = sy.SPECS[args.workload]
+    P0, P1 = spec.problems  # e.g. fused qkv and o_proj, or fused gate+up and down
     props = torch.cuda.get_device_properties(dev_idx)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20)
 
@@ -271,17 +280,17 @@ def run_ours(args):
     max_sets = args.sets or 64
     while len(sets) < max_sets:
         raw = sy.draw(spec, rank_seed(rank, len(sets)))
-        qkv = device.prepare(raw, "qkv", fused=spec.fused_qkv)
-        o = device.prepare(raw, "o")
-        b = algorithmic_bytes(qkv["route_host"], raw, "qkv") + algorithmic_bytes(o["route_host"], raw, "o")
-        sets.append({"raw": raw, "qkv": qkv, "o": o, "bytes": b, "E": qkv["route_host"]["end"]})
+        d0 = device.prepare(raw, P0, fused=spec.fused_qkv)
+        d1 = device.prepare(raw, P1)
+        b = algorithmic_bytes(d0["route_host"], raw, P0) + algorithmic_bytes(d1["route_host"], raw, P1)
+        sets.append({"raw": raw, "p0": d0, "p1": d1, "bytes": b, "E": d0["route_host"]["end"]})
         foot += b
         if not args.sets and foot >= 4 * l2 and len(sets) >= 2:
             break
     NS = len(sets)
     for s in sets:
-        s["call_qkv"] = lk.CallBuilder(s["qkv"]["problem"], s["qkv"]["routing"], s["qkv"]["workspace"])
-        s["call_o"] = lk.CallBuilder(s["o"]["problem"], s["o"]["routing"], s["o"]["workspace"])
+        s["call_qkv"] = lk.CallBuilder(s["p0"]["problem"], s["p0"]["routing"], s["p0"]["workspace"])
+        s["call_o"] = lk.CallBuilder(s["p1"]["problem"], s["p1"]["routing"], s["p1"]["workspace"])
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -354,7 +363,7 @@ def run_ours(args):
         r1.record(stream)
     torch.cuda.synchronize()
     qkv_ms = r0.elapsed_time(r1) / (reps * NS)
-    qkv_bytes = statistics.mean(algorithmic_bytes(s["qkv"]["route_host"], s["raw"], "qkv") for s in sets)
+    qkv_bytes = statistics.mean(algorithmic_bytes(s["p0"]["route_host"], s["raw"], P0) for s in sets)
     clocks = sampler.stop() if sampler else None
 
     (ms, qkv_ms), (tokens,) = reduce_across_ranks([ms, qkv_ms], [tokens], dist, "cuda")
@@ -382,7 +391,7 @@ def run_ours(args):
                    "routed_tokens_per_step": tokens / args.steps / max(world, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "fused-qkv SGMV apply (shrink + expand, PDL-chained)",
+                     "kernel": "%s SGMV apply (shrink + expand, PDL-chained)" % ("fused-" + P0 if len(_names(P0)) > 1 else P0),
                      "peak_source": "%s HBM copy bandwidth (MEASURED_PEAKS.json)" % peak_kind
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": int(qkv_bytes), "avg_launch_us": round(qkv_ms * 1e3, 3)},
@@ -416,12 +425,13 @@ def run_e2e(args, sets, lk, torch, stream, dist):
     for s in sets[:n]:
         raw = s["raw"]
         h = {}
-        for key in ("x_qkv", "x_o", "y_qkv", "y_o"):
+        P0, P1 = raw["problems"]
+        for key in ("x_" + P0, "x_" + P1, "y_" + P0, "y_" + P1):
             arr = np.ascontiguousarray(raw[key]).view(np.int16)
             t = torch.from_numpy(arr).view(torch.bfloat16).pin_memory()
             h[key] = t
-        h["out_qkv"] = torch.empty_like(h["y_qkv"]).pin_memory()
-        h["out_o"] = torch.empty_like(h["y_o"]).pin_memory()
+        h["out_p0"] = torch.empty_like(h["y_" + P0]).pin_memory()
+        h["out_p1"] = torch.empty_like(h["y_" + P1]).pin_memory()
         h["ids"] = torch.empty(raw["max_num_loras"], dtype=torch.int32).pin_memory()
         h["offs"] = torch.empty(raw["max_num_loras"] + 1, dtype=torch.int32).pin_memory()
         h["ev"] = torch.cuda.Event()
@@ -438,8 +448,8 @@ def run_e2e(args, sets, lk, torch, stream, dist):
         h["ev"].synchronize()  # the previous copy out of these pinned buffers has finished
         h["ids"][:G].copy_(torch.from_numpy(rt["lora_ids"]))
         h["offs"][:G + 1].copy_(torch.from_numpy(rt["grouped_offsets"]))
-        for proj in ("qkv", "o"):
-            d = s[proj]
+        for key, proj in (("p0", raw["problems"][0]), ("p1", raw["problems"][1])):
+            d = s[key]
             d["x"].copy_(h["x_" + proj], non_blocking=True)
             d["y_all"].copy_(h["y_" + proj], non_blocking=True)
             d["routing"].lora_ids[:G].copy_(h["ids"][:G], non_blocking=True)
@@ -447,9 +457,9 @@ def run_e2e(args, sets, lk, torch, stream, dist):
             h2d += 2 * h["x_" + proj].numel() + 2 * h["y_" + proj].numel() + 4 * (2 * G + 1)
             lk.lora_sgmv_apply(d["problem"], lk.Routing(d["routing"].lora_ids, d["routing"].grouped_offsets,
                                                         G, rt["end"]), d["workspace"], st)
-        for proj in ("qkv", "o"):
-            h["out_" + proj].copy_(s[proj]["y_all"], non_blocking=True)
-            d2h += 2 * h["out_" + proj].numel()
+        for key in ("p0", "p1"):
+            h["out_" + key].copy_(s[key]["y_all"], non_blocking=True)
+            d2h += 2 * h["out_" + key].numel()
         h["ev"].record(st)
         return rt["end"]
 

@@ -282,12 +282,13 @@ def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
 
     ``raw`` is a workload drawn by ``workloads.synthetic`` (raw fp32 adapter
     matrices per slot and projection, ranks, alphas, rsLoRA flags, request
-    list, x and y in storage type).  ``proj`` is "qkv" or "o".  Returns the
+    list, x and y in storage type).  ``proj`` is "qkv", "o", "gateup" or
+    "down" (the last two: the MLP projections, gate + up fused).  Returns the
     routing (oracle's own), the stacked storage buffers and fp64 views.
     """
     dt = raw["dtype"]
     S, R = raw["max_num_loras"], raw["max_lora_rank"]
-    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    names = {"qkv": ["q", "k", "v"], "o": ["o"], "gateup": ["gate", "up"], "down": ["down"]}[proj]
     route = build_routing(raw["req_slot"], raw["req_len"], S)
     in_dim = raw["x_" + proj].shape[1]
     outs = [raw["out_dims"][nm] for nm in names]

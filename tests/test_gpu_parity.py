@@ -159,6 +159,23 @@ def test_mixed70b_sampled(proj):
     run_case(sy.draw("mixed70b", 0), proj, rows="sample")
 
 
+@pytest.mark.parametrize("proj", ["gateup", "down"])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_mlp8b_full(proj, mode):
+    """MLP projections (gate + up fused as two slices; down over the 14336-wide
+    intermediate activations)."""
+    run_case(sy.draw("mlp8b", 0), proj, mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_mlp_long_groups_tensor_core_path(mode):
+    spec = _spec(family="mlp", hidden=512, intermediate=1024, max_num_loras=3, max_lora_rank=64,
+                 rank_choices=(32, 64), kind="fixed", fixed_slots=(2, 0, 1, -1),
+                 fixed_lens=(300, 513, 200, 11))
+    run_case(sy.draw(spec, 9), "gateup", mode=mode)
+    run_case(sy.draw(spec, 10), "down", mode=mode)
+
+
 # ------------------------------------------------------------ edge cases --
 
 def _spec(**kw):

@@ -359,3 +359,24 @@ def test_generator_is_deterministic():
     assert np.array_equal(a["x_qkv"], b["x_qkv"])
     c = sy.draw("decode8b", 6, with_weights=False)
     assert not np.array_equal(a["x_qkv"], c["x_qkv"])
+
+
+def test_mlp_gate_up_fused_equals_per_projection():
+    """MLP projections: gate and up fused as two slices over the same input
+    give bit-identical results to two separate projections; down reads the
+    intermediate activations."""
+    spec = sy.custom_spec(family="mlp", intermediate=96, hidden=64, n_requests=9, max_num_loras=3,
+                          rank_choices=(8, 16))
+    raw = sy.draw(spec, seed=4)
+    assert raw["x_gateup"].shape[1] == 64 and raw["x_down"].shape[1] == 96
+    assert raw["y_gateup"].shape[1] == 192 and raw["y_down"].shape[1] == 64
+    pf = oracle.prepare_problem(raw, "gateup", fused=True)
+    pp = oracle.prepare_problem(raw, "gateup", fused=False)
+    rows = np.arange(pf["end"])
+    uf, yf = oracle.problem_rows(pf, rows)
+    up, yp = oracle.problem_rows(pp, rows)
+    assert np.array_equal(uf, up)
+    for a, b in zip(yf, yp):
+        assert np.array_equal(a, b)
+    pd = oracle.prepare_problem(raw, "down")
+    assert pd["in_dim"] == 96 and pd["out_dims"] == [64]

@@ -33,7 +33,7 @@ def torch_to_storage(t: torch.Tensor, dtype: str) -> np.ndarray:
 
 
 def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y: bool = False) -> dict:
-    """Build one projection problem ("qkv" or "o") on the device.
+    """Build one projection problem ("qkv", "o", "gateup" or "down") on the device.
 
     fused=True: one fused stack A [S, n*R, in], B [S, O, R] and y [T, O].
     fused=False: per-projection stacks A_j [S, R, in], B_j [S, out_j, R]; y is
@@ -43,7 +43,8 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
     dt = raw["dtype"]
     tdt = _TORCH_DT[dt]
     S, R = raw["max_num_loras"], raw["max_lora_rank"]
-    names = ["q", "k", "v"] if proj == "qkv" else ["o"]
+    from workloads.synthetic import PROBLEMS
+    names = list(PROBLEMS[proj])
     outs = [raw["out_dims"][nm] for nm in names]
     O = sum(outs)
     x = storage_to_torch(raw["x_" + proj], dt, device)

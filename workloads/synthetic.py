@@ -41,6 +41,9 @@ import numpy as np
 import torch
 
 PROJS = ("q", "k", "v", "o")
+MLP_PROJS = ("gate", "up", "down")
+# Problems of a layer: one shared input per problem, its projections as slices.
+PROBLEMS = {"qkv": ("q", "k", "v"), "o": ("o",), "gateup": ("gate", "up"), "down": ("down",)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -68,15 +71,29 @@ class Spec:
     fixed_slots: Optional[Sequence[int]] = None
     fixed_lens: Optional[Sequence[int]] = None
     fixed_ranks: Optional[Sequence[int]] = None
+    family: str = "attn"           # "attn": q/k/v + o; "mlp": gate/up + down
+    intermediate: int = 0          # MLP intermediate width
+
+    @property
+    def projs(self):
+        return MLP_PROJS if self.family == "mlp" else PROJS
+
+    @property
+    def problems(self):
+        return ("gateup", "down") if self.family == "mlp" else ("qkv", "o")
 
     @property
     def out_dims(self):
+        if self.family == "mlp":
+            return {"gate": self.intermediate, "up": self.intermediate, "down": self.hidden}
         q = self.n_heads * self.head_dim
         kv = self.n_kv_heads * self.head_dim
         return {"q": q, "k": kv, "v": kv, "o": self.hidden}
 
     @property
     def in_dims(self):
+        if self.family == "mlp":
+            return {"gate": self.hidden, "up": self.hidden, "down": self.intermediate}
         return {"q": self.hidden, "k": self.hidden, "v": self.hidden,
                 "o": self.n_heads * self.head_dim}
 
@@ -93,6 +110,11 @@ SPECS = {
     "mixed70b": Spec("mixed70b", "bf16", 64, 8, 128, 8192, 16, 128, (16, 64, 128), kind="mixed",
                      total_tokens=8192, n_prefill=6, base_prob=0.20, slot_dist="uniform",
                      len_range=(512, 1024)),
+    # MLP projections of the same 8B shape (intermediate 14336): gate + up
+    # fused as a two-slice problem, down separately.
+    "mlp8b": Spec("mlp8b", "bf16", 32, 8, 128, 4096, 8, 16, (8, 16), kind="decode",
+                  n_requests=256, base_prob=0.25, slot_dist="uniform", family="mlp",
+                  intermediate=14336),
 }
 
 
@@ -168,7 +190,7 @@ def draw(spec, seed: int = 0, with_weights: bool = True) -> dict:
            "fused_qkv": spec.fused_qkv}
     if with_weights:
         A, B = {}, {}
-        for p in PROJS:
+        for p in spec.projs:
             kin, dout = spec.in_dims[p], spec.out_dims[p]
             A[p], B[p] = [], []
             for s in range(S):
@@ -176,11 +198,15 @@ def draw(spec, seed: int = 0, with_weights: bool = True) -> dict:
                 A[p].append(rng.standard_normal((r, kin), dtype=np.float32) / np.float32(np.sqrt(kin)))
                 B[p].append(np.float32(0.02) * rng.standard_normal((dout, r), dtype=np.float32))
         out["A"], out["B"] = A, B
-    O = sum(spec.out_dims[p] for p in ("q", "k", "v"))
-    out["x_qkv"] = to_storage(rng.standard_normal((T, spec.hidden), dtype=np.float32), spec.dtype)
-    out["x_o"] = to_storage(rng.standard_normal((T, spec.in_dims["o"]), dtype=np.float32), spec.dtype)
-    out["y_qkv"] = to_storage(rng.standard_normal((T, O), dtype=np.float32), spec.dtype)
-    out["y_o"] = to_storage(rng.standard_normal((T, spec.hidden), dtype=np.float32), spec.dtype)
+    out["problems"] = spec.problems
+    for prob in spec.problems:
+        names = PROBLEMS[prob]
+        k_in = spec.in_dims[names[0]]
+        O = sum(spec.out_dims[p] for p in names)
+        out["x_" + prob] = to_storage(rng.standard_normal((T, k_in), dtype=np.float32), spec.dtype)
+    for prob in spec.problems:
+        O = sum(spec.out_dims[p] for p in PROBLEMS[prob])
+        out["y_" + prob] = to_storage(rng.standard_normal((T, O), dtype=np.float32), spec.dtype)
     return out
 
 

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_ERR_NULL", 2: "LORA_ERR_SHAPE", 3: "LORA_
                 7: "LORA_ERR_ALIGN", 8: "LORA_ERR_WORKSPACE", 9: "LORA_ERR_CUDA",
                 10: "LORA_ERR_DEVICE_CHECK"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
-DEV_BAD_SLOT, DEV_BAD_OFFSETS, DEV_BAD_END, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_SLOT, DEV_BAD_OFFSETS, DEV_BAD_END, DEV_TIMEOUT, DEV_BAD_ROW = 1, 2, 4, 8, 16
 MAX_SLICES = 3
 
 
@@ -54,7 +54,7 @@ class _Problem(ctypes.Structure):
 
 class _Routing(ctypes.Structure):
     _fields_ = [("lora_ids", ctypes.c_void_p), ("grouped_offsets", ctypes.c_void_p),
-                ("num_groups", ctypes.c_int32), ("end", ctypes.c_int32)]
+                ("num_groups", ctypes.c_int32), ("end", ctypes.c_int32), ("token_rows", ctypes.c_void_p)]
 
 
 _lib = None
@@ -79,6 +79,8 @@ def lib():
     vp = ctypes.c_void_p
     L.lora_build_routing.restype = ctypes.c_int
     L.lora_build_routing.argtypes = [i32, i32p, i32p, i32, i32p, i32p, i32p, i32p, i32p, i32p]
+    L.lora_build_token_rows.restype = ctypes.c_int
+    L.lora_build_token_rows.argtypes = [i32, i32p, i32p, i32, i32p]
     L.lora_set_slot.restype = ctypes.c_int
     L.lora_set_slot.argtypes = [ctypes.POINTER(_Problem), i32, i32, i32, ctypes.c_double, i32, vp, vp,
                                 ctypes.c_int, vp]
@@ -137,17 +139,31 @@ def lora_build_routing(req_slot, req_num_tokens, max_num_loras: int) -> dict:
             "num_groups": g, "end": end.value, "total_tokens": T.value}
 
 
+def lora_build_token_rows(req_num_tokens, perm, end: int) -> np.ndarray:
+    """Rows of the routed tokens in sorted order for an arrival-order batch."""
+    L = lib()
+    lens = np.ascontiguousarray(np.asarray(req_num_tokens, dtype=np.int32))
+    pm = np.ascontiguousarray(np.asarray(perm, dtype=np.int32))
+    out = np.zeros(max(int(end), 1), dtype=np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    _check(L.lora_build_token_rows(int(lens.size), p(lens), p(pm), int(end), p(out)), "lora_build_token_rows")
+    return out[:int(end)].copy()
+
+
 @dataclass
 class Routing:
-    """Routing triple: device lora_ids / grouped_offsets tensors, host num_groups / end."""
+    """Routing triple: device lora_ids / grouped_offsets tensors, host num_groups / end,
+    and optionally device token_rows (row of each sorted token, unsorted batches)."""
     lora_ids: object
     grouped_offsets: object
     num_groups: int
     end: int
+    token_rows: object = None
 
     def _c(self) -> _Routing:
         ptr = lambda t: t.data_ptr() if t is not None and t.numel() > 0 else None
-        return _Routing(ptr(self.lora_ids), ptr(self.grouped_offsets), int(self.num_groups), int(self.end))
+        return _Routing(ptr(self.lora_ids), ptr(self.grouped_offsets), int(self.num_groups), int(self.end),
+                        ptr(self.token_rows))
 
 
 def routing_to_device(r: dict, device="cuda", non_blocking=False) -> Routing:

@@ -76,6 +76,7 @@ ProblemDesc make_desc(const lora_problem_t* p, const lora_routing_t* r) {
     d.offs = r->grouped_offsets;
     d.G = r->num_groups;
     d.end = r->end;
+    d.token_rows = r->token_rows;
   }
   d.status = status_ptr();
   return d;

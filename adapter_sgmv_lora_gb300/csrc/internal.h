@@ -35,6 +35,7 @@ struct ProblemDesc {
   const int* offs;      // device [G + 1]
   int G;
   int end;
+  const int* token_rows;  // device [end] or nullptr (row i of the sorted order is row i)
   unsigned* status;  // device status word (LORA_DEV_* flags)
 };
 

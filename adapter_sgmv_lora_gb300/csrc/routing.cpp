@@ -66,3 +66,23 @@ extern "C" lora_status_t lora_build_routing(int32_t num_requests, const int32_t*
   *total_tokens = static_cast<int32_t>(total);
   return LORA_OK;
 }
+
+extern "C" lora_status_t lora_build_token_rows(int32_t num_requests, const int32_t* req_num_tokens,
+                                               const int32_t* perm, int32_t end, int32_t* token_rows) {
+  if (num_requests < 0 || end < 0) return LORA_ERR_SHAPE;
+  if (end > 0 && !token_rows) return LORA_ERR_NULL;
+  if (num_requests > 0 && (!req_num_tokens || !perm)) return LORA_ERR_NULL;
+  // Row where each request starts, in arrival order.
+  std::vector<int64_t> start(static_cast<size_t>(num_requests) + 1, 0);
+  for (int32_t i = 0; i < num_requests; ++i) {
+    if (req_num_tokens[i] < 0) return LORA_ERR_SHAPE;
+    start[i + 1] = start[i] + req_num_tokens[i];
+  }
+  int32_t k = 0;
+  for (int32_t i = 0; i < num_requests && k < end; ++i) {
+    const int32_t r = perm[i];
+    if (r < 0 || r >= num_requests) return LORA_ERR_SHAPE;
+    for (int32_t t = 0; t < req_num_tokens[r] && k < end; ++t) token_rows[k++] = (int32_t)(start[r] + t);
+  }
+  return k == end ? LORA_OK : LORA_ERR_SHAPE;
+}

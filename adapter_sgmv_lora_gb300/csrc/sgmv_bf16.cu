@@ -103,13 +103,20 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   const int ch = threadIdx.x & 7;
   const __nv_bfloat16* srcs[MAXR];
   uint32_t dsts[MAXR];
+  int bad_row = 0;
 #pragma unroll
   for (int i = 0; i < MAXR; ++i) {
     const int row = (threadIdx.x >> 3) + 16 * i;
     srcs[i] = nullptr;
     dsts[i] = 0;
     if (row < t.rows) {
-      srcs[i] = xg + (long long)(t.row0 + row) * p.x_row_stride + k0 + ch * 8;
+      // Row of x holding this token (gathered batches map through token_rows).
+      const int xr = p.token_rows ? p.token_rows[t.row0 + row] : t.row0 + row;
+      if (xr < 0 || xr >= p.num_tokens) {
+        bad_row = 1;
+        continue;
+      }
+      srcs[i] = xg + (long long)xr * p.x_row_stride + k0 + ch * 8;
       dsts[i] = row * XPITCH + ch * 16;
     } else if (row < nrows_total) {
       const int col = n0 + row - t.rows;
@@ -120,6 +127,13 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     }
   }
   (void)warp;
+
+  // Every CTA of the tile (and of its cluster) checks all of the tile's rows
+  // and reaches the same verdict.
+  if (__syncthreads_or(bad_row)) {
+    if (threadIdx.x == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
+    return;
+  }
 
   auto issue = [&](int s) {
     uint8_t* xs = smem + (s % NSTAGE) * Cfg::STAGE_BYTES;
@@ -283,6 +297,20 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   if (!s_ok) return;
   const Tile t = s_tile;
 
+  // Row of y holding each token of the tile (gathered batches map through
+  // token_rows); an out-of-range entry skips the tile.
+  __shared__ int s_rows[MT];
+  int bad_row = 0;
+  for (int r = threadIdx.x; r < t.rows; r += blockDim.x) {
+    const int yr = p.token_rows ? p.token_rows[t.row0 + r] : t.row0 + r;
+    if (yr < 0 || yr >= p.num_tokens) bad_row = 1;
+    s_rows[r] = yr;
+  }
+  if (__syncthreads_or(bad_row)) {
+    if (threadIdx.x == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
+    return;
+  }
+
   uint8_t* Ys = smem + Cfg::Y_OFF;
   uint8_t* Bs = smem + Cfg::B_OFF;
   uint8_t* Hs = smem + Cfg::H_OFF;
@@ -300,7 +328,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   for (int c = threadIdx.x; c < t.rows * YW; c += blockDim.x) {
     const int r = c / YW, ch = c % YW;
     if (ch < ych)
-      cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8);
+      cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)s_rows[r] * sl.y_row_stride + o0 + ch * 8);
   }
   for (int c = threadIdx.x; c < ovalid * BW; c += blockDim.x) {
     const int o = c / BW, ch = c % BW;
@@ -392,7 +420,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   for (int c = threadIdx.x; c < t.rows * YW; c += blockDim.x) {
     const int r = c / YW, ch = c % YW;
     if (ch < ych)
-      *reinterpret_cast<uint4*>(yg + (long long)(t.row0 + r) * sl.y_row_stride + o0 + ch * 8) =
+      *reinterpret_cast<uint4*>(yg + (long long)s_rows[r] * sl.y_row_stride + o0 + ch * 8) =
           *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
   }
 }

@@ -271,6 +271,7 @@ int tc_shrink_splits(int end, int in_dim) {
 }
 
 bool tc_shrink_ok(const ProblemDesc& p) {
+  if (p.token_rows) return false;  // TMA boxes need the tile's rows contiguous
   const int nR = p.n_slices * p.R;
   switch (nR) {
     case 16: case 32: case 48: case 64: case 96: case 128: case 192: case 256: case 384: break;

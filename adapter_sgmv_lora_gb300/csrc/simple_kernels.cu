@@ -55,7 +55,12 @@ __global__ void __launch_bounds__(256) shrink_simple_kernel(const __grid_constan
   const int slot = p.lora_ids[group_of_row(p, t)];
   const T* a = static_cast<const T*>(p.sl[j].A) + (long long)slot * p.sl[j].A_slot_stride +
                (long long)k * p.in_dim;
-  const T* x = static_cast<const T*>(p.x) + (long long)t * p.x_row_stride;
+  const int xr = p.token_rows ? p.token_rows[t] : t;  // row of x holding token t
+  if (xr < 0 || xr >= p.num_tokens) {
+    if (lane == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
+    return;
+  }
+  const T* x = static_cast<const T*>(p.x) + (long long)xr * p.x_row_stride;
   float acc = 0.f;
   for (int i = lane; i < p.in_dim; i += 32) acc = fmaf(to_f32(a[i]), to_f32(x[i]), acc);
 #pragma unroll
@@ -90,7 +95,12 @@ __global__ void __launch_bounds__(256) expand_simple_kernel(const __grid_constan
   const T* b = static_cast<const T*>(p.sl[j].B) + (long long)slot * p.sl[j].B_slot_stride +
                (long long)o * p.R;
   const float* ut = u + (long long)t * nR + (long long)j * p.R;
-  T* y = static_cast<T*>(p.sl[j].y) + (long long)t * p.sl[j].y_row_stride + o;
+  const int yr = p.token_rows ? p.token_rows[t] : t;  // row of y holding token t
+  if (yr < 0 || yr >= p.num_tokens) {
+    atomicOr(p.status, LORA_DEV_BAD_ROW);
+    return;
+  }
+  T* y = static_cast<T*>(p.sl[j].y) + (long long)yr * p.sl[j].y_row_stride + o;
   float acc = 0.f;
   for (int k = 0; k < p.R; ++k) acc = fmaf(to_f32(b[k]), ut[k], acc);
   *y = from_f32<T>(to_f32(*y) + acc);

@@ -64,6 +64,7 @@ typedef enum { LORA_DTYPE_F32 = 0, LORA_DTYPE_BF16 = 1 } lora_dtype_t;
 #define LORA_DEV_BAD_OFFSETS 2u  /* grouped_offsets[0] != 0 or a decreasing offset */
 #define LORA_DEV_BAD_END 4u      /* grouped_offsets[num_groups] != end */
 #define LORA_DEV_TIMEOUT 8u      /* a kernel gave up waiting for its own copies */
+#define LORA_DEV_BAD_ROW 16u     /* a token_rows entry outside [0, num_tokens) */
 
 #define LORA_MAX_SLICES 3
 
@@ -125,6 +126,15 @@ typedef struct {
   const int32_t* grouped_offsets;
   int32_t num_groups;
   int32_t end;
+  /* Optional, DEVICE int32 [end]: token_rows[i] is the row of x and y that
+   * holds the i-th routed token of the sorted order, for batches that are not
+   * physically sorted (the per-token slot mapping of "vLLM LoRA 实现深度解析"
+   * section 6, whose kernels walk tokens sorted by adapter).  NULL: row i is
+   * row i (the sorted batch of the MAX page).  Entries must be distinct and in
+   * [0, num_tokens); an entry outside that range makes the launch skip the
+   * tiles containing it and raises LORA_DEV_BAD_ROW.  Gathered batches do not
+   * use the tcgen05 kernels. */
+  const int32_t* token_rows;
 } lora_routing_t;
 
 /*
@@ -152,6 +162,19 @@ lora_status_t lora_build_routing(int32_t num_requests, const int32_t* req_slot,
                                  const int32_t* req_num_tokens, int32_t max_num_loras,
                                  int32_t* perm, int32_t* lora_ids, int32_t* grouped_offsets,
                                  int32_t* num_groups, int32_t* end, int32_t* total_tokens);
+
+/*
+ * lora_build_token_rows -- HOST ONLY.  For a batch whose rows are in ARRIVAL
+ * order (request i owns rows [start_i, start_i + req_num_tokens[i]), start
+ * the running sum in arrival order), write the row of every routed token in
+ * the sorted order produced by lora_build_routing: token_rows[0, end) lists
+ * the rows of request perm[0], then perm[1], ..., stopping after `end` rows.
+ * Pass it (uploaded) as lora_routing_t.token_rows.
+ * Errors: LORA_ERR_NULL, LORA_ERR_SHAPE (negative counts, a perm entry out of
+ * range, end larger than the rows of the batch).
+ */
+lora_status_t lora_build_token_rows(int32_t num_requests, const int32_t* req_num_tokens,
+                                    const int32_t* perm, int32_t end, int32_t* token_rows);
 
 /*
  * lora_set_slot -- load-time preparation of one adapter slot for one slice

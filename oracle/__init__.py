@@ -74,6 +74,10 @@ def lib():
                                        ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
                                        ctypes.c_longlong, i32p, i32p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_void_p]
+        L.oracle_sgmv_token_slots.restype = ctypes.c_int
+        L.oracle_sgmv_token_slots.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
+                                              ctypes.c_longlong, ctypes.c_void_p]
         _LIB = L
     return _LIB
 
@@ -327,3 +331,67 @@ def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
     return {"dtype": dt, "S": S, "R": R, "in_dim": in_dim, "x": raw["x_" + proj], "slices": slices,
             "lora_ids": route["lora_ids"], "grouped_offsets": route["grouped_offsets"],
             "end": route["end"], "route": route, "stored": stored, "out_dims": outs}
+
+
+# --------------------------------------------------------------------------
+# Unsorted batches: per-token slots
+# --------------------------------------------------------------------------
+
+def token_rows(req_len, perm, end: int) -> np.ndarray:
+    """Rows (arrival-order batch) of the routed tokens in sorted order: the
+    rows of request perm[0], then perm[1], ..., the first `end` of them."""
+    lens = [int(v) for v in req_len]
+    start = [0]
+    for ln in lens:
+        start.append(start[-1] + ln)
+    out = []
+    for i in perm:
+        out.extend(range(start[int(i)], start[int(i)] + lens[int(i)]))
+        if len(out) >= end:
+            break
+    return np.asarray(out[:end], dtype=np.int32)
+
+
+def row_slots(req_slot, req_len) -> np.ndarray:
+    """Slot of every row of an arrival-order batch (base -1): the per-token map."""
+    return np.repeat(np.asarray(req_slot, dtype=np.int32), np.asarray(req_len, dtype=np.int64))
+
+
+def sgmv_token_slots(row_slot, x_rows, slices, in_dim: int, R: int, max_num_loras: int):
+    """Per-token definition (C): listed rows with their slots; see lora_oracle.c."""
+    L = lib()
+    rs = _i32(row_slot)
+    n = int(rs.size)
+    x_rows = np.ascontiguousarray(x_rows, dtype=np.float64)
+    ns = len(slices)
+    keep, arr, outs = [], (_Slice * ns)(), []
+    for j, sl in enumerate(slices):
+        A = np.ascontiguousarray(sl["A"], dtype=np.float64)
+        B = np.ascontiguousarray(sl["B"], dtype=np.float64)
+        yi = np.ascontiguousarray(sl["y_in"], dtype=np.float64)
+        od = int(sl["out_dim"])
+        yo = np.empty((n, od), dtype=np.float64)
+        keep += [A, B, yi, yo]
+        arr[j] = _Slice(A.ctypes.data + 8 * int(sl.get("A_offset", 0)), int(sl["A_slot_stride"]),
+                        B.ctypes.data + 8 * int(sl.get("B_offset", 0)), int(sl["B_slot_stride"]), od,
+                        yi.ctypes.data, od, yo.ctypes.data, od)
+        outs.append(yo)
+    u = np.empty((n, ns * R), dtype=np.float64)
+    rc = L.oracle_sgmv_token_slots(n, _p32(rs), int(in_dim), int(R), int(max_num_loras), ns, arr,
+                                   x_rows.ctypes.data, int(in_dim), u.ctypes.data)
+    if rc != OK:
+        raise ValueError("oracle_sgmv_token_slots failed with code %d" % rc)
+    return u, outs
+
+
+def problem_token_rows(prob, rows, row_slot):
+    """Per-token oracle on a prepared problem whose x / y are in arrival order."""
+    rows = _i32(rows)
+    dt = prob["dtype"]
+    x_rows = to_f64(prob["x"][rows], dt)
+    slices = []
+    for sl in prob["slices"]:
+        d = dict(sl)
+        d["y_in"] = to_f64(sl["y"][rows][:, sl["y_col0"]:sl["y_col0"] + sl["out_dim"]], dt)
+        slices.append(d)
+    return sgmv_token_slots(row_slot, x_rows, slices, prob["in_dim"], prob["R"], prob["S"])

@@ -199,3 +199,50 @@ int oracle_sgmv_rows(int n_rows, const int* rows, int in_dim, int R, int max_num
   }
   return ORACLE_OK;
 }
+
+/*
+ * oracle_sgmv_token_slots: the delta defined per token, with no routing
+ * triple ("vLLM LoRA 实现深度解析" section 6: token_lora_mapping gives the slot of
+ * every token; output += lora_b_stacked[slot] . lora_a_stacked[slot] . x).
+ * For each listed row r with slot row_slot[r] >= 0, and every slice j:
+ *     u[r, j*R + k] = sum_i A_j[slot, k, i] * x_rows[r, i]
+ *     y_out_j[r, o] = y_in_j[r, o] + sum_k B_j[slot, o, k] * u[r, j*R + k]
+ * Rows with slot -1 (base) are copied unchanged to y_out and get u = 0.
+ */
+int oracle_sgmv_token_slots(int n_rows, const int* row_slot, int in_dim, int R, int max_num_loras,
+                            int n_slices, const oracle_slice* slices, const double* x_rows,
+                            long long x_row_stride, double* u) {
+  if (n_rows < 0 || in_dim <= 0 || R <= 0 || R > 1024 || n_slices <= 0) return ORACLE_BAD_ARG;
+  if (n_rows > 0 && (!row_slot || !slices || !x_rows)) return ORACLE_BAD_ARG;
+  for (int r = 0; r < n_rows; ++r) {
+    const int s = row_slot[r];
+    if (s < -1 || s >= max_num_loras) return ORACLE_BAD_SLOT;
+    const double* xt = x_rows + (long long)r * x_row_stride;
+    for (int j = 0; j < n_slices; ++j) {
+      const oracle_slice* sl = &slices[j];
+      const double* yi = sl->y_in + (long long)r * sl->y_in_row_stride;
+      double* yo = sl->y_out + (long long)r * sl->y_out_row_stride;
+      if (s < 0) {
+        for (int o = 0; o < sl->out_dim; ++o) yo[o] = yi[o];
+        if (u)
+          for (int k = 0; k < R; ++k) u[(long long)r * n_slices * R + (long long)j * R + k] = 0.0;
+        continue;
+      }
+      double uj[1024];
+      for (int k = 0; k < R; ++k) {
+        const double* a = sl->A + (long long)s * sl->A_slot_stride + (long long)k * in_dim;
+        double acc = 0.0;
+        for (int i = 0; i < in_dim; ++i) acc += a[i] * xt[i];
+        uj[k] = acc;
+        if (u) u[(long long)r * n_slices * R + (long long)j * R + k] = acc;
+      }
+      for (int o = 0; o < sl->out_dim; ++o) {
+        const double* b = sl->B + (long long)s * sl->B_slot_stride + (long long)o * R;
+        double acc = 0.0;
+        for (int k = 0; k < R; ++k) acc += b[k] * uj[k];
+        yo[o] = yi[o] + acc;
+      }
+    }
+  }
+  return ORACLE_OK;
+}

@@ -176,6 +176,71 @@ def test_mlp_long_groups_tensor_core_path(mode):
     run_case(sy.draw(spec, 10), "down", mode=mode)
 
 
+def run_unsorted(raw, proj="qkv", mode="apply"):
+    """x and y rows in ARRIVAL order; token_rows maps the sorted order to rows.
+    Compared with the per-token oracle (slot of each row, no routing triple)."""
+    lk, device = _lk(), _dev()
+    dev = device.prepare(raw, proj)
+    rt = dev["route_host"]
+    rows = lk.lora_build_token_rows(raw["req_len"], rt["perm"], rt["end"])
+    assert np.array_equal(rows, oracle.token_rows(raw["req_len"], rt["perm"], rt["end"]))
+    tr = torch.from_numpy(rows).cuda() if rt["end"] > 0 else None
+    routing = lk.Routing(dev["routing"].lora_ids, dev["routing"].grouped_offsets, rt["num_groups"], rt["end"], tr)
+    y_before = device.y_host(dev)
+    if mode == "apply":
+        lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
+    else:
+        nR = len(dev["names"]) * raw["max_lora_rank"]
+        u = torch.empty((max(rt["end"], 1), nR), dtype=torch.float32, device="cuda")
+        lk.lora_shrink(dev["problem"], routing, u)
+        lk.lora_expand(dev["problem"], routing, u)
+    torch.cuda.synchronize()
+    assert lk.lora_get_device_status() == 0
+    y_after = device.y_host(dev)
+    ref = oracle.prepare_problem(raw, proj)
+    slots = oracle.row_slots(raw["req_slot"], raw["req_len"])
+    all_rows = np.arange(raw["T"], dtype=np.int32)
+    _, ys = oracle.problem_token_rows(ref, all_rows, slots)
+    got = oracle.to_f64(y_after, raw["dtype"])
+    base = slots < 0
+    assert np.array_equal(_bits(y_after[base]), _bits(y_before[base]))
+    col = 0
+    for yj in ys:
+        g = got[:, col:col + yj.shape[1]]
+        err = (np.abs(g - yj) / (1.0 + np.abs(yj)))[~base]
+        assert err.max() <= TOL_Y[raw["dtype"]], float(err.max())
+        col += yj.shape[1]
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_unsorted_decode_batch_token_rows(mode, proj):
+    run_unsorted(sy.draw("decode8b", 3), proj, mode)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_unsorted_multi_token_requests(mode):
+    spec = _spec(max_num_loras=5, max_lora_rank=32, rank_choices=(16, 32), kind="prefill", n_requests=14,
+                 len_range=(1, 150), slot_dist="uniform+base", hidden=1024, n_heads=16, n_kv_heads=4,
+                 head_dim=64)
+    run_unsorted(sy.draw(spec, 11), "qkv", mode)
+    run_unsorted(sy.draw(_spec(dtype="f32", n_requests=20), 12), "qkv", mode)
+
+
+def test_token_rows_out_of_range_is_flagged_and_skipped():
+    lk, device = _lk(), _dev()
+    raw = sy.draw("decode8b", 4)
+    dev = device.prepare(raw, "qkv")
+    rt = dev["route_host"]
+    rows = lk.lora_build_token_rows(raw["req_len"], rt["perm"], rt["end"])
+    rows[3] = raw["T"] + 100
+    routing = lk.Routing(dev["routing"].lora_ids, dev["routing"].grouped_offsets, rt["num_groups"], rt["end"],
+                         torch.from_numpy(rows).cuda())
+    assert lk.lora_get_device_status() == 0
+    lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
+    assert lk.lora_get_device_status() & lk.DEV_BAD_ROW
+
+
 # ------------------------------------------------------------ edge cases --
 
 def _spec(**kw):

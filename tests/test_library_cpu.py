@@ -129,3 +129,18 @@ def test_host_validation_without_gpu():
     assert L.lora_set_slot(ctypes.byref(prob), 0, 2, 4, 1.0, 0, 16, 16, 0, None) == 4
     assert L.lora_set_slot(ctypes.byref(prob), 1, 0, 4, 1.0, 0, 16, 16, 0, None) == 2
     assert L.lora_workspace_bytes(ctypes.byref(prob), 100) == 100 * 16 * 4 + (256 - (6400 % 256)) % 256
+
+
+def test_token_rows_match_oracle():
+    rng = np.random.default_rng(14)
+    for _ in range(200):
+        S = int(rng.integers(1, 10))
+        n = int(rng.integers(0, 40))
+        slots = rng.integers(-1, S, size=n).astype(np.int32)
+        lens = rng.integers(0, 6, size=n).astype(np.int32)
+        r = lk.lora_build_routing(slots, lens, S)
+        a = lk.lora_build_token_rows(lens, r["perm"], r["end"])
+        b = oracle.token_rows(lens, r["perm"], r["end"])
+        assert np.array_equal(a, b)
+    with pytest.raises(lk.LoraError):
+        lk.lora_build_token_rows([2, 3], [0, 1], 9)   # more rows than the batch has

@@ -380,3 +380,60 @@ def test_mlp_gate_up_fused_equals_per_projection():
         assert np.array_equal(a, b)
     pd = oracle.prepare_problem(raw, "down")
     assert pd["in_dim"] == 96 and pd["out_dims"] == [64]
+
+
+def test_token_rows_brute_force():
+    """Rows of the sorted tokens of an arrival-order batch: the routed rows,
+    each exactly once, grouped by slot in the order of the triple."""
+    rng = np.random.default_rng(12)
+    for _ in range(300):
+        n = int(rng.integers(0, 12))
+        slots = rng.integers(-1, 4, size=n).astype(np.int32)
+        lens = rng.integers(0, 5, size=n).astype(np.int32)
+        r = oracle.build_routing(slots, lens, 4)
+        rows = oracle.token_rows(lens, r["perm"], r["end"])
+        per_row = oracle.row_slots(slots, lens)
+        assert len(rows) == r["end"] == int((per_row >= 0).sum())
+        assert sorted(rows.tolist()) == np.nonzero(per_row >= 0)[0].tolist()
+        for g in range(r["num_groups"]):
+            seg = rows[r["grouped_offsets"][g]:r["grouped_offsets"][g + 1]]
+            assert np.all(per_row[seg] == r["lora_ids"][g])
+
+
+def test_per_token_definition_matches_routed_definition():
+    """The per-token oracle (slot per row, no triple) and the routed oracle
+    agree bit-exactly on a sorted batch; base rows come back unchanged."""
+    spec = sy.custom_spec(dtype="bf16", n_requests=12, max_num_loras=4, rank_choices=(8, 16))
+    raw = sy.draw(spec, seed=6)
+    p = oracle.prepare_problem(raw, "qkv")
+    r = p["route"]
+    sorted_rows = oracle.token_rows(raw["req_len"], r["perm"], r["total_tokens"])
+    # present x / y in sorted order: the routed oracle then reads rows 0..end
+    ps = dict(p)
+    ps["x"] = raw["x_qkv"][sorted_rows]
+    ps["slices"] = [dict(sl, y=raw["y_qkv"][sorted_rows]) for sl in p["slices"]]
+    rows = np.arange(r["end"])
+    u1, y1 = oracle.problem_rows(ps, rows)
+    slot_sorted = oracle.row_slots(raw["req_slot"], raw["req_len"])[sorted_rows]
+    u2, y2 = oracle.problem_token_rows(ps, np.arange(r["total_tokens"]), slot_sorted)
+    assert np.array_equal(u1, u2[:r["end"]])
+    for a, b in zip(y1, y2):
+        assert np.array_equal(a, b[:r["end"]])
+    yin = oracle.to_f64(ps["slices"][0]["y"], "bf16")
+    assert np.array_equal(y2[0][r["end"]:], yin[r["end"]:, :y2[0].shape[1]])
+
+
+def test_per_token_merged_weight():
+    rng = np.random.default_rng(13)
+    S, R, k, o = 3, 4, 10, 6
+    A = rng.standard_normal((S, R, k))
+    B = rng.standard_normal((S, o, R))
+    x = rng.standard_normal((7, k))
+    W0 = rng.standard_normal((o, k))
+    y = x @ W0.T
+    slots = np.array([2, -1, 0, 0, 1, -1, 2], dtype=np.int32)
+    sl = [{"A": A, "A_slot_stride": R * k, "B": B, "B_slot_stride": o * R, "out_dim": o, "y_in": y}]
+    _, (yo,) = oracle.sgmv_token_slots(slots, x, sl, k, R, S)
+    for t, s in enumerate(slots):
+        W = W0 + (B[s] @ A[s] if s >= 0 else 0)
+        np.testing.assert_allclose(yo[t], W @ x[t], rtol=1e-12, atol=1e-12)

@@ -42,14 +42,14 @@ class LoraError(RuntimeError):
 class _Slice(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("A_slot_stride", ctypes.c_int64), ("B", ctypes.c_void_p),
                 ("B_slot_stride", ctypes.c_int64), ("out_dim", ctypes.c_int32), ("y", ctypes.c_void_p),
-                ("y_row_stride", ctypes.c_int64)]
+                ("y_row_stride", ctypes.c_int64), ("bias", ctypes.c_void_p), ("bias_slot_stride", ctypes.c_int64)]
 
 
 class _Problem(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("num_tokens", ctypes.c_int32), ("in_dim", ctypes.c_int32),
                 ("max_num_loras", ctypes.c_int32), ("max_lora_rank", ctypes.c_int32),
                 ("x", ctypes.c_void_p), ("x_row_stride", ctypes.c_int64),
-                ("num_slices", ctypes.c_int32), ("slices", _Slice * MAX_SLICES)]
+                ("num_slices", ctypes.c_int32), ("slices", _Slice * MAX_SLICES), ("slot_ranks", ctypes.c_void_p)]
 
 
 class _Routing(ctypes.Structure):
@@ -81,6 +81,8 @@ def lib():
     L.lora_build_routing.argtypes = [i32, i32p, i32p, i32, i32p, i32p, i32p, i32p, i32p, i32p]
     L.lora_build_token_rows.restype = ctypes.c_int
     L.lora_build_token_rows.argtypes = [i32, i32p, i32p, i32, i32p]
+    L.lora_set_slot_bias.restype = ctypes.c_int
+    L.lora_set_slot_bias.argtypes = [ctypes.POINTER(_Problem), i32, i32, vp, ctypes.c_int, vp]
     L.lora_set_slot.restype = ctypes.c_int
     L.lora_set_slot.argtypes = [ctypes.POINTER(_Problem), i32, i32, i32, ctypes.c_double, i32, vp, vp,
                                 ctypes.c_int, vp]
@@ -191,6 +193,9 @@ class Slice:
     A_offset: int = 0
     B_offset: int = 0
     y_col: int = 0
+    bias: object = None          # optional [S, >= out] stack (element offset bias_offset)
+    bias_slot_stride: int = 0
+    bias_offset: int = 0
 
 
 @dataclass
@@ -199,6 +204,7 @@ class Problem:
     slices: List[Slice]
     max_num_loras: int
     max_lora_rank: int
+    slot_ranks: object = None    # optional device int32 [S]: true ranks (skip the padding)
     _keep: list = field(default_factory=list)
 
     def _c(self) -> _Problem:
@@ -219,11 +225,14 @@ class Problem:
                     raise ValueError("x, y, A and B must share one dtype")
             if s.y.dim() != 2 or s.y.stride(1) != 1:
                 raise ValueError("y must be 2-D with unit column stride")
+            bias_ptr = s.bias.data_ptr() + es * int(s.bias_offset) if s.bias is not None else None
             arr[j] = _Slice(s.A.data_ptr() + es * int(s.A_offset), int(s.A_slot_stride),
                             s.B.data_ptr() + es * int(s.B_offset), int(s.B_slot_stride), int(s.out_dim),
-                            s.y.data_ptr() + es * int(s.y_col), int(s.y.stride(0)))
+                            s.y.data_ptr() + es * int(s.y_col), int(s.y.stride(0)), bias_ptr,
+                            int(s.bias_slot_stride))
+        ranks = self.slot_ranks.data_ptr() if self.slot_ranks is not None else None
         return _Problem(dt, int(x.shape[0]), int(x.shape[1]), int(self.max_num_loras),
-                        int(self.max_lora_rank), x.data_ptr(), int(x.stride(0)), len(self.slices), arr)
+                        int(self.max_lora_rank), x.data_ptr(), int(x.stride(0)), len(self.slices), arr, ranks)
 
 
 def fused_problem(x, A_fused, B_fused, y, out_dims: Sequence[int]) -> Problem:
@@ -266,6 +275,16 @@ def lora_set_slot(problem: Problem, slice_index: int, slot: int, r: int, lora_al
     _check(L.lora_set_slot(ctypes.byref(c), int(slice_index), int(slot), int(r), float(lora_alpha),
                            int(bool(use_rslora)), pa, pb, raw_dt, _stream_handle(stream)),
            "lora_set_slot")
+
+
+def lora_set_slot_bias(problem: Problem, slice_index: int, slot: int, bias_raw, stream=None) -> None:
+    import torch
+    L = lib()
+    raw_dt = DTYPE_BF16 if (bias_raw is not None and bias_raw.dtype == torch.bfloat16) else DTYPE_F32
+    c = problem._c()
+    _check(L.lora_set_slot_bias(ctypes.byref(c), int(slice_index), int(slot),
+                                bias_raw.data_ptr() if bias_raw is not None else None, raw_dt,
+                                _stream_handle(stream)), "lora_set_slot_bias")
 
 
 def lora_shrink(problem: Problem, routing: Routing, u, stream=None) -> None:

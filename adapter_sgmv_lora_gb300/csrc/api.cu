@@ -43,6 +43,7 @@ lora_status_t validate_problem(const lora_problem_t* p) {
     if (s.A_slot_stride < R * p->in_dim) return LORA_ERR_SHAPE;
     if (s.B_slot_stride < R * s.out_dim) return LORA_ERR_SHAPE;
     if (s.y_row_stride < s.out_dim) return LORA_ERR_SHAPE;
+    if (s.bias && s.bias_slot_stride < s.out_dim) return LORA_ERR_SHAPE;
   }
   return LORA_OK;
 }
@@ -69,8 +70,9 @@ ProblemDesc make_desc(const lora_problem_t* p, const lora_routing_t* r) {
   for (int j = 0; j < p->num_slices; ++j) {
     const lora_slice_t& s = p->slices[j];
     d.sl[j] = SliceDesc{s.A, (long long)s.A_slot_stride, s.B, (long long)s.B_slot_stride,
-                        s.out_dim, s.y, (long long)s.y_row_stride};
+                        s.out_dim, s.y, (long long)s.y_row_stride, s.bias, (long long)s.bias_slot_stride};
   }
+  d.slot_ranks = p->slot_ranks;
   if (r) {
     d.lora_ids = r->lora_ids;
     d.offs = r->grouped_offsets;
@@ -127,6 +129,18 @@ extern "C" lora_status_t lora_set_slot(const lora_problem_t* problem, int32_t sl
   ProblemDesc d = make_desc(problem, nullptr);
   return cuda_status(launch_set_slot(d, slice, slot, r, scale, A_raw, B_raw, raw_dtype,
                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" lora_status_t lora_set_slot_bias(const lora_problem_t* problem, int32_t slice, int32_t slot,
+                                            const void* bias_raw, lora_dtype_t raw_dtype, lora_stream_t stream) {
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if (slice < 0 || slice >= problem->num_slices) return LORA_ERR_SHAPE;
+  if (!problem->slices[slice].bias) return LORA_ERR_NULL;
+  if (slot < 0 || slot >= problem->max_num_loras) return LORA_ERR_SLOT_RANGE;
+  if (raw_dtype != LORA_DTYPE_F32 && raw_dtype != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  ProblemDesc d = make_desc(problem, nullptr);
+  return cuda_status(launch_set_bias(d, slice, slot, bias_raw, raw_dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" lora_status_t lora_shrink(const lora_problem_t* problem, const lora_routing_t* routing,

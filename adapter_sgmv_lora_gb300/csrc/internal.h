@@ -18,6 +18,8 @@ struct SliceDesc {
   int out_dim;
   void* y;
   long long y_row_stride;
+  const void* bias;  // [S, out_dim] at bias + s * bias_slot_stride, or nullptr
+  long long bias_slot_stride;
 };
 
 // A validated problem plus its routing, passed by value to every kernel.
@@ -36,6 +38,7 @@ struct ProblemDesc {
   int G;
   int end;
   const int* token_rows;  // device [end] or nullptr (row i of the sorted order is row i)
+  const int* slot_ranks;  // device [S] true ranks, or nullptr (all R)
   unsigned* status;  // device status word (LORA_DEV_* flags)
 };
 
@@ -47,6 +50,8 @@ cudaError_t launch_shrink_simple(const ProblemDesc& p, float* u, cudaStream_t s)
 cudaError_t launch_expand_simple(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl);
 cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, float scale,
                             const void* A_raw, const void* B_raw, int raw_dtype, cudaStream_t s);
+cudaError_t launch_set_bias(const ProblemDesc& p, int slice, int slot, const void* bias_raw, int raw_dtype,
+                            cudaStream_t s);
 
 // bf16 fast path (tensor cores + bulk copies + clusters).  `fast_path_ok`
 // tells whether a problem meets its alignment / size preconditions.

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   constexpr int MAXR = (MT + NB + 15) / 16;  // rows per thread
   const int nrows_total = t.rows + nvalid;
   const int ch = threadIdx.x & 7;
+  const int kmax = slot_kmax(p, t.slot);  // rank columns past this are zero: not read
   const __nv_bfloat16* srcs[MAXR];
   uint32_t dsts[MAXR];
   int bad_row = 0;
@@ -121,9 +122,11 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     } else if (row < nrows_total) {
       const int col = n0 + row - t.rows;
       const int j = col / R, k = col - j * R;
-      srcs[i] = static_cast<const __nv_bfloat16*>(p.sl[j].A) + (long long)t.slot * p.sl[j].A_slot_stride +
-                (long long)k * p.in_dim + k0 + ch * 8;
-      dsts[i] = (MT + row - t.rows) * XPITCH + ch * 16;
+      if (k < kmax) {
+        srcs[i] = static_cast<const __nv_bfloat16*>(p.sl[j].A) + (long long)t.slot * p.sl[j].A_slot_stride +
+                  (long long)k * p.in_dim + k0 + ch * 8;
+        dsts[i] = (MT + row - t.rows) * XPITCH + ch * 16;
+      }
     }
   }
   (void)warp;
@@ -193,8 +196,12 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
 #pragma unroll
     for (int nt = 0; nt < NB / 8; ++nt) {
       const int row = warp * 16 + g, col = nt * 8 + 2 * tq;
-      *reinterpret_cast<float2*>(&P[row * Cfg::PPITCH + col]) = make_float2(acc[nt][0], acc[nt][1]);
-      *reinterpret_cast<float2*>(&P[(row + 8) * Cfg::PPITCH + col]) = make_float2(acc[nt][2], acc[nt][3]);
+      // Columns past the slot's rank read no A rows (stale shared memory): 0.
+      const bool keep = ((n0 + col) % R) < kmax;
+      *reinterpret_cast<float2*>(&P[row * Cfg::PPITCH + col]) =
+          keep ? make_float2(acc[nt][0], acc[nt][1]) : make_float2(0.f, 0.f);
+      *reinterpret_cast<float2*>(&P[(row + 8) * Cfg::PPITCH + col]) =
+          keep ? make_float2(acc[nt][2], acc[nt][3]) : make_float2(0.f, 0.f);
     }
   }
   const int q4 = nvalid / 4;
@@ -330,9 +337,10 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
     if (ch < ych)
       cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)s_rows[r] * sl.y_row_stride + o0 + ch * 8);
   }
+  const int kmax = slot_kmax(p, t.slot);  // B columns past this are not read
   for (int c = threadIdx.x; c < ovalid * BW; c += blockDim.x) {
     const int o = c / BW, ch = c % BW;
-    cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
+    if (ch * 8 < kmax) cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
   }
   cp_async_commit();
 
@@ -388,14 +396,23 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
       acc[nt][1] = __high2float(v0);
       acc[nt][2] = __low2float(v1);
       acc[nt][3] = __high2float(v1);
+      if (sl.bias && o0 + col < sl.out_dim) {  // bias joins y before the one rounding
+        const __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(
+            static_cast<const __nv_bfloat16*>(sl.bias) + (long long)t.slot * sl.bias_slot_stride + o0 + col);
+        acc[nt][0] += __low2float(bv);
+        acc[nt][1] += __high2float(bv);
+        acc[nt][2] += __low2float(bv);
+        acc[nt][3] += __high2float(bv);
+      }
     }
     const uint32_t hs = smem_addr(Hs), bs = smem_addr(Bs);
 #pragma unroll
     for (int kk = 0; kk < (2 * R) / 16; ++kk) {
+      const int kb = (kk * 16) % R;
+      if (kb >= kmax) continue;  // past the slot's rank (hi and lo halves alike)
       uint32_t a[4];
       ldsm_x4(hs + (m * 16 + (lane & 15)) * Cfg::UPITCH + (kk * 16 + (lane >> 4) * 8) * 2, a[0], a[1],
               a[2], a[3]);
-      const int kb = (kk * 16) % R;
 #pragma unroll
       for (int np = 0; np < NT / 2; ++np) {
         uint32_t b0, b1, b2, b3;
@@ -556,6 +573,7 @@ bool fast_path_ok(const ProblemDesc& p, const void* u) {
     if (!aligned16(sl.A) || !aligned16(sl.B) || !aligned16(sl.y)) return false;
     if (sl.A_slot_stride % 8 != 0 || sl.B_slot_stride % 8 != 0) return false;
     if (sl.out_dim % 8 != 0 || sl.y_row_stride % 8 != 0) return false;
+    if (sl.bias && (!aligned16(sl.bias) || sl.bias_slot_stride % 8 != 0)) return false;
   }
   return true;
 }

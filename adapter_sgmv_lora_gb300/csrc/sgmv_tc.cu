@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   __shared__ Tile s_tile;
   __shared__ int s_ok;
   __shared__ int s_fail;
+  __shared__ int s_kmax;
 
   // 1024-byte aligned ring (the 128-byte swizzle repeats every 1024 bytes).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
       s_tile = t;
       s_ok = ok;
       s_fail = 0;
+      s_kmax = ok ? slot_kmax(p, t.slot) : 0;
       for (int i = 0; i < NSTAGE; ++i) {
         mbar_init(&full[i], 1);
         mbar_init(&empty[i], 1);
@@ -107,6 +109,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   const Tile t = s_tile;
   const bool ok = s_ok != 0;
   const int R = p.R;
+  const int kmax = s_kmax;  // A rows past this (per slice) are not loaded
   const int kc = p.in_dim / nsplit;
   const int k0 = split * kc;
   const int nst = kc / TK;
@@ -123,11 +126,12 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
       }
       uint8_t* xs = smem + slot * Cfg::STAGE;
       uint8_t* as = xs + Cfg::X_BYTES;
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::X_BYTES + p.n_slices * R * TK * 2));
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::X_BYTES + p.n_slices * kmax * TK * 2));
       const int kk = k0 + s * TK;
       tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
       for (int j = 0; j < p.n_slices; ++j)
-        tma_load_3d_hint(as + j * R * TK * 2, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
+        for (int kb = 0; kb < kmax; kb += 16)  // 16-row boxes of the slot's A rows
+          tma_load_3d_hint(as + (j * R + kb) * TK * 2, &maps.a[j], kk, kb, t.slot, &full[slot], pol_keep);
     }
   } else if (ok && warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -168,9 +172,12 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
         if (row < t.rows) {
+          // Columns past the slot's rank came from rows never loaded: 0.
+          const bool keep = (c % R) < kmax;
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(up + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            *reinterpret_cast<float4*>(up + c + i) =
+                keep ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
     }
@@ -224,7 +231,7 @@ bool encode_maps(const ProblemDesc& p, TcMaps* m) {
   for (int j = 0; j < p.n_slices; ++j) {
     const cuuint64_t dims[3] = {(cuuint64_t)p.in_dim, (cuuint64_t)p.R, (cuuint64_t)p.S};
     const cuuint64_t strides[2] = {(cuuint64_t)p.in_dim * 2, (cuuint64_t)p.sl[j].A_slot_stride * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)TK, (cuuint32_t)p.R, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)TK, 16, 1};
     if (enc(&m->a[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.sl[j].A), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -365,7 +372,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
   __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], tfull[2], tempty[2], uready;
   __shared__ uint32_t s_tmem;
   __shared__ Tile s_tile;
-  __shared__ int s_ok, s_fail;
+  __shared__ int s_ok, s_fail, s_kmax;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Ua = smem;
@@ -386,6 +393,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       s_tile = t;
       s_ok = ok;
       s_fail = 0;
+      s_kmax = ok ? slot_kmax(p, t.slot) : 0;
       for (int i = 0; i < NSLOT; ++i) {
         mbar_init(&full[i], 1);
         mbar_init(&empty[i], 4);
@@ -408,6 +416,8 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
   const uint32_t tmem = s_tmem;
   const Tile t = s_tile;
   const bool ok = s_ok != 0;
+  const int kmax = s_kmax;  // rank columns past this: no B boxes, no MMA steps
+  const int nbbox = (kmax + 63) / 64;
 
   if (ok && warp == 0 && lane == 0) {
     // ---- producer: y and B of block i into slot i % 2 (independent of the
@@ -422,10 +432,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       uint8_t* ys = smem + Cfg::U_BYTES + slot * Cfg::SLOT;
       uint8_t* bs = ys + Cfg::Y_BYTES;
       const int o0 = (b_first + i) * XB;
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + Cfg::B_BYTES));
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + nbbox * XB * 128));
       tma_load_2d_hint(ys, &maps.y[j], o0, t.row0, &full[slot], pol_stream);
       tma_load_2d_hint(ys + TM * 128, &maps.y[j], o0 + 64, t.row0, &full[slot], pol_stream);
-      for (int kb = 0; kb < R / 64; ++kb)
+      for (int kb = 0; kb < nbbox; ++kb)
         tma_load_3d_hint(bs + kb * XB * 128, &maps.b[j], kb * 64, o0, t.slot, &full[slot], pol_keep);
     }
   } else if (ok && warp == 1 && lane == 0) {
@@ -443,12 +453,15 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       tc_fence_after_sync();
       const uint32_t ua = smem_addr(Ua);
       const uint32_t bs = smem_addr(smem + Cfg::U_BYTES + slot * Cfg::SLOT + Cfg::Y_BYTES);
+      uint32_t acc = 0;
 #pragma unroll
       for (int ks = 0; ks < 2 * R / 16; ++ks) {
-        const uint64_t adesc = sw128_desc(ua + (ks >> 2) * TM * 128 + (ks & 3) * 32);
         const int kbk = (ks * 16) % R;  // the lo half reuses B's K columns
+        if (kbk >= kmax) continue;      // past the slot's rank
+        const uint64_t adesc = sw128_desc(ua + (ks >> 2) * TM * 128 + (ks & 3) * 32);
         const uint64_t bdesc = sw128_desc(bs + (kbk >> 6) * XB * 128 + ((kbk & 63) >> 4) * 32);
-        tc_mma_bf16(tmem + buf * XB, adesc, bdesc, idesc, ks > 0 ? 1u : 0u);
+        tc_mma_bf16(tmem + buf * XB, adesc, bdesc, idesc, acc);
+        acc = 1;
       }
       tc_commit(&tfull[buf]);
     }
@@ -517,7 +530,24 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const int ovalid = min(XB, sl.out_dim - o0);
         for (int c16 = 0; c16 < XB / 16; ++c16) {
           float d[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
+          if (kmax > 0) {
+            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
+          } else {  // rank 0: no MMA was issued for this block, the delta is zero
+#pragma unroll
+            for (int i = 0; i < 16; ++i) d[i] = 0.f;
+          }
+          if (sl.bias && c16 * 16 < ovalid) {  // bias joins the delta before the one rounding
+            const uint4* bp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(sl.bias) +
+                                                             (long long)t.slot * sl.bias_slot_stride + o0 + c16 * 16);
+            const uint4 b0 = __ldg(bp);
+            const uint4 b1 = (c16 * 16 + 8 < ovalid) ? __ldg(bp + 1) : make_uint4(0, 0, 0, 0);
+            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              d[2 * e] += __uint_as_float(bw[e] << 16);
+              d[2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
+            }
+          }
           if (live && c16 * 16 < ovalid) {
             uint32_t out[8];
 #pragma unroll

@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(256) shrink_simple_kernel(const __grid_constan
   const int col = (int)(task % nR);
   const int j = col / p.R, k = col % p.R;
   const int slot = p.lora_ids[group_of_row(p, t)];
+  if (k >= slot_kmax(p, slot)) {  // past the slot's rank: zero, A not read
+    if (lane == 0) u[(long long)t * nR + col] = 0.f;
+    return;
+  }
   const T* a = static_cast<const T*>(p.sl[j].A) + (long long)slot * p.sl[j].A_slot_stride +
                (long long)k * p.in_dim;
   const int xr = p.token_rows ? p.token_rows[t] : t;  // row of x holding token t
@@ -102,7 +106,10 @@ __global__ void __launch_bounds__(256) expand_simple_kernel(const __grid_constan
   }
   T* y = static_cast<T*>(p.sl[j].y) + (long long)yr * p.sl[j].y_row_stride + o;
   float acc = 0.f;
-  for (int k = 0; k < p.R; ++k) acc = fmaf(to_f32(b[k]), ut[k], acc);
+  const int kmax = slot_kmax(p, slot);
+  for (int k = 0; k < kmax; ++k) acc = fmaf(to_f32(b[k]), ut[k], acc);
+  if (p.sl[j].bias)
+    acc += to_f32(static_cast<const T*>(p.sl[j].bias)[(long long)slot * p.sl[j].bias_slot_stride + o]);
   *y = from_f32<T>(to_f32(*y) + acc);
 }
 
@@ -132,6 +139,33 @@ __global__ void set_slot_kernel(const __grid_constant__ ProblemDesc p, int slice
       B[f] = from_f32<T>(v);
     }
   }
+}
+
+// Bias preparation: bias[slot, o] = cast(bias_raw[o]), or zero when bias_raw is null.
+template <typename T, typename RawT>
+__global__ void set_bias_kernel(const __grid_constant__ ProblemDesc p, int slice, int slot,
+                                const RawT* __restrict__ bias_raw) {
+  const SliceDesc& sl = p.sl[slice];
+  T* b = static_cast<T*>(const_cast<void*>(sl.bias)) + (long long)slot * sl.bias_slot_stride;
+  for (int o = blockIdx.x * blockDim.x + threadIdx.x; o < sl.out_dim; o += gridDim.x * blockDim.x)
+    b[o] = bias_raw ? from_f32<T>(to_f32(bias_raw[o])) : from_f32<T>(0.f);
+}
+
+cudaError_t launch_set_bias(const ProblemDesc& p, int slice, int slot, const void* bias_raw, int raw_dtype,
+                            cudaStream_t s) {
+  const unsigned g = (unsigned)((p.sl[slice].out_dim + 255) / 256);
+  if (p.dtype == LORA_DTYPE_BF16) {
+    if (raw_dtype == LORA_DTYPE_BF16)
+      set_bias_kernel<__nv_bfloat16, __nv_bfloat16><<<g, 256, 0, s>>>(p, slice, slot, (const __nv_bfloat16*)bias_raw);
+    else
+      set_bias_kernel<__nv_bfloat16, float><<<g, 256, 0, s>>>(p, slice, slot, (const float*)bias_raw);
+  } else {
+    if (raw_dtype == LORA_DTYPE_BF16)
+      set_bias_kernel<float, __nv_bfloat16><<<g, 256, 0, s>>>(p, slice, slot, (const __nv_bfloat16*)bias_raw);
+    else
+      set_bias_kernel<float, float><<<g, 256, 0, s>>>(p, slice, slot, (const float*)bias_raw);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_shrink_simple(const ProblemDesc& p, float* u, cudaStream_t s) {

@@ -105,6 +105,16 @@ __device__ __forceinline__ bool warp_check_routing(const ProblemDesc& p) {
   return bad == 0;
 }
 
+// Rank columns of slot `slot` that can be non-zero: ceil16 of its true rank
+// when the problem carries slot_ranks (clamped to [0, R]), else R.
+__device__ __forceinline__ int slot_kmax(const ProblemDesc& p, int slot) {
+  if (!p.slot_ranks) return p.R;
+  int r = p.slot_ranks[slot];
+  r = r < 0 ? 0 : r;
+  r = (r + 15) & ~15;
+  return r < p.R ? r : p.R;
+}
+
 // Group of routed row t (binary search; routing already validated).
 __device__ __forceinline__ int group_of_row(const ProblemDesc& p, int t) {
   int lo = 0, hi = p.G - 1;

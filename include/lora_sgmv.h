@@ -94,6 +94,13 @@ typedef struct {
   int32_t out_dim;
   void* y;
   int64_t y_row_stride;
+  /* Optional LoRA bias ("MAX max.pipelines.lora 模块解析", LoRA types: BIAS, the
+   * bias attached to B; "vLLM LoRA 实现深度解析" section 8, --enable-lora-bias):
+   * slot s's vector of out_dim values at bias + s*bias_slot_stride, storage
+   * type, added unscaled to every routed row (inside the one rounding).
+   * NULL: no bias. */
+  const void* bias;
+  int64_t bias_slot_stride;
 } lora_slice_t;
 
 /*
@@ -111,6 +118,12 @@ typedef struct {
   int64_t x_row_stride;
   int32_t num_slices;
   lora_slice_t slices[LORA_MAX_SLICES];
+  /* Optional DEVICE int32 [max_num_loras]: the true rank r_s of each slot
+   * (0..max_lora_rank), a hint that lets the kernels skip the zero padding:
+   * rank columns from ceil16(r_s) on (A rows, B columns) are then never read
+   * and contribute nothing; columns [r_s, ceil16(r_s)) must still be zero, as
+   * lora_set_slot writes them.  NULL: every slot uses max_lora_rank. */
+  const int32_t* slot_ranks;
 } lora_problem_t;
 
 /*
@@ -199,6 +212,17 @@ lora_status_t lora_set_slot(const lora_problem_t* problem, int32_t slice, int32_
                             const void* B_raw, lora_dtype_t raw_dtype, lora_stream_t stream);
 
 /*
+ * lora_set_slot_bias -- load-time preparation of slot `slot`'s bias for slice
+ * `slice`: bias[slot, o] = cast(bias_raw[o]) (round to nearest even), or zero
+ * when bias_raw is NULL.  bias_raw is a contiguous DEVICE array of out_dim
+ * values of raw_dtype.  The slice's bias pointer must be set.
+ * Errors: LORA_ERR_NULL (no bias stack), LORA_ERR_SLOT_RANGE, LORA_ERR_SHAPE,
+ * LORA_ERR_DTYPE.
+ */
+lora_status_t lora_set_slot_bias(const lora_problem_t* problem, int32_t slice, int32_t slot,
+                                 const void* bias_raw, lora_dtype_t raw_dtype, lora_stream_t stream);
+
+/*
  * lora_shrink -- u[t, j*R + k] = sum_i A_j[lora_ids[g], k, i] * x[t, i] for
  * every routed row t < end (group g), slice j, k < R.  u is a DEVICE fp32
  * array [end, num_slices*R] (row stride num_slices*R), fully overwritten.
@@ -209,7 +233,8 @@ lora_status_t lora_shrink(const lora_problem_t* problem, const lora_routing_t* r
 
 /*
  * lora_expand -- boundary-aware expand: y_j[t, o] = rn(y_j[t, o] +
- * sum_k B_j[lora_ids[g], o, k] * u[t, j*R + k]) for routed rows t < end only,
+ * bias_j[s, o] + sum_k B_j[s, o, k] * u[t, j*R + k]) with s = lora_ids[g]
+ * (bias only when the slice has one) for routed rows t < end only,
  * with one rounding to the storage type.  u as produced by lora_shrink.
  * Accumulation is fp32.  On the bf16 tensor-core path u enters the product as
  * two bf16 terms (u = hi + lo, 16 significant bits, the split is exact);

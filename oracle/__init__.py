@@ -56,6 +56,8 @@ class _Slice(ctypes.Structure):
         ("y_in_row_stride", ctypes.c_longlong),
         ("y_out", ctypes.c_void_p),
         ("y_out_row_stride", ctypes.c_longlong),
+        ("bias", ctypes.c_void_p),
+        ("bias_slot_stride", ctypes.c_longlong),
     ]
 
 
@@ -218,6 +220,15 @@ def lora_memory_bytes(num_lora_layers: int, in_features: int, out_features: int,
 # The delta
 # --------------------------------------------------------------------------
 
+def _bias_args(sl, keep):
+    """(pointer, slot stride) of a slice's optional fp64 bias stack."""
+    if sl.get("bias") is None:
+        return None, 0
+    b = np.ascontiguousarray(sl["bias"], dtype=np.float64)
+    keep.append(b)
+    return b.ctypes.data + 8 * int(sl.get("bias_offset", 0)), int(sl["bias_slot_stride"])
+
+
 def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim: int, R: int,
               max_num_loras: int):
     """Delta for the listed rows, in double.
@@ -251,8 +262,9 @@ def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim:
         keep += [A, B, yi, yo]
         base_a = A.ctypes.data + 8 * int(sl.get("A_offset", 0))
         base_b = B.ctypes.data + 8 * int(sl.get("B_offset", 0))
+        bias_ptr, bias_stride = _bias_args(sl, keep)
         arr[j] = _Slice(base_a, int(sl["A_slot_stride"]), base_b, int(sl["B_slot_stride"]), od,
-                        yi.ctypes.data, od, yo.ctypes.data, od)
+                        yi.ctypes.data, od, yo.ctypes.data, od, bias_ptr, bias_stride)
         outs.append(yo)
     ids = _i32(lora_ids)
     offs = _i32(grouped_offsets)
@@ -296,8 +308,12 @@ def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
     route = build_routing(raw["req_slot"], raw["req_len"], S)
     in_dim = raw["x_" + proj].shape[1]
     outs = [raw["out_dims"][nm] for nm in names]
-    stacks_a, stacks_b = [], []
+    stacks_a, stacks_b, stacks_bias = [], [], []
+    has_bias = raw.get("bias") is not None
     for nm in names:
+        if has_bias:  # the bias is added unscaled; stored in the storage type
+            stacks_bias.append(np.stack([from_f32(np.asarray(raw["bias"][nm][s], dtype=np.float32), dt)
+                                         for s in range(S)]))
         a_s, b_s = [], []
         for s in range(S):
             r = int(raw["rank"][s])
@@ -313,21 +329,28 @@ def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
         B_st = np.stack([fuse_qkv_b([stacks_b[j][s] for j in range(len(names))]) for s in range(S)])
         A64, B64 = to_f64(A_st, dt), to_f64(B_st, dt)
         O = sum(outs)
+        bias64 = to_f64(np.concatenate(stacks_bias, axis=1), dt) if has_bias else None
         off = 0
         for j, od in enumerate(outs):
             slices.append({"A": A64, "A_offset": j * R * in_dim, "A_slot_stride": len(names) * R * in_dim,
                            "B": B64, "B_offset": off * R, "B_slot_stride": O * R, "out_dim": od,
-                           "y": y, "y_col0": off})
+                           "y": y, "y_col0": off, "bias": bias64, "bias_offset": off, "bias_slot_stride": O})
             off += od
         stored = {"A": A_st, "B": B_st}
+        if has_bias:
+            stored["bias"] = np.concatenate(stacks_bias, axis=1)
     else:
         off = 0
         for j, od in enumerate(outs):
             slices.append({"A": to_f64(stacks_a[j], dt), "A_offset": 0, "A_slot_stride": R * in_dim,
                            "B": to_f64(stacks_b[j], dt), "B_offset": 0, "B_slot_stride": od * R,
-                           "out_dim": od, "y": y, "y_col0": off})
+                           "out_dim": od, "y": y, "y_col0": off,
+                           "bias": to_f64(stacks_bias[j], dt) if has_bias else None, "bias_offset": 0,
+                           "bias_slot_stride": od})
             off += od
         stored = {"A": stacks_a, "B": stacks_b} if len(names) > 1 else {"A": stacks_a[0], "B": stacks_b[0]}
+        if has_bias:
+            stored["bias"] = stacks_bias if len(names) > 1 else stacks_bias[0]
     return {"dtype": dt, "S": S, "R": R, "in_dim": in_dim, "x": raw["x_" + proj], "slices": slices,
             "lora_ids": route["lora_ids"], "grouped_offsets": route["grouped_offsets"],
             "end": route["end"], "route": route, "stored": stored, "out_dims": outs}
@@ -372,9 +395,10 @@ def sgmv_token_slots(row_slot, x_rows, slices, in_dim: int, R: int, max_num_lora
         od = int(sl["out_dim"])
         yo = np.empty((n, od), dtype=np.float64)
         keep += [A, B, yi, yo]
+        bias_ptr, bias_stride = _bias_args(sl, keep)
         arr[j] = _Slice(A.ctypes.data + 8 * int(sl.get("A_offset", 0)), int(sl["A_slot_stride"]),
                         B.ctypes.data + 8 * int(sl.get("B_offset", 0)), int(sl["B_slot_stride"]), od,
-                        yi.ctypes.data, od, yo.ctypes.data, od)
+                        yi.ctypes.data, od, yo.ctypes.data, od, bias_ptr, bias_stride)
         outs.append(yo)
     u = np.empty((n, ns * R), dtype=np.float64)
     rc = L.oracle_sgmv_token_slots(n, _p32(rs), int(in_dim), int(R), int(max_num_loras), ns, arr,

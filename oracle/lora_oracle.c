@@ -121,7 +121,9 @@ int oracle_build_routing(int n_req, const int* req_slot, const int* req_len, int
  * For the fused q/k/v layout the caller points slice j at
  *   A_fused + j*R*in_dim (slot stride n*R*in_dim) and
  *   B_fused + off_j*R    (slot stride O*R),
- * which is exactly the block-diagonal reading of the fused weights. */
+ * which is exactly the block-diagonal reading of the fused weights.
+ * An optional LoRA bias (the BIAS type of the MAX page's LoRA types; vLLM's
+ * --enable-lora-bias) adds bias[s, o] to every routed output. */
 typedef struct {
   const double* A;
   long long A_slot_stride;
@@ -132,6 +134,8 @@ typedef struct {
   long long y_in_row_stride;
   double* y_out;
   long long y_out_row_stride;
+  const double* bias;        /* bias of slot s, output o: bias[s*bias_slot_stride + o]; NULL: none */
+  long long bias_slot_stride;
 } oracle_slice;
 
 /* Group of a LoRA-routed row, by linear scan of the offsets. */
@@ -149,8 +153,8 @@ static int group_of_row(int t, const int* grouped_offsets, int num_groups) {
  * For each listed row with 0 <= t < end, group g (grouped_offsets[g] <= t <
  * grouped_offsets[g+1]) and slot s = lora_ids[g], and for every slice j:
  *     u[r, j*R + k]   = sum_i A_j[s, k, i] * x_rows[r, i]              (k < R)
- *     y_out_j[r, o]   = y_in_j[r, o] + sum_k B_j[s, o, k] * u[r, j*R + k]
- * u may be NULL.  A row t >= end (a base or post-end row) is an error: the
+ *     y_out_j[r, o]   = y_in_j[r, o] + bias_j[s, o] + sum_k B_j[s, o, k] * u[r, j*R + k]
+ * (bias term only when the slice has a bias).  u may be NULL.  A row t >= end (a base or post-end row) is an error: the
  * method never touches those rows, so the oracle refuses to produce them.
  */
 int oracle_sgmv_rows(int n_rows, const int* rows, int in_dim, int R, int max_num_loras,
@@ -193,7 +197,8 @@ int oracle_sgmv_rows(int n_rows, const int* rows, int in_dim, int R, int max_num
         const double* b = sl->B + (long long)s * sl->B_slot_stride + (long long)o * R;
         double acc = 0.0;
         for (int k = 0; k < R; ++k) acc += b[k] * uj[k];
-        yo[o] = yi[o] + acc;
+        const double bias = sl->bias ? sl->bias[(long long)s * sl->bias_slot_stride + o] : 0.0;
+        yo[o] = yi[o] + bias + acc;
       }
     }
   }
@@ -240,7 +245,8 @@ int oracle_sgmv_token_slots(int n_rows, const int* row_slot, int in_dim, int R, 
         const double* b = sl->B + (long long)s * sl->B_slot_stride + (long long)o * R;
         double acc = 0.0;
         for (int k = 0; k < R; ++k) acc += b[k] * uj[k];
-        yo[o] = yi[o] + acc;
+        const double bias = sl->bias ? sl->bias[(long long)s * sl->bias_slot_stride + o] : 0.0;
+        yo[o] = yi[o] + bias + acc;
       }
     }
   }

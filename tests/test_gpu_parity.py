@@ -70,10 +70,30 @@ def _sample_rows(offs, end, rng, extra=48):
     return np.array(sorted(rows), dtype=np.int32)
 
 
-def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0):
+def _poison_padding(dev, raw):
+    """NaN into every A row / B column from ceil16(rank) on: with slot ranks
+    passed, the kernels must never read them."""
+    R = raw["max_lora_rank"]
+    A, B = dev["stacks"]["A"], dev["stacks"]["B"]
+    As = A if isinstance(A, list) else [A]
+    Bs = B if isinstance(B, list) else [B]
+    n = len(dev["names"])
+    for s, r in enumerate(raw["rank"]):
+        k16 = min(R, (int(r) + 15) // 16 * 16)
+        if k16 >= R:
+            continue
+        for a in As:
+            for j in range(a.shape[1] // R):
+                a[s, j * R + k16:(j + 1) * R].fill_(float("nan"))
+        for b in Bs:
+            b[s, :, k16:].fill_(float("nan"))
+
+
+def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0,
+             slot_ranks=False, poison=False):
     """Prepare on the device, run, compare with the oracle.  Returns the device dict."""
     lk, device = _lk(), _dev()
-    dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y)
+    dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y, slot_ranks=slot_ranks)
     ref = oracle.prepare_problem(raw, proj, fused=fused)
     dt = raw["dtype"]
     # routing: library == oracle, bit-exact
@@ -90,6 +110,16 @@ def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=F
         for j in range(len(dev["names"])):
             assert np.array_equal(device.torch_to_storage(dev["stacks"]["A"][j], dt), ref["stored"]["A"][j])
             assert np.array_equal(device.torch_to_storage(dev["stacks"]["B"][j], dt), ref["stored"]["B"][j])
+    if raw.get("bias") is not None:
+        got_b = dev["stacks"]["bias"]
+        want_b = ref["stored"]["bias"]
+        if isinstance(got_b, list):
+            for gb, wb in zip(got_b, want_b):
+                assert np.array_equal(device.torch_to_storage(gb, dt), wb)
+        else:
+            assert np.array_equal(device.torch_to_storage(got_b, dt), want_b)
+    if poison:
+        _poison_padding(dev, raw)
     _plant_sentinels(dev, end)
     y_before = device.y_host(dev)
     prob, routing = dev["problem"], dev["routing"]
@@ -239,6 +269,46 @@ def test_token_rows_out_of_range_is_flagged_and_skipped():
     assert lk.lora_get_device_status() == 0
     lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
     assert lk.lora_get_device_status() & lk.DEV_BAD_ROW
+
+
+# ------------------------------------------ LoRA bias and true-rank hints --
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_bias_decode(mode):
+    run_case(sy.add_bias(sy.draw("decode8b", 5), 5), "qkv", mode=mode)
+    run_case(sy.add_bias(sy.draw("decode8b", 6), 6), "o", mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_bias_and_ranks_long_groups(mode):
+    """tcgen05 path with bias and rank hints (ranks 16/32/64 of max 64), NaN in
+    the padding the hints skip."""
+    spec = _spec(max_num_loras=4, max_lora_rank=64, rank_choices=(16, 32, 64), kind="fixed",
+                 fixed_slots=(3, 0, 2, 1, -1), fixed_lens=(150, 300, 129, 260, 9), hidden=512, n_heads=8,
+                 n_kv_heads=2, head_dim=64)
+    for seed in (1, 2):
+        raw = sy.add_bias(sy.draw(spec, seed), seed)
+        run_case(raw, "qkv", mode=mode, slot_ranks=True, poison=True)
+        run_case(raw, "o", mode=mode, slot_ranks=True, poison=True)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_rank_hints_short_groups(mode):
+    """mma.sync path with rank hints (ranks 16..128 of max 128), NaN padding."""
+    spec = _spec(max_num_loras=6, max_lora_rank=128, rank_choices=(16, 48, 64, 128), n_requests=40,
+                 hidden=512, n_heads=8, n_kv_heads=2, head_dim=64)
+    raw = sy.add_bias(sy.draw(spec, 3), 3)
+    run_case(raw, "qkv", mode=mode, slot_ranks=True, poison=True)
+    run_case(sy.draw(spec, 4), "o", mode=mode, slot_ranks=True, poison=True)
+
+
+def test_bias_and_ranks_generic_path():
+    spec = _spec(dtype="f32", max_lora_rank=32, rank_choices=(8, 32), n_requests=25)
+    run_case(sy.add_bias(sy.draw(spec, 1), 1), "qkv", mode="split", slot_ranks=True, poison=True)
+
+
+def test_bias_unsorted_batch():
+    run_unsorted(sy.add_bias(sy.draw("decode8b", 7), 7), "qkv", "apply")
 
 
 # ------------------------------------------------------------ edge cases --

@@ -437,3 +437,26 @@ def test_per_token_merged_weight():
     for t, s in enumerate(slots):
         W = W0 + (B[s] @ A[s] if s >= 0 else 0)
         np.testing.assert_allclose(yo[t], W @ x[t], rtol=1e-12, atol=1e-12)
+
+
+def test_bias_merged_weight():
+    """With a LoRA bias the routed rows get W0 x + b_s + B_s A_s x; the bias is
+    added unscaled (vLLM page section 8, --enable-lora-bias; MAX page LoRA types)."""
+    rng = np.random.default_rng(15)
+    S, R, k, o = 3, 4, 9, 5
+    A = rng.standard_normal((S, R, k))
+    B = rng.standard_normal((S, o, R))
+    bias = rng.standard_normal((S, o))
+    x = rng.standard_normal((6, k))
+    W0 = rng.standard_normal((o, k))
+    y = x @ W0.T
+    sl = [{"A": A, "A_slot_stride": R * k, "B": B, "B_slot_stride": o * R, "out_dim": o, "y_in": y,
+           "bias": bias, "bias_slot_stride": o}]
+    lora_ids, offs = [1, 2], [0, 2, 5]
+    _, (yo,) = oracle.sgmv_rows(list(range(5)), x[:5], [dict(sl[0], y_in=y[:5])], lora_ids, offs, 5, k, R, S)
+    for t in range(5):
+        s_ = 1 if t < 2 else 2
+        np.testing.assert_allclose(yo[t], (W0 + B[s_] @ A[s_]) @ x[t] + bias[s_], rtol=1e-12, atol=1e-12)
+    _, (yt,) = oracle.sgmv_token_slots([1, 1, 2, 2, 2, -1], x, sl, k, R, S)
+    np.testing.assert_allclose(yt[:5], yo, rtol=0, atol=0)
+    assert np.array_equal(yt[5], y[5])

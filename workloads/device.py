@@ -32,13 +32,16 @@ def torch_to_storage(t: torch.Tensor, dtype: str) -> np.ndarray:
     return t.numpy().copy()
 
 
-def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y: bool = False) -> dict:
+def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y: bool = False,
+            slot_ranks: bool = False) -> dict:
     """Build one projection problem ("qkv", "o", "gateup" or "down") on the device.
 
     fused=True: one fused stack A [S, n*R, in], B [S, O, R] and y [T, O].
     fused=False: per-projection stacks A_j [S, R, in], B_j [S, out_j, R]; y is
     one [T, O] tensor addressed by column offsets, or (separate_y) one tensor
-    per projection.
+    per projection.  When the workload carries a bias (synthetic.add_bias) the
+    slices get bias stacks filled by lora_set_slot_bias; slot_ranks=True
+    passes the slots' true ranks so the kernels skip the padding.
     """
     dt = raw["dtype"]
     tdt = _TORCH_DT[dt]
@@ -50,11 +53,19 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
     x = storage_to_torch(raw["x_" + proj], dt, device)
     T, k = x.shape
     y_all = storage_to_torch(raw["y_" + proj], dt, device)
+    has_bias = raw.get("bias") is not None
     if fused or len(names) == 1:
         A = torch.empty((S, len(names) * R, k), dtype=tdt, device=device)
         B = torch.empty((S, O, R), dtype=tdt, device=device)
         prob = lk.fused_problem(x, A, B, y_all, outs)
         stacks = {"A": A, "B": B}
+        if has_bias:
+            bias = torch.empty((S, O), dtype=tdt, device=device)
+            off = 0
+            for sl, od in zip(prob.slices, outs):
+                sl.bias, sl.bias_slot_stride, sl.bias_offset = bias, O, off
+                off += od
+            stacks["bias"] = bias
         ys = [y_all]
     else:
         As = [torch.empty((S, R, k), dtype=tdt, device=device) for _ in names]
@@ -68,12 +79,22 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
             ys = [y_all]
             prob = lk.per_projection_problem(x, As, Bs, [y_all] * len(names), y_cols=cols)
         stacks = {"A": As, "B": Bs}
+        if has_bias:
+            stacks["bias"] = []
+            for sl, od in zip(prob.slices, outs):
+                sl.bias, sl.bias_slot_stride = torch.empty((S, od), dtype=tdt, device=device), od
+                stacks["bias"].append(sl.bias)
+    if slot_ranks:
+        prob.slot_ranks = torch.from_numpy(np.asarray(raw["rank"], dtype=np.int32)).to(device)
     for j, nm in enumerate(names):
         for s in range(S):
             r = int(raw["rank"][s])
             a_raw = torch.from_numpy(np.ascontiguousarray(raw["A"][nm][s], dtype=np.float32)).to(device)
             b_raw = torch.from_numpy(np.ascontiguousarray(raw["B"][nm][s], dtype=np.float32)).to(device)
             lk.lora_set_slot(prob, j, s, r, float(raw["alpha"][s]), bool(raw["rslora"][s]), a_raw, b_raw)
+            if has_bias:
+                bias_raw = torch.from_numpy(np.ascontiguousarray(raw["bias"][nm][s], dtype=np.float32)).to(device)
+                lk.lora_set_slot_bias(prob, j, s, bias_raw)
     rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], S)
     routing = lk.routing_to_device(rt, device)
     ws = torch.empty(max(lk.lora_workspace_bytes(prob, rt["end"]), 256) // 4, dtype=torch.float32,

@@ -217,3 +217,13 @@ def custom_spec(**kw) -> Spec:
                 n_requests=8, base_prob=0.2, slot_dist="uniform")
     base.update(kw)
     return Spec(**base)
+
+
+def add_bias(raw: dict, seed: int = 0, scale: float = 0.1) -> dict:
+    """Draw a LoRA bias vector per (projection, slot): scale * N(0, 1), fp32.
+    Drawn from its own stream so the rest of the workload is unchanged."""
+    rng = np.random.default_rng([seed, 7919])
+    spec = raw["spec"]
+    raw["bias"] = {p: [np.float32(scale) * rng.standard_normal(spec.out_dims[p], dtype=np.float32)
+                       for _ in range(spec.max_num_loras)] for p in spec.projs}
+    return raw

@@ -89,16 +89,19 @@ def _names(proj):
     return list(PROBLEMS[proj])
 
 
-def algorithmic_bytes(route_host, raw, proj, e=2):
-    """Per-apply algorithmic bytes: routed x rows + touched A/B slots (padded) + y read+write."""
+def algorithmic_bytes(route_host, raw, proj, e=2, slot_ranks=False):
+    """Per-apply algorithmic bytes: routed x rows + touched A/B slots + y read+write.
+    A/B count the padded rank R, or ceil16(rank) per slot when the kernels are
+    given the true ranks (they then skip the rest)."""
     E = route_host["end"]
-    touched = len(set(int(s) for s in route_host["lora_ids"]))
+    touched = sorted(set(int(s) for s in route_host["lora_ids"]))
     names = _names(proj)
     n = len(names)
     O = sum(raw["out_dims"][nm] for nm in names)
     R = raw["max_lora_rank"]
     k = raw["in_dims"][names[0]]
-    return E * k * e + touched * n * R * k * e + touched * O * R * e + 2 * E * O * e
+    ranks = [min(R, (int(raw["rank"][s]) + 15) // 16 * 16) if slot_ranks else R for s in touched]
+    return E * k * e + sum(n * r * k * e + O * r * e for r in ranks) + 2 * E * O * e
 
 
 def algorithmic_flops(route_host, raw, proj):
@@ -280,9 +283,10 @@ def run_ours(args):
     max_sets = args.sets or 64
     while len(sets) < max_sets:
         raw = sy.draw(spec, rank_seed(rank, len(sets)))
-        d0 = device.prepare(raw, P0, fused=spec.fused_qkv)
-        d1 = device.prepare(raw, P1)
-        b = algorithmic_bytes(d0["route_host"], raw, P0) + algorithmic_bytes(d1["route_host"], raw, P1)
+        d0 = device.prepare(raw, P0, fused=spec.fused_qkv, slot_ranks=args.slot_ranks)
+        d1 = device.prepare(raw, P1, slot_ranks=args.slot_ranks)
+        b = (algorithmic_bytes(d0["route_host"], raw, P0, slot_ranks=args.slot_ranks) +
+             algorithmic_bytes(d1["route_host"], raw, P1, slot_ranks=args.slot_ranks))
         sets.append({"raw": raw, "p0": d0, "p1": d1, "bytes": b, "E": d0["route_host"]["end"]})
         foot += b
         if not args.sets and foot >= 4 * l2 and len(sets) >= 2:
@@ -363,7 +367,8 @@ def run_ours(args):
         r1.record(stream)
     torch.cuda.synchronize()
     qkv_ms = r0.elapsed_time(r1) / (reps * NS)
-    qkv_bytes = statistics.mean(algorithmic_bytes(s["p0"]["route_host"], s["raw"], P0) for s in sets)
+    qkv_bytes = statistics.mean(algorithmic_bytes(s["p0"]["route_host"], s["raw"], P0, slot_ranks=args.slot_ranks)
+                                for s in sets)
     clocks = sampler.stop() if sampler else None
 
     (ms, qkv_ms), (tokens,) = reduce_across_ranks([ms, qkv_ms], [tokens], dist, "cuda")
@@ -387,6 +392,8 @@ def run_ours(args):
                    "footprint_MB": round(foot / 1e6, 1), "l2_MB": round(l2 / 2 ** 20, 1),
                    "l2_policy": "inputs larger than L2: %d rotated input sets, %.0f MB > 4x L2" % (NS, foot / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "slot_ranks": "true ranks passed (A/B bytes counted at ceil16(rank))" if args.slot_ranks
+                   else "padded to max_lora_rank",
                    "hbm_GBps_step": round(bytes_steps / (ms * 1e-3) / 1e9, 1),
                    "routed_tokens_per_step": tokens / args.steps / max(world, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -497,6 +504,8 @@ def main():
     ap.add_argument("--workload", default="decode8b", choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--slot-ranks", action="store_true",
+                    help="pass the adapters' true ranks so the kernels skip the rank padding")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -52,8 +52,10 @@ struct TcCfg {
 }  // namespace
 
 struct TcMaps {
-  CUtensorMap x;                    // [T rows, in] bf16, box 64 x 128
-  CUtensorMap a[LORA_MAX_SLICES];   // per slice [S, R, in] bf16, box 64 x R x 1
+  CUtensorMap x;                     // [T rows, in] bf16, box 64 x 128
+  CUtensorMap a[LORA_MAX_SLICES];    // per slice [S, R, in] bf16, box 64 x R x 1 (full rank)
+  CUtensorMap a64[LORA_MAX_SLICES];  // same tensor, box 64 x 64 x 1 (slots below full rank)
+  CUtensorMap a16[LORA_MAX_SLICES];  // same tensor, box 64 x 16 x 1
 };
 
 template <int NR>
@@ -129,9 +131,17 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
       mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::X_BYTES + p.n_slices * kmax * TK * 2));
       const int kk = k0 + s * TK;
       tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
-      for (int j = 0; j < p.n_slices; ++j)
-        for (int kb = 0; kb < kmax; kb += 16)  // 16-row boxes of the slot's A rows
-          tma_load_3d_hint(as + (j * R + kb) * TK * 2, &maps.a[j], kk, kb, t.slot, &full[slot], pol_keep);
+      for (int j = 0; j < p.n_slices; ++j) {
+        if (kmax == R) {  // one box per slice (few large TMA requests)
+          tma_load_3d_hint(as + j * R * TK * 2, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
+        } else {  // below full rank: 64-row boxes, then 16-row boxes, up to the rank only
+          int kb = 0;
+          for (; kb + 64 <= kmax; kb += 64)
+            tma_load_3d_hint(as + (j * R + kb) * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
+          for (; kb < kmax; kb += 16)
+            tma_load_3d_hint(as + (j * R + kb) * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
+        }
+      }
     }
   } else if (ok && warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
     tc_commit(&done);  // accumulator complete
   } else if (ok && warp >= 2) {
     // ---- epilogue: warp w reads TMEM lanes 32*(w % 4) .. +31 (= tile rows)
-    const bool got = mbar_wait(&done, 0);
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0));  // warp-uniform for tcgen05.ld
     tc_fence_after_sync();
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -231,9 +241,19 @@ bool encode_maps(const ProblemDesc& p, TcMaps* m) {
   for (int j = 0; j < p.n_slices; ++j) {
     const cuuint64_t dims[3] = {(cuuint64_t)p.in_dim, (cuuint64_t)p.R, (cuuint64_t)p.S};
     const cuuint64_t strides[2] = {(cuuint64_t)p.in_dim * 2, (cuuint64_t)p.sl[j].A_slot_stride * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)TK, 16, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)TK, (cuuint32_t)p.R, 1};
+    const cuuint32_t box16[3] = {(cuuint32_t)TK, 16, 1};
+    const cuuint32_t box64[3] = {(cuuint32_t)TK, (cuuint32_t)(p.R < 64 ? p.R : 64), 1};
     if (enc(&m->a[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.sl[j].A), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+    if (enc(&m->a64[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.sl[j].A), dims, strides, box64,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+    if (enc(&m->a16[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.sl[j].A), dims, strides, box16,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
@@ -325,14 +345,14 @@ namespace lora {
 namespace {
 
 constexpr int XB = 128;     // output columns per block (MMA N)
-constexpr int XCHUNK = 8;   // blocks per CTA
+constexpr int XCHUNK = 8;   // blocks per CTA (1024 columns)
 
 template <int R>
 struct TxCfg {
   static constexpr int KB = 2 * R / 64;               // 64-wide K blocks of the hi|lo operand
   static constexpr int U_BYTES = KB * TM * 128;       // A operand (u hi|lo)
-  static constexpr int Y_BYTES = 2 * TM * 128;        // two 64-column y boxes
-  static constexpr int B_BYTES = (R / 64) * XB * 128; // R/64 boxes of 128 rows x 64
+  static constexpr int Y_BYTES = (XB / 64) * TM * 128;  // 64-column y boxes
+  static constexpr int B_BYTES = (R / 64) * XB * 128;   // R/64 boxes of XB rows x 64
   static constexpr int SLOT = Y_BYTES + B_BYTES;
   static constexpr int NSLOT = (U_BYTES + 3 * SLOT + 1024 <= 220 * 1024) ? 3 : 2;  // y/B pipeline depth
   static constexpr int SMEM = U_BYTES + NSLOT * SLOT + 1024;
@@ -433,8 +453,8 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       uint8_t* bs = ys + Cfg::Y_BYTES;
       const int o0 = (b_first + i) * XB;
       mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + nbbox * XB * 128));
-      tma_load_2d_hint(ys, &maps.y[j], o0, t.row0, &full[slot], pol_stream);
-      tma_load_2d_hint(ys + TM * 128, &maps.y[j], o0 + 64, t.row0, &full[slot], pol_stream);
+      for (int yb = 0; yb < XB / 64; ++yb)
+        tma_load_2d_hint(ys + yb * TM * 128, &maps.y[j], o0 + yb * 64, t.row0, &full[slot], pol_stream);
       for (int kb = 0; kb < nbbox; ++kb)
         tma_load_3d_hint(bs + kb * XB * 128, &maps.b[j], kb * 64, o0, t.slot, &full[slot], pol_keep);
     }
@@ -518,17 +538,21 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
 
       __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(sl.y) + (long long)(t.row0 + row) * sl.y_row_stride;
       const uint64_t pol_stream = policy_evict_first();
+      // A warp whose wait expired keeps walking the barrier protocol (doing
+      // no work) so the other epilogue warps never block on it.
+      bool bad = false;
       for (int i = 0; i < nblk; ++i) {
         const int slot = i % NSLOT, buf = i & 1;
-        if (!mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
+        if (!bad && !mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
           atomicOr(&s_fail, 1);
-          break;
+          bad = true;
         }
+        bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below needs the whole warp
         tc_fence_after_sync();
         const uint8_t* ys = smem + Cfg::U_BYTES + slot * Cfg::SLOT;
         const int o0 = (b_first + i) * XB;
         const int ovalid = min(XB, sl.out_dim - o0);
-        for (int c16 = 0; c16 < XB / 16; ++c16) {
+        for (int c16 = 0; !bad && c16 < XB / 16; ++c16) {
           float d[16];
           if (kmax > 0) {
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
@@ -565,7 +589,8 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
             }
             uint4* dst = reinterpret_cast<uint4*>(yrow + o0 + c16 * 16);
             st_global_v4_hint(dst, make_uint4(out[0], out[1], out[2], out[3]), pol_stream);
-            if (c16 * 16 + 8 < ovalid) st_global_v4_hint(dst + 1, make_uint4(out[4], out[5], out[6], out[7]), pol_stream);
+            if (c16 * 16 + 8 < ovalid)
+              st_global_v4_hint(dst + 1, make_uint4(out[4], out[5], out[6], out[7]), pol_stream);
           }
         }
         tc_fence_before_sync();

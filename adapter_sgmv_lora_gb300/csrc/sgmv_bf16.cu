@@ -57,7 +57,10 @@ struct ShrinkCfg {
 // C partials are reduced through distributed shared memory into u.
 // plane_stride > 0: no cluster; K-split rank c stores its partial tile into
 // plane c (u + c * plane_stride) and the expand sums the planes.
-template <int NB>
+// GEN: the problem uses token_rows, slot ranks or a bias.  The plain
+// instantiation compiles none of that bookkeeping (it costs registers and a
+// barrier ahead of the first loads, which decode-sized launches feel).
+template <int NB, bool GEN>
 __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                float* __restrict__ u, int C,
                                                                int nblk, int Kc, long long plane_stride) {
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   constexpr int MAXR = (MT + NB + 15) / 16;  // rows per thread
   const int nrows_total = t.rows + nvalid;
   const int ch = threadIdx.x & 7;
-  const int kmax = slot_kmax(p, t.slot);  // rank columns past this are zero: not read
+  const int kmax = GEN ? slot_kmax(p, t.slot) : R;  // rank columns past this are zero: not read
   const __nv_bfloat16* srcs[MAXR];
   uint32_t dsts[MAXR];
   int bad_row = 0;
@@ -112,8 +115,8 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     dsts[i] = 0;
     if (row < t.rows) {
       // Row of x holding this token (gathered batches map through token_rows).
-      const int xr = p.token_rows ? p.token_rows[t.row0 + row] : t.row0 + row;
-      if (xr < 0 || xr >= p.num_tokens) {
+      const int xr = (GEN && p.token_rows) ? p.token_rows[t.row0 + row] : t.row0 + row;
+      if (GEN && (xr < 0 || xr >= p.num_tokens)) {
         bad_row = 1;
         continue;
       }
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     } else if (row < nrows_total) {
       const int col = n0 + row - t.rows;
       const int j = col / R, k = col - j * R;
-      if (k < kmax) {
+      if (!GEN || k < kmax) {
         srcs[i] = static_cast<const __nv_bfloat16*>(p.sl[j].A) + (long long)t.slot * p.sl[j].A_slot_stride +
                   (long long)k * p.in_dim + k0 + ch * 8;
         dsts[i] = (MT + row - t.rows) * XPITCH + ch * 16;
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
 
   // Every CTA of the tile (and of its cluster) checks all of the tile's rows
   // and reaches the same verdict.
-  if (__syncthreads_or(bad_row)) {
+  if (GEN && __syncthreads_or(bad_row)) {
     if (threadIdx.x == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
     return;
   }
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     for (int nt = 0; nt < NB / 8; ++nt) {
       const int row = warp * 16 + g, col = nt * 8 + 2 * tq;
       // Columns past the slot's rank read no A rows (stale shared memory): 0.
-      const bool keep = ((n0 + col) % R) < kmax;
+      const bool keep = !GEN || ((n0 + col) % R) < kmax;
       *reinterpret_cast<float2*>(&P[row * Cfg::PPITCH + col]) =
           keep ? make_float2(acc[nt][0], acc[nt][1]) : make_float2(0.f, 0.f);
       *reinterpret_cast<float2*>(&P[(row + 8) * Cfg::PPITCH + col]) =
@@ -273,7 +276,8 @@ struct ExpandMap {
   long long plane_stride;             // elements between planes
 };
 
-template <int R, int OB>
+// GEN as for the shrink: token_rows, slot ranks or a bias in use.
+template <int R, int OB, bool GEN>
 __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                const float* __restrict__ u,
                                                                const __grid_constant__ ExpandMap map) {
@@ -307,16 +311,19 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   // Row of y holding each token of the tile (gathered batches map through
   // token_rows); an out-of-range entry skips the tile.
   __shared__ int s_rows[MT];
-  int bad_row = 0;
-  for (int r = threadIdx.x; r < t.rows; r += blockDim.x) {
-    const int yr = p.token_rows ? p.token_rows[t.row0 + r] : t.row0 + r;
-    if (yr < 0 || yr >= p.num_tokens) bad_row = 1;
-    s_rows[r] = yr;
+  if constexpr (GEN) {
+    int bad_row = 0;
+    for (int r = threadIdx.x; r < t.rows; r += blockDim.x) {
+      const int yr = p.token_rows ? p.token_rows[t.row0 + r] : t.row0 + r;
+      if (yr < 0 || yr >= p.num_tokens) bad_row = 1;
+      s_rows[r] = yr;
+    }
+    if (__syncthreads_or(bad_row)) {
+      if (threadIdx.x == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
+      return;
+    }
   }
-  if (__syncthreads_or(bad_row)) {
-    if (threadIdx.x == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
-    return;
-  }
+  auto y_row = [&](int r) -> long long { return GEN ? s_rows[r] : t.row0 + r; };
 
   uint8_t* Ys = smem + Cfg::Y_OFF;
   uint8_t* Bs = smem + Cfg::B_OFF;
@@ -335,12 +342,12 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   for (int c = threadIdx.x; c < t.rows * YW; c += blockDim.x) {
     const int r = c / YW, ch = c % YW;
     if (ch < ych)
-      cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + (long long)s_rows[r] * sl.y_row_stride + o0 + ch * 8);
+      cp_async16(Ys + r * Cfg::YPITCH + ch * 16, yg + y_row(r) * sl.y_row_stride + o0 + ch * 8);
   }
-  const int kmax = slot_kmax(p, t.slot);  // B columns past this are not read
+  const int kmax = GEN ? slot_kmax(p, t.slot) : R;  // B columns past this are not read
   for (int c = threadIdx.x; c < ovalid * BW; c += blockDim.x) {
     const int o = c / BW, ch = c % BW;
-    if (ch * 8 < kmax) cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
+    if (!GEN || ch * 8 < kmax) cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
   }
   cp_async_commit();
 
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
       acc[nt][1] = __high2float(v0);
       acc[nt][2] = __low2float(v1);
       acc[nt][3] = __high2float(v1);
-      if (sl.bias && o0 + col < sl.out_dim) {  // bias joins y before the one rounding
+      if (GEN && sl.bias && o0 + col < sl.out_dim) {  // bias joins y before the one rounding
         const __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(
             static_cast<const __nv_bfloat16*>(sl.bias) + (long long)t.slot * sl.bias_slot_stride + o0 + col);
         acc[nt][0] += __low2float(bv);
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 #pragma unroll
     for (int kk = 0; kk < (2 * R) / 16; ++kk) {
       const int kb = (kk * 16) % R;
-      if (kb >= kmax) continue;  // past the slot's rank (hi and lo halves alike)
+      if (GEN && kb >= kmax) continue;  // past the slot's rank (hi and lo halves alike)
       uint32_t a[4];
       ldsm_x4(hs + (m * 16 + (lane & 15)) * Cfg::UPITCH + (kk * 16 + (lane >> 4) * 8) * 2, a[0], a[1],
               a[2], a[3]);
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   for (int c = threadIdx.x; c < t.rows * YW; c += blockDim.x) {
     const int r = c / YW, ch = c % YW;
     if (ch < ych)
-      *reinterpret_cast<uint4*>(yg + (long long)s_rows[r] * sl.y_row_stride + o0 + ch * 8) =
+      *reinterpret_cast<uint4*>(yg + y_row(r) * sl.y_row_stride + o0 + ch * 8) =
           *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
   }
 }
@@ -490,9 +497,9 @@ int num_sms() {
   return sms[dev];
 }
 
-template <int NB>
+template <int NB, bool GEN>
 cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
-  auto kernel = sgmv_shrink_bf16_kernel<NB>;
+  auto kernel = sgmv_shrink_bf16_kernel<NB, GEN>;
   const int smem = ShrinkCfg<NB>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);
@@ -527,9 +534,9 @@ cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int
   return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride);
 }
 
-template <int R, int OB>
+template <int R, int OB, bool GEN>
 cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
-  auto kernel = sgmv_expand_bf16_kernel<R, OB>;
+  auto kernel = sgmv_expand_bf16_kernel<R, OB, GEN>;
   const int smem = ExpandCfg<R, OB>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);
@@ -593,16 +600,39 @@ int apply_splits(int end, int in_dim, int nR) {
   return C;
 }
 
-static cudaError_t dispatch_shrink(const ProblemDesc& p, float* u, cudaStream_t s, bool partial) {
+// Any of token_rows, slot ranks or a bias selects the general kernels.
+static bool needs_general(const ProblemDesc& p) {
+  if (p.token_rows || p.slot_ranks) return true;
+  for (int j = 0; j < p.n_slices; ++j)
+    if (p.sl[j].bias) return true;
+  return false;
+}
+
+template <bool GEN>
+static cudaError_t dispatch_shrink_g(const ProblemDesc& p, float* u, cudaStream_t s, bool partial) {
   int nblk = 1;
   const int nb = pick_nb(p.n_slices * p.R, &nblk);
   switch (nb) {
-    case 16: return launch_shrink_nb<16>(p, u, s, nblk, partial);
-    case 32: return launch_shrink_nb<32>(p, u, s, nblk, partial);
-    case 48: return launch_shrink_nb<48>(p, u, s, nblk, partial);
-    case 64: return launch_shrink_nb<64>(p, u, s, nblk, partial);
-    case 96: return launch_shrink_nb<96>(p, u, s, nblk, partial);
-    default: return launch_shrink_nb<128>(p, u, s, nblk, partial);
+    case 16: return launch_shrink_nb<16, GEN>(p, u, s, nblk, partial);
+    case 32: return launch_shrink_nb<32, GEN>(p, u, s, nblk, partial);
+    case 48: return launch_shrink_nb<48, GEN>(p, u, s, nblk, partial);
+    case 64: return launch_shrink_nb<64, GEN>(p, u, s, nblk, partial);
+    case 96: return launch_shrink_nb<96, GEN>(p, u, s, nblk, partial);
+    default: return launch_shrink_nb<128, GEN>(p, u, s, nblk, partial);
+  }
+}
+
+static cudaError_t dispatch_shrink(const ProblemDesc& p, float* u, cudaStream_t s, bool partial) {
+  return needs_general(p) ? dispatch_shrink_g<true>(p, u, s, partial) : dispatch_shrink_g<false>(p, u, s, partial);
+}
+
+template <bool GEN>
+static cudaError_t dispatch_expand_g(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
+  switch (p.R) {
+    case 16: return launch_expand_r<16, 256, GEN>(p, u, s, pdl, nsplit);
+    case 32: return launch_expand_r<32, 256, GEN>(p, u, s, pdl, nsplit);
+    case 64: return launch_expand_r<64, 128, GEN>(p, u, s, pdl, nsplit);
+    default: return launch_expand_r<128, 64, GEN>(p, u, s, pdl, nsplit);
   }
 }
 
@@ -615,12 +645,8 @@ cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStrea
 }
 
 cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
-  switch (p.R) {
-    case 16: return launch_expand_r<16, 256>(p, u, s, pdl, nsplit);
-    case 32: return launch_expand_r<32, 256>(p, u, s, pdl, nsplit);
-    case 64: return launch_expand_r<64, 128>(p, u, s, pdl, nsplit);
-    default: return launch_expand_r<128, 64>(p, u, s, pdl, nsplit);
-  }
+  return needs_general(p) ? dispatch_expand_g<true>(p, u, s, pdl, nsplit)
+                          : dispatch_expand_g<false>(p, u, s, pdl, nsplit);
 }
 
 }  // namespace lora

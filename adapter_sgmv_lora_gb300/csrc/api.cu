@@ -95,13 +95,17 @@ size_t plane_bytes(const lora_problem_t* p, int32_t end) {
 }
 
 // lora_sgmv_apply's workspace: its shrink may split the input dimension into
-// up to 8 partial planes (apply_splits), summed by the expand.
+// up to 8 partial planes (apply_splits), summed by the expand; or, on the
+// tensor-core path for ranks 64 and 128, it holds u packed per 128-row tile
+// (at most max_num_loras + end / 128 tiles).
 size_t ws_bytes(const lora_problem_t* p, int32_t end) {
   int splits = apply_splits(end, p->in_dim, p->num_slices * p->max_lora_rank);
   const int tc = tc_shrink_splits(end, p->in_dim);
   if (tc > splits) splits = tc;
-  const size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
-                     (size_t)p->max_lora_rank * 4;
+  size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
+               (size_t)p->max_lora_rank * 4;
+  const size_t packed = tc_packed_bytes(p->max_num_loras, end, p->num_slices, p->max_lora_rank);
+  if (packed > raw) raw = packed;
   return (raw + 255) & ~(size_t)255;
 }
 
@@ -202,15 +206,15 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* u = static_cast<float*>(workspace);
   if (fast_path_ok(d, u)) {
+    if (tc_expand_ok(d)) {
+      const cudaError_t e = launch_tc_apply_packed(d, workspace, s);
+      if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
     if (tc_shrink_ok(d)) {
       const int tcs = tc_shrink_splits(d.end, d.in_dim);
       const cudaError_t e = launch_tc_shrink(d, u, s, tcs);
       if (e != cudaErrorNotSupported) {
         if (e != cudaSuccess) return LORA_ERR_CUDA;
-        if (tc_expand_ok(d)) {
-          const cudaError_t e2 = launch_tc_expand(d, u, s, true, tcs);
-          if (e2 != cudaErrorNotSupported) return cuda_status(e2);
-        }
         return cuda_status(launch_expand_bf16(d, u, s, true, tcs));
       }
     }

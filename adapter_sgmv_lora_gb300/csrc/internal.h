@@ -76,5 +76,12 @@ cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int
 // tcgen05 expand for long groups with R = 64 or 128 (sums nsplit planes of u).
 bool tc_expand_ok(const ProblemDesc& p);
 cudaError_t launch_tc_expand(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit);
+// The apply on tensor cores when tc_expand_ok: the shrink writes u packed as
+// the expand's bf16 hi|lo operand image per (128-row tile, slice) into the
+// workspace (tc_packed_bytes(S, end, n, R) bytes; 0 unless R is 64 or 128)
+// and the expand copies it in whole.  Returns cudaErrorNotSupported, having
+// launched nothing, when the tensor maps cannot be encoded.
+size_t tc_packed_bytes(int S, int end, int n_slices, int R);
+cudaError_t launch_tc_apply_packed(const ProblemDesc& p, void* workspace, cudaStream_t s);
 
 }  // namespace lora

@@ -49,6 +49,35 @@ struct TcCfg {
   static constexpr uint32_t TMEM_COLS = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : NR <= 256 ? 256 : 512;
 };
 
+// Byte offset of bf16 element (row r, k) in a K-major operand made of
+// [128 rows x 64] blocks with the 128-byte swizzle (16-byte chunk c of row r
+// stored at chunk c ^ (r % 8)).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
+  const int kb = k >> 6, kk = k & 63;
+  return (uint32_t)(kb * TM * 128 + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + ((kk & 7) << 1));
+}
+
+// Packed u: for every (tile, slice) the expand's A operand as it sits in
+// shared memory, 2R/64 swizzled [128 rows x 64] bf16 blocks holding u's hi
+// part (k < R) and lo part (k >= R), u = hi + lo to 16 significant bits.
+// Row r's 16 values k0 .. k0+15 of one slice go to `blk` (that slice's image).
+__device__ __forceinline__ void pack_u16(uint8_t* blk, int R, int r, int k0, const float* v) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = v[8 * h + 2 * e], b = v[8 * h + 2 * e + 1];
+      const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+      hi[e] = pack_bf16x2(ha, hb);
+      lo[e] = pack_bf16x2(__float2bfloat16_rn(a - __bfloat162float(ha)), __float2bfloat16_rn(b - __bfloat162float(hb)));
+    }
+    const int k = k0 + 8 * h;
+    *reinterpret_cast<uint4*>(blk + sw128_offset(r, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(blk + sw128_offset(r, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
 }  // namespace
 
 struct TcMaps {
@@ -58,11 +87,16 @@ struct TcMaps {
   CUtensorMap a16[LORA_MAX_SLICES];  // same tensor, box 64 x 16 x 1
 };
 
-template <int NR>
+// grid.x = tiles * nsn * nsplit.  CTA (tile, column part cn, K split ks)
+// computes columns [cn * NR, +NR) of u (n*R columns in all) over input range
+// ks of nsplit.  Output: fp32 plane ks of u (plane_stride apart), or, with
+// PACK (nsplit == 1), packed u (see pack_u16) at upk, tile-major.
+template <int NR, bool PACK>
 __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __grid_constant__ ProblemDesc p,
                                                                     const __grid_constant__ TcMaps maps,
                                                                     float* __restrict__ u, int nsplit,
-                                                                    long long plane_stride) {
+                                                                    long long plane_stride, int nsn,
+                                                                    uint8_t* __restrict__ upk) {
   using Cfg = TcCfg<NR>;
   constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
@@ -80,7 +114,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = (int)(blockIdx.x % (unsigned)nsplit);
-  const long long tile = blockIdx.x / (unsigned)nsplit;
+  const int cn = (int)((blockIdx.x / (unsigned)nsplit) % (unsigned)nsn);
+  const long long tile = blockIdx.x / (unsigned)(nsplit * nsn);
+  const int n_base = cn * NR;  // first u column of this CTA
   if (warp == 0) {
     Tile t{};
     const bool ok = warp_locate_tile(p, TM, tile, t);
@@ -120,6 +156,11 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
     // ---- producer (x streams through L2 once; the slot's A rows are re-read
     // by every tile of the group, so they are kept)
     const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+    uint32_t a_bytes = Cfg::X_BYTES;
+    for (int j = 0; j < p.n_slices; ++j) {
+      const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+      if (khi > klo) a_bytes += (uint32_t)((khi - klo) * TK * 2);
+    }
     for (int s = 0; s < nst; ++s) {
       const int slot = s % NSTAGE;
       if (s >= NSTAGE && !mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1))) {
@@ -128,18 +169,22 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
       }
       uint8_t* xs = smem + slot * Cfg::STAGE;
       uint8_t* as = xs + Cfg::X_BYTES;
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::X_BYTES + p.n_slices * kmax * TK * 2));
+      mbar_arrive_expect_tx(&full[slot], a_bytes);
       const int kk = k0 + s * TK;
       tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
       for (int j = 0; j < p.n_slices; ++j) {
-        if (kmax == R) {  // one box per slice (few large TMA requests)
-          tma_load_3d_hint(as + j * R * TK * 2, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
-        } else {  // below full rank: 64-row boxes, then 16-row boxes, up to the rank only
-          int kb = 0;
-          for (; kb + 64 <= kmax; kb += 64)
-            tma_load_3d_hint(as + (j * R + kb) * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
-          for (; kb < kmax; kb += 16)
-            tma_load_3d_hint(as + (j * R + kb) * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
+        // Rows [klo, khi) of slice j fall in this CTA's columns (and the rank).
+        const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+        if (khi <= klo) continue;
+        uint8_t* dst = as + (j * R - n_base) * TK * 2;
+        if (klo == 0 && khi == R) {  // one box per slice (few large TMA requests)
+          tma_load_3d_hint(dst, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
+        } else {  // 64-row boxes, then 16-row boxes
+          int kb = klo;
+          for (; kb + 64 <= khi; kb += 64)
+            tma_load_3d_hint(dst + kb * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
+          for (; kb < khi; kb += 16)
+            tma_load_3d_hint(dst + kb * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
         }
       }
     }
@@ -174,16 +219,23 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int nR = p.n_slices * R;
-    float* up = u + split * plane_stride + (long long)(t.row0 + row) * nR;
+    const bool live = row < t.rows;
+    const int uimg = 4 * R * TM;  // bytes of one (tile, slice) packed image
     if (!got) {
       atomicOr(&s_fail, 1);
     } else {
-      for (int c = 0; c < nR; c += 16) {
+      float* up = u + split * plane_stride + (long long)(t.row0 + row) * nR + n_base;
+      for (int c = 0; c < NR; c += 16) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
-        if (row < t.rows) {
-          // Columns past the slot's rank came from rows never loaded: 0.
-          const bool keep = (c % R) < kmax;
+        // Columns past the slot's rank came from rows never loaded: 0.
+        const int col = n_base + c, j = col / R, k = col - j * R;
+        const bool keep = k < kmax;
+        if (PACK) {  // rows past the group: zeros
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = (keep && live) ? v[e] : 0.f;
+          pack_u16(upk + ((long long)tile * p.n_slices + j) * uimg, R, row, k, v);
+        } else if (live) {
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
             *reinterpret_cast<float4*>(up + c + i) =
@@ -260,9 +312,10 @@ bool encode_maps(const ProblemDesc& p, TcMaps* m) {
   return true;
 }
 
-template <int NR>
-cudaError_t launch_tc_t(const ProblemDesc& p, const TcMaps& maps, float* u, cudaStream_t s, int nsplit) {
-  auto kernel = sgmv_tc_shrink_kernel<NR>;
+template <int NR, bool PACK>
+cudaError_t launch_tc_t(const ProblemDesc& p, const TcMaps& maps, float* u, cudaStream_t s, int nsplit, int nsn,
+                        uint8_t* upk) {
+  auto kernel = sgmv_tc_shrink_kernel<NR, PACK>;
   static unsigned long long done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -278,11 +331,18 @@ cudaError_t launch_tc_t(const ProblemDesc& p, const TcMaps& maps, float* u, cuda
   const long long tiles = (long long)p.G + p.end / TM;
   const long long plane_stride = nsplit > 1 ? (long long)p.end * p.n_slices * p.R : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * nsplit));
+  cfg.gridDim = dim3((unsigned)(tiles * nsplit * nsn));
   cfg.blockDim = dim3(TTHREADS);
   cfg.dynamicSmemBytes = TcCfg<NR>::SMEM;
   cfg.stream = s;
-  return cudaLaunchKernelEx(&cfg, kernel, p, maps, u, nsplit, plane_stride);
+  return cudaLaunchKernelEx(&cfg, kernel, p, maps, u, nsplit, plane_stride, nsn, upk);
+}
+
+template <int NR>
+cudaError_t launch_tc_nr(const ProblemDesc& p, const TcMaps& maps, float* u, cudaStream_t s, int nsplit, int nsn,
+                         uint8_t* upk) {
+  return upk ? launch_tc_t<NR, true>(p, maps, u, s, nsplit, nsn, upk)
+             : launch_tc_t<NR, false>(p, maps, u, s, nsplit, nsn, nullptr);
 }
 
 }  // namespace
@@ -309,21 +369,31 @@ bool tc_shrink_ok(const ProblemDesc& p) {
   return p.G > 0 && p.end >= 96LL * p.G;
 }
 
+namespace {
+
+// N (columns per CTA) = n*R / nsn.
+cudaError_t launch_tc_shrink_maps(const ProblemDesc& p, const TcMaps& maps, float* u, cudaStream_t s, int nsplit,
+                                  int nsn, uint8_t* upk) {
+  switch (p.n_slices * p.R / nsn) {
+    case 16: return launch_tc_nr<16>(p, maps, u, s, nsplit, nsn, upk);
+    case 32: return launch_tc_nr<32>(p, maps, u, s, nsplit, nsn, upk);
+    case 48: return launch_tc_nr<48>(p, maps, u, s, nsplit, nsn, upk);
+    case 64: return launch_tc_nr<64>(p, maps, u, s, nsplit, nsn, upk);
+    case 96: return launch_tc_nr<96>(p, maps, u, s, nsplit, nsn, upk);
+    case 128: return launch_tc_nr<128>(p, maps, u, s, nsplit, nsn, upk);
+    case 192: return launch_tc_nr<192>(p, maps, u, s, nsplit, nsn, upk);
+    case 256: return launch_tc_nr<256>(p, maps, u, s, nsplit, nsn, upk);
+    case 384: return launch_tc_nr<384>(p, maps, u, s, nsplit, nsn, upk);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
 cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int nsplit) {
   TcMaps maps;
   if (!encode_maps(p, &maps)) return cudaErrorNotSupported;
-  switch (p.n_slices * p.R) {
-    case 16: return launch_tc_t<16>(p, maps, u, s, nsplit);
-    case 32: return launch_tc_t<32>(p, maps, u, s, nsplit);
-    case 48: return launch_tc_t<48>(p, maps, u, s, nsplit);
-    case 64: return launch_tc_t<64>(p, maps, u, s, nsplit);
-    case 96: return launch_tc_t<96>(p, maps, u, s, nsplit);
-    case 128: return launch_tc_t<128>(p, maps, u, s, nsplit);
-    case 192: return launch_tc_t<192>(p, maps, u, s, nsplit);
-    case 256: return launch_tc_t<256>(p, maps, u, s, nsplit);
-    case 384: return launch_tc_t<384>(p, maps, u, s, nsplit);
-  }
-  return cudaErrorNotSupported;
+  return launch_tc_shrink_maps(p, maps, u, s, nsplit, 1, nullptr);
 }
 
 }  // namespace lora
@@ -331,40 +401,65 @@ cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int
 // ===========================================================================
 // Expand on tcgen05 for long groups (R = 64 or 128):
 //   y_j[t, o] = rn(y_j[t, o] + sum_k B_j[s, o, k] u[t, j*R+k])
-// One CTA per (128-row tile, slice j, chunk of up to 8 output blocks of 128
-// columns).  Warps 2-5 first sum the u planes of their row and write u as
-// bf16 hi | lo (K = 2R) straight into the 128-byte-swizzled K-major layout
-// the MMA reads; warp 0 streams each block's y (two 64-column boxes) and B
-// (R/64 boxes of 128 rows) through two smem slots with TMA; warp 1 issues
-// tcgen05.mma M=128 N=128 K=2R into one of two TMEM buffers; warps 2-5 add
-// the TMEM delta to the swizzled y block, round once and store the routed
-// rows (16-byte stores; rows past the group are never written).
+// Persistent: one CTA per SM.  The work is the list of units (128-row tile,
+// slice j, output block of 128 columns), tile-major; CTA c takes the c-th of
+// gridDim.x equal contiguous ranges, so no SM idles through a partial last
+// wave and the pipeline runs across unit boundaries.  Consecutive units of
+// one (tile, slice) form a segment sharing the A operand u.  Warp 0 streams
+// each unit's y (two 64-column boxes) and B (R/64 boxes of 128 rows) through
+// NSLOT smem slots with TMA; warp 1 issues tcgen05.mma M=128 N=128 K=2R into
+// one of two TMEM buffers; warps 2-5 sum the u planes of a segment into the
+// u buffer as bf16 hi | lo (K = 2R, 128-byte-swizzled K-major, one row per
+// thread), then add the TMEM delta of each unit to its swizzled y block,
+// round once and store the routed rows (16-byte stores; rows past the group
+// are never written).  With two u buffers (R = 64) the next segment's u is
+// loaded while the current one is multiplied.
 // ===========================================================================
 namespace lora {
 
 namespace {
 
-constexpr int XB = 128;     // output columns per block (MMA N)
-constexpr int XCHUNK = 8;   // blocks per CTA (1024 columns)
+constexpr int XB = 128;         // output columns per unit (MMA N)
+constexpr int RC_MAX_G = 256;   // groups cached in shared memory
 
 template <int R>
 struct TxCfg {
-  static constexpr int KB = 2 * R / 64;               // 64-wide K blocks of the hi|lo operand
-  static constexpr int U_BYTES = KB * TM * 128;       // A operand (u hi|lo)
+  static constexpr int KB = 2 * R / 64;                 // 64-wide K blocks of the hi|lo operand
+  static constexpr int U_BYTES = KB * TM * 128;         // A operand (u hi|lo) of one segment
   static constexpr int Y_BYTES = (XB / 64) * TM * 128;  // 64-column y boxes
   static constexpr int B_BYTES = (R / 64) * XB * 128;   // R/64 boxes of XB rows x 64
   static constexpr int SLOT = Y_BYTES + B_BYTES;
-  static constexpr int NSLOT = (U_BYTES + 3 * SLOT + 1024 <= 220 * 1024) ? 3 : 2;  // y/B pipeline depth
-  static constexpr int SMEM = U_BYTES + NSLOT * SLOT + 1024;
+  static constexpr int BUDGET = 212 * 1024;             // dynamic smem (static arrays use the rest)
+  static constexpr int NUB = (2 * U_BYTES + 3 * SLOT + 1024 <= BUDGET) ? 2 : 1;   // u buffers
+  static constexpr int NSLOT = (NUB * U_BYTES + 3 * SLOT + 1024 <= BUDGET) ? 3 : 2;  // y/B depth
+  static constexpr int SMEM = NUB * U_BYTES + NSLOT * SLOT + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * XB;
+  static_assert(SMEM <= BUDGET, "expand pipeline exceeds shared memory");
 };
 
-// Byte offset of bf16 element (row r, k) in a K-major operand made of
-// [128 rows x 64] blocks with the 128-byte swizzle (16-byte chunk c of row r
-// stored at chunk c ^ (r % 8)).
-__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
-  const int kb = k >> 6, kk = k & 63;
-  return (uint32_t)(kb * TM * 128 + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + ((kk & 7) << 1));
+// The routing triple as cached in shared memory: group g's rows
+// [offs[g], offs[g+1]), slot ids[g], first tile tstart[g] (tstart[G] = tiles).
+struct RouteCache {
+  int offs[RC_MAX_G + 1];
+  int ids[RC_MAX_G];
+  int tstart[RC_MAX_G + 1];
+};
+
+// Tile `tile` (< tstart[G]) of the cached routing: the last group whose first
+// tile is <= tile, which is never an empty group.
+__device__ __forceinline__ Tile rc_tile(const RouteCache& rc, int G, int tile) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rc.tstart[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile t;
+  t.g = lo;
+  t.slot = rc.ids[lo];
+  t.row0 = rc.offs[lo] + (tile - rc.tstart[lo]) * TM;
+  t.rows = min(TM, rc.offs[lo + 1] - t.row0);
+  return t;
 }
 
 }  // namespace
@@ -375,45 +470,82 @@ struct TxMaps {
 };
 
 struct TxWork {
-  int n_chunks;                          // chunks per tile, all slices
-  int chunk_begin[LORA_MAX_SLICES + 1];  // first chunk of each slice
-  int nsplit;                            // partial planes of u
+  int nbt;                             // output blocks per tile, all slices
+  int blk_begin[LORA_MAX_SLICES + 1];  // first block of each slice
+  int nsplit;                          // partial planes of u
   long long plane_stride;
 };
 
-template <int R>
+// Unit -> (tile, slice, first output column).
+struct Unit {
+  int tile, j, o0;
+};
+__device__ __forceinline__ Unit tx_unit(const TxWork& w, int n_slices, long long un) {
+  Unit x;
+  x.tile = (int)(un / w.nbt);
+  const int b = (int)(un - (long long)x.tile * w.nbt);
+  x.j = 0;
+  if (n_slices > 1 && b >= w.blk_begin[1]) x.j = 1;
+  if (n_slices > 2 && b >= w.blk_begin[2]) x.j = 2;
+  x.o0 = (b - (x.j == 0 ? 0 : (x.j == 1 ? w.blk_begin[1] : w.blk_begin[2]))) * XB;
+  return x;
+}
+
+// PACKED: u arrives packed (the tcgen05 shrink's image per (tile, slice),
+// see pack_u16) and warp 0 copies each segment's image into its u buffer;
+// otherwise u is fp32 [end, n*R] (nsplit planes) and the epilogue warps
+// convert it.
+template <int R, bool PACKED>
 __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __grid_constant__ ProblemDesc p,
                                                                     const __grid_constant__ TxMaps maps,
                                                                     const __grid_constant__ TxWork w,
-                                                                    const float* __restrict__ u) {
+                                                                    const float* __restrict__ u,
+                                                                    const uint8_t* __restrict__ upk) {
   using Cfg = TxCfg<R>;
-  constexpr int NSLOT = Cfg::NSLOT;
+  constexpr int NSLOT = Cfg::NSLOT, NUB = Cfg::NUB;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], tfull[2], tempty[2], uready;
+  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], tfull[2], tempty[2], uready[NUB], ufree[NUB];
   __shared__ uint32_t s_tmem;
-  __shared__ Tile s_tile;
-  __shared__ int s_ok, s_fail, s_kmax;
+  __shared__ RouteCache rc;
+  __shared__ int s_ok, s_fail;
+  __shared__ long long s_u0, s_u1;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Ua = smem;
+  uint8_t* slots = smem + NUB * Cfg::U_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long tile = blockIdx.x / (unsigned)w.n_chunks;
-  const int cg = (int)(blockIdx.x % (unsigned)w.n_chunks);
-  int j = 0;
-  while (j + 1 < p.n_slices && cg >= w.chunk_begin[j + 1]) ++j;
-  const SliceDesc& sl = p.sl[j];
-  const int b_first = (cg - w.chunk_begin[j]) * XCHUNK;
-  const int nblocks_slice = (sl.out_dim + XB - 1) / XB;
-  const int nblk = min(XCHUNK, nblocks_slice - b_first);
+  const int G = p.G;
 
   if (warp == 0) {
-    Tile t{};
-    const bool ok = warp_locate_tile(p, TM, tile, t);
+    // Validate the triple, cache it and number the tiles group by group.
+    const bool valid = warp_check_routing(p);
+    int base = 0;
+    for (int c = 0; valid && c < G; c += 32) {
+      const int g = c + lane;
+      int nt = 0;
+      if (g < G) {
+        const int o0 = p.offs[g], o1 = p.offs[g + 1];
+        rc.offs[g] = o0;
+        rc.ids[g] = p.lora_ids[g];
+        nt = (o1 - o0 + TM - 1) / TM;
+      }
+      int incl = nt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      if (g < G) rc.tstart[g] = base + incl - nt;
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
     if (lane == 0) {
-      s_tile = t;
-      s_ok = ok;
+      rc.offs[G] = p.end;
+      rc.tstart[G] = base;
+      // This CTA's contiguous share of the unit list.
+      const long long units = valid ? (long long)base * w.nbt : 0;
+      s_u0 = units * blockIdx.x / gridDim.x;
+      s_u1 = units * (blockIdx.x + 1) / gridDim.x;
+      s_ok = valid;
       s_fail = 0;
-      s_kmax = ok ? slot_kmax(p, t.slot) : 0;
       for (int i = 0; i < NSLOT; ++i) {
         mbar_init(&full[i], 1);
         mbar_init(&empty[i], 4);
@@ -422,7 +554,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         mbar_init(&tfull[i], 1);
         mbar_init(&tempty[i], 4);
       }
-      mbar_init(&uready, 4 * 32);
+      for (int i = 0; i < NUB; ++i) {
+        mbar_init(&uready[i], PACKED ? 1 : 4 * 32);
+        mbar_init(&ufree[i], 1);
+      }
       fence_mbar_init();
     }
   }
@@ -434,36 +569,80 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = s_tmem;
-  const Tile t = s_tile;
   const bool ok = s_ok != 0;
-  const int kmax = s_kmax;  // rank columns past this: no B boxes, no MMA steps
-  const int nbbox = (kmax + 63) / 64;
+  const long long u0 = s_u0, u1 = s_u1;
 
   if (ok && warp == 0 && lane == 0) {
-    // ---- producer: y and B of block i into slot i % 2 (independent of the
-    // shrink, so it starts before the dependency wait).
+    // ---- producer: y and B of unit i into slot i % NSLOT (independent of
+    // the shrink, so the first slots are filled before the dependency wait);
+    // with PACKED also each segment's u image into buffer seg % NUB.
     const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
-    for (int i = 0; i < nblk; ++i) {
-      const int slot = i % NSLOT;
-      if (i >= NSLOT && !mbar_wait(&empty[slot], (uint32_t)(((i / NSLOT) - 1) & 1))) {
-        atomicOr(&s_fail, 1);
-        break;
+    int cur = -1, nbbox = 0;
+    Tile t{};
+    auto issue_yb = [&](int i, const Unit& x) {
+      if (x.tile != cur) {
+        cur = x.tile;
+        t = rc_tile(rc, G, x.tile);
+        nbbox = (slot_kmax(p, t.slot) + 63) / 64;
       }
-      uint8_t* ys = smem + Cfg::U_BYTES + slot * Cfg::SLOT;
+      const int slot = i % NSLOT;
+      uint8_t* ys = slots + slot * Cfg::SLOT;
       uint8_t* bs = ys + Cfg::Y_BYTES;
-      const int o0 = (b_first + i) * XB;
       mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + nbbox * XB * 128));
       for (int yb = 0; yb < XB / 64; ++yb)
-        tma_load_2d_hint(ys + yb * TM * 128, &maps.y[j], o0 + yb * 64, t.row0, &full[slot], pol_stream);
+        tma_load_2d_hint(ys + yb * TM * 128, &maps.y[x.j], x.o0 + yb * 64, t.row0, &full[slot], pol_stream);
       for (int kb = 0; kb < nbbox; ++kb)
-        tma_load_3d_hint(bs + kb * XB * 128, &maps.b[j], kb * 64, o0, t.slot, &full[slot], pol_keep);
+        tma_load_3d_hint(bs + kb * XB * 128, &maps.b[x.j], kb * 64, x.o0, t.slot, &full[slot], pol_keep);
+    };
+    const int pre = (int)min((long long)NSLOT, u1 - u0);  // slots free at the start
+    if (PACKED) {
+      for (int i = 0; i < pre; ++i) issue_yb(i, tx_unit(w, p.n_slices, u0 + i));
+      pdl_wait();  // the packed u comes from the shrink grid
+    }
+    int seg = -1, seg_tile = -1, seg_j = -1;
+    int i = 0;
+    for (long long un = u0; un < u1; ++un, ++i) {
+      const Unit x = tx_unit(w, p.n_slices, un);
+      if (!PACKED || i >= pre) {
+        if (i >= NSLOT && !mbar_wait(&empty[i % NSLOT], (uint32_t)(((i / NSLOT) - 1) & 1))) {
+          atomicOr(&s_fail, 1);
+          break;
+        }
+        issue_yb(i, x);
+      }
+      if (PACKED && (x.tile != seg_tile || x.j != seg_j)) {
+        seg_tile = x.tile;
+        seg_j = x.j;
+        ++seg;
+        const int ub = seg % NUB;
+        // The buffer's previous segment must be fully multiplied.
+        if (seg >= NUB && !mbar_wait(&ufree[ub], (uint32_t)(((seg / NUB) - 1) & 1))) {
+          atomicOr(&s_fail, 1);
+          break;
+        }
+        const uint8_t* src = upk + ((long long)x.tile * p.n_slices + x.j) * Cfg::U_BYTES;
+        mbar_arrive_expect_tx(&uready[ub], (uint32_t)Cfg::U_BYTES);
+        for (int kb = 0; kb < Cfg::KB; ++kb)
+          bulk_g2s(smem + ub * Cfg::U_BYTES + kb * TM * 128, src + kb * TM * 128, TM * 128, &uready[ub]);
+      }
     }
   } else if (ok && warp == 1 && lane == 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(TM, XB);
-    const bool ready = mbar_wait(&uready, 0);
-    if (!ready) atomicOr(&s_fail, 1);
-    for (int i = 0; ready && i < nblk; ++i) {
+    int cur_tile = -1, cur_j = -1, seg = -1, kmax = 0;
+    int i = 0;
+    for (long long un = u0; un < u1; ++un, ++i) {
+      const Unit x = tx_unit(w, p.n_slices, un);
+      if (x.tile != cur_tile || x.j != cur_j) {  // new segment: wait for its u
+        cur_tile = x.tile;
+        cur_j = x.j;
+        ++seg;
+        kmax = slot_kmax(p, rc_tile(rc, G, x.tile).slot);
+        if (!mbar_wait(&uready[seg % NUB], (uint32_t)((seg / NUB) & 1))) {
+          atomicOr(&s_fail, 1);
+          break;
+        }
+      }
       const int slot = i % NSLOT, buf = i & 1;
       if (!mbar_wait(&full[slot], (uint32_t)((i / NSLOT) & 1)) ||
           (i >= 2 && !mbar_wait(&tempty[buf], (uint32_t)(((i >> 1) - 1) & 1)))) {
@@ -471,8 +650,8 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         break;
       }
       tc_fence_after_sync();
-      const uint32_t ua = smem_addr(Ua);
-      const uint32_t bs = smem_addr(smem + Cfg::U_BYTES + slot * Cfg::SLOT + Cfg::Y_BYTES);
+      const uint32_t ua = smem_addr(smem + (seg % NUB) * Cfg::U_BYTES);
+      const uint32_t bs = smem_addr(slots + slot * Cfg::SLOT + Cfg::Y_BYTES);
       uint32_t acc = 0;
 #pragma unroll
       for (int ks = 0; ks < 2 * R / 16; ++ks) {
@@ -484,6 +663,11 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         acc = 1;
       }
       tc_commit(&tfull[buf]);
+      if (PACKED) {  // last unit of the segment: its u buffer is free once these MMAs finish
+        const long long seg_end = x.j + 1 < p.n_slices ? (long long)x.tile * w.nbt + w.blk_begin[x.j + 1]
+                                                       : (long long)(x.tile + 1) * w.nbt;
+        if (un + 1 == min(seg_end, u1)) tc_commit(&ufree[seg % NUB]);
+      }
     }
   } else if (warp >= 2) {
     // ---- epilogue warps: thread = one tile row = one TMEM lane
@@ -491,57 +675,85 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
     const int row = q * 32 + lane;
     const int nR = p.n_slices * R;
     if (ok) {
-      pdl_wait();  // u comes from the shrink grid
-      // u row (sum of planes, plane order) -> bf16 hi | lo, swizzled K-major.
-      const bool live = row < t.rows;
-      const float* ur = u + (long long)(t.row0 + (live ? row : 0)) * nR + (long long)j * R;
-      // 32 columns per batch: all loads of a batch (every plane) are issued
-      // before any is consumed, so a batch costs one L2 round trip.
-      for (int k0 = 0; k0 < R; k0 += 32) {
-        float4 a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          a[i] = live ? __ldcg(reinterpret_cast<const float4*>(ur + k0 + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp = 1; sp < w.nsplit; ++sp) {
-          float4 b[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            b[i] = live ? __ldcg(reinterpret_cast<const float4*>(ur + sp * w.plane_stride + k0 + 4 * i))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            a[i].x += b[i].x;
-            a[i].y += b[i].y;
-            a[i].z += b[i].z;
-            a[i].w += b[i].w;
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 8 columns -> one 16-byte hi chunk and one lo chunk
-          const float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w,
-                              a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z, a[2 * c + 1].w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-            hi[i] = pack_bf16x2(h0, h1);
-            lo[i] = pack_bf16x2(__float2bfloat16_rn(v[2 * i] - __bfloat162float(h0)),
-                                __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1)));
-          }
-          const int k = k0 + 8 * c;
-          *reinterpret_cast<uint4*>(Ua + sw128_offset(row, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(Ua + sw128_offset(row, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      }
-      fence_proxy_async_smem();  // generic writes -> visible to the tensor cores
-      mbar_arrive(&uready);
-
-      __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(sl.y) + (long long)(t.row0 + row) * sl.y_row_stride;
-      const uint64_t pol_stream = policy_evict_first();
+      if (!PACKED) pdl_wait();  // u comes from the shrink grid
       // A warp whose wait expired keeps walking the barrier protocol (doing
-      // no work) so the other epilogue warps never block on it.
+      // no work) so the other roles never block on it.
       bool bad = false;
-      for (int i = 0; i < nblk; ++i) {
+      // Segment s's u (sum of planes, plane order) -> bf16 hi | lo in buffer
+      // s % NUB; every epilogue thread arrives on uready once the rows are in.
+      auto load_u = [&](int s, const Tile& ts, int js) {
+        uint8_t* Ub = smem + (s % NUB) * Cfg::U_BYTES;
+        const bool live = !bad && row < ts.rows;
+        const float* ur = u + (long long)(ts.row0 + (live ? row : 0)) * nR + (long long)js * R;
+        // 32 columns per batch: all loads of a batch (every plane) are issued
+        // before any is consumed, so a batch costs one L2 round trip.
+        for (int k0 = 0; k0 < R; k0 += 32) {
+          float4 a[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            a[e] = live ? __ldcg(reinterpret_cast<const float4*>(ur + k0 + 4 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 1; live && sp < w.nsplit; ++sp) {
+            float4 b[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) b[e] = __ldcg(reinterpret_cast<const float4*>(ur + sp * w.plane_stride + k0 + 4 * e));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              a[e].x += b[e].x;
+              a[e].y += b[e].y;
+              a[e].z += b[e].z;
+              a[e].w += b[e].w;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 8 columns -> one 16-byte hi chunk and one lo chunk
+            const float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w,
+                                a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z, a[2 * c + 1].w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+              hi[e] = pack_bf16x2(h0, h1);
+              lo[e] = pack_bf16x2(__float2bfloat16_rn(v[2 * e] - __bfloat162float(h0)),
+                                  __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1)));
+            }
+            const int k = k0 + 8 * c;
+            *reinterpret_cast<uint4*>(Ub + sw128_offset(row, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(Ub + sw128_offset(row, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        fence_proxy_async_smem();  // generic writes -> visible to the tensor cores
+        mbar_arrive(&uready[s % NUB]);
+      };
+
+      const uint64_t pol_stream = policy_evict_first();
+      int cur_tile = -1, cur_j = -1, seg = -1, kmax = 0;
+      Tile t{};
+      int i = 0;
+      for (long long un = u0; un < u1; ++un, ++i) {
+        const Unit x = tx_unit(w, p.n_slices, un);
+        if (x.tile != cur_tile || x.j != cur_j) {
+          // New segment.  Every MMA of the previous segment has completed
+          // (its TMEM results were all consumed), so the u buffer it read is
+          // free: fill this segment's buffer if it was not prefetched, then
+          // prefetch the next segment's into the freed one.
+          if (x.tile != cur_tile) t = rc_tile(rc, G, x.tile);
+          cur_tile = x.tile;
+          cur_j = x.j;
+          ++seg;
+          kmax = slot_kmax(p, t.slot);
+          if (!PACKED && (NUB == 1 || seg == 0)) load_u(seg, t, x.j);
+          if (!PACKED && NUB == 2) {
+            const long long next = x.j + 1 < p.n_slices ? (long long)x.tile * w.nbt + w.blk_begin[x.j + 1]
+                                                        : (long long)(x.tile + 1) * w.nbt;
+            if (next < u1) {
+              const Unit nx = tx_unit(w, p.n_slices, next);
+              load_u(seg + 1, nx.tile == x.tile ? t : rc_tile(rc, G, nx.tile), nx.j);
+            }
+          }
+        }
+        const SliceDesc& sl = p.sl[x.j];
+        const bool live = row < t.rows;
+        __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(sl.y) + (long long)(t.row0 + (live ? row : 0)) * sl.y_row_stride;
         const int slot = i % NSLOT, buf = i & 1;
         if (!bad && !mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
           atomicOr(&s_fail, 1);
@@ -549,16 +761,16 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         }
         bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below needs the whole warp
         tc_fence_after_sync();
-        const uint8_t* ys = smem + Cfg::U_BYTES + slot * Cfg::SLOT;
-        const int o0 = (b_first + i) * XB;
+        const uint8_t* ys = slots + slot * Cfg::SLOT;
+        const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
         for (int c16 = 0; !bad && c16 < XB / 16; ++c16) {
           float d[16];
           if (kmax > 0) {
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
-          } else {  // rank 0: no MMA was issued for this block, the delta is zero
+          } else {  // rank 0: no MMA was issued for this unit, the delta is zero
 #pragma unroll
-            for (int i = 0; i < 16; ++i) d[i] = 0.f;
+            for (int e = 0; e < 16; ++e) d[e] = 0.f;
           }
           if (sl.bias && c16 * 16 < ovalid) {  // bias joins the delta before the one rounding
             const uint4* bp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(sl.bias) +
@@ -644,10 +856,10 @@ bool encode_tx_maps(const ProblemDesc& p, TxMaps* m) {
   return true;
 }
 
-template <int R>
+template <int R, bool PACKED>
 cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& w, const float* u,
-                        cudaStream_t s, bool pdl) {
-  auto kernel = sgmv_tc_expand_kernel<R>;
+                        const uint8_t* upk, cudaStream_t s, bool pdl) {
+  auto kernel = sgmv_tc_expand_kernel<R, PACKED>;
   static unsigned long long done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -660,9 +872,13 @@ cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& 
       done |= 1ull << (dev & 63);
     }
   }
-  const long long tiles = (long long)p.G + p.end / TM;
+  // Persistent: one CTA per SM, or fewer when there are fewer units.
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units_max = ((long long)p.G + p.end / TM) * w.nbt;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * w.n_chunks));
+  cfg.gridDim = dim3((unsigned)std::max(1LL, std::min<long long>(sms, units_max)));
   cfg.blockDim = dim3(TTHREADS);
   cfg.dynamicSmemBytes = TxCfg<R>::SMEM;
   cfg.stream = s;
@@ -673,30 +889,72 @@ cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, p, maps, w, u);
+  return cudaLaunchKernelEx(&cfg, kernel, p, maps, w, u, upk);
+}
+
+TxWork make_tx_work(const ProblemDesc& p, int nsplit) {
+  TxWork w{};
+  int acc = 0;
+  for (int j = 0; j < p.n_slices; ++j) {
+    w.blk_begin[j] = acc;
+    acc += (p.sl[j].out_dim + XB - 1) / XB;
+  }
+  w.blk_begin[p.n_slices] = acc;
+  w.nbt = acc;
+  w.nsplit = nsplit;
+  w.plane_stride = (long long)p.end * p.n_slices * p.R;
+  return w;
+}
+
+bool nr_supported(int n) {
+  switch (n) {
+    case 16: case 32: case 48: case 64: case 96: case 128: case 192: case 256: case 384: return true;
+  }
+  return false;
 }
 
 }  // namespace
 
 bool tc_expand_ok(const ProblemDesc& p) {
-  return (p.R == 64 || p.R == 128) && tc_shrink_ok(p);
+  return (p.R == 64 || p.R == 128) && p.G <= RC_MAX_G && tc_shrink_ok(p);
 }
 
 cudaError_t launch_tc_expand(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
   TxMaps maps;
   if (!encode_tx_maps(p, &maps)) return cudaErrorNotSupported;
-  TxWork w{};
-  int acc = 0;
-  for (int j = 0; j < p.n_slices; ++j) {
-    w.chunk_begin[j] = acc;
-    acc += ((p.sl[j].out_dim + XB - 1) / XB + XCHUNK - 1) / XCHUNK;
-  }
-  w.chunk_begin[p.n_slices] = acc;
-  w.n_chunks = acc;
-  w.nsplit = nsplit;
-  w.plane_stride = (long long)p.end * p.n_slices * p.R;
-  if (p.R == 64) return launch_tx_t<64>(p, maps, w, u, s, pdl);
-  return launch_tx_t<128>(p, maps, w, u, s, pdl);
+  const TxWork w = make_tx_work(p, nsplit);
+  if (p.R == 64) return launch_tx_t<64, false>(p, maps, w, u, nullptr, s, pdl);
+  return launch_tx_t<128, false>(p, maps, w, u, nullptr, s, pdl);
+}
+
+size_t tc_packed_bytes(int S, int end, int n_slices, int R) {
+  if (R != 64 && R != 128) return 0;
+  const long long tiles = (long long)S + (end > 0 ? end : 0) / TM;
+  return (size_t)tiles * n_slices * 4 * R * TM;
+}
+
+int tc_pack_splits(const ProblemDesc& p) {
+  // Column parts of the packed shrink: split the n*R columns (whole 16-column
+  // groups, a supported tile width) while a lower bound on the tiles times
+  // the parts stays within 152 CTAs.
+  const int nR = p.n_slices * p.R;
+  const long long tiles = (p.end + TM - 1) / TM;
+  int n = 1;
+  while (n < 4 && tiles * n * 2 <= 152 && nR % (32 * n) == 0 && nr_supported(nR / (2 * n))) n *= 2;
+  return n;
+}
+
+cudaError_t launch_tc_apply_packed(const ProblemDesc& p, void* workspace, cudaStream_t s) {
+  TcMaps smaps;
+  TxMaps xmaps;
+  if (!encode_maps(p, &smaps) || !encode_tx_maps(p, &xmaps)) return cudaErrorNotSupported;
+  const int nsn = tc_pack_splits(p);
+  uint8_t* upk = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_tc_shrink_maps(p, smaps, nullptr, s, 1, nsn, upk);
+  if (e != cudaSuccess) return e;
+  const TxWork w = make_tx_work(p, 1);
+  if (p.R == 64) return launch_tx_t<64, true>(p, xmaps, w, nullptr, upk, s, true);
+  return launch_tx_t<128, true>(p, xmaps, w, nullptr, upk, s, true);
 }
 
 }  // namespace lora

@@ -243,15 +243,23 @@ lora_status_t lora_shrink(const lora_problem_t* problem, const lora_routing_t* r
 lora_status_t lora_expand(const lora_problem_t* problem, const lora_routing_t* routing,
                           const float* u, lora_stream_t stream);
 
-/* Bytes of device workspace lora_sgmv_apply needs for `end` routed rows. */
+/*
+ * Bytes of device workspace lora_sgmv_apply needs for `end` routed rows: the
+ * larger of the fp32 intermediate (up to 16 partial planes of end x n*R) and,
+ * for max_lora_rank 64 or 128, the packed intermediate of the tensor-core path
+ * ((max_num_loras + end / 128) tiles x n*R x 512 bytes).  Depends on shapes
+ * only.
+ */
 size_t lora_workspace_bytes(const lora_problem_t* problem, int32_t end);
 
 /*
- * lora_sgmv_apply -- shrink then expand in one call; the fp32 intermediate
- * lives in `workspace` (DEVICE, >= lora_workspace_bytes(problem, end) bytes,
- * 16-byte aligned, contents on entry ignored).  The expand is launched as a
- * programmatic dependent of the shrink, so its weight and y loads overlap the
- * shrink.
+ * lora_sgmv_apply -- shrink then expand in one call; the intermediate lives in
+ * `workspace` (DEVICE, >= lora_workspace_bytes(problem, end) bytes, 16-byte
+ * aligned, contents on entry ignored): fp32 partial planes, or, on the
+ * tensor-core path (bf16, rank 64 or 128, long groups), u already split into
+ * bf16 hi + lo terms and laid out as the expand's operand per 128-row tile.
+ * The expand is launched as a programmatic dependent of the shrink, so its
+ * weight and y loads overlap the shrink.
  */
 lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_t* routing,
                               void* workspace, size_t workspace_bytes, lora_stream_t stream);
@@ -268,9 +276,9 @@ lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_
  * library (every GPU that loads the library holds it until the process exits).
  *
  * Same problem, routing, results and errors as lora_sgmv_apply, plus:
- *   - LORA_ERR_WORKSPACE if lora_workspace_bytes(problem, end) exceeds
- *     LORA_NOALLOC_MAX_WORKSPACE_BYTES (use lora_sgmv_apply with your own
- *     workspace for such batches).
+ *   - LORA_ERR_WORKSPACE if the fp32 intermediate, end x n*R x 4 bytes
+ *     rounded up to 256, exceeds LORA_NOALLOC_MAX_WORKSPACE_BYTES (use
+ *     lora_sgmv_apply with your own workspace for such batches).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; LORA_ERR_CUDA if the lookup fails.
  *     Make that first call before any stream capture.

@@ -679,47 +679,59 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       // A warp whose wait expired keeps walking the barrier protocol (doing
       // no work) so the other roles never block on it.
       bool bad = false;
-      // Segment s's u (sum of planes, plane order) -> bf16 hi | lo in buffer
-      // s % NUB; every epilogue thread arrives on uready once the rows are in.
-      auto load_u = [&](int s, const Tile& ts, int js) {
+      // fp32 u of segment s -> bf16 hi | lo in buffer s % NUB, in two steps.
+      // stage_u: 16-byte async copies put the fp32 values of columns
+      // k .. k+7 of this thread's row where their hi chunk (k .. k+3) and lo
+      // chunk (k+4 .. k+7) will live, so finish_u converts every 8-column
+      // group in place.  finish_u adds planes 1.. (plane order), converts and
+      // arrives on uready.
+      auto stage_u = [&](int s, const Tile& ts, int js) {
+        uint8_t* Ub = smem + (s % NUB) * Cfg::U_BYTES;
+        if (!bad && row < ts.rows) {
+          const float* ur = u + (long long)(ts.row0 + row) * nR + (long long)js * R;
+#pragma unroll
+          for (int m = 0; m < R / 8; ++m) {
+            cp_async16(Ub + sw128_offset(row, 8 * m), ur + 8 * m);
+            cp_async16(Ub + sw128_offset(row, R + 8 * m), ur + 8 * m + 4);
+          }
+        }
+        cp_async_commit();
+      };
+      auto finish_u = [&](int s, const Tile& ts, int js) {
         uint8_t* Ub = smem + (s % NUB) * Cfg::U_BYTES;
         const bool live = !bad && row < ts.rows;
         const float* ur = u + (long long)(ts.row0 + (live ? row : 0)) * nR + (long long)js * R;
-        // 32 columns per batch: all loads of a batch (every plane) are issued
-        // before any is consumed, so a batch costs one L2 round trip.
-        for (int k0 = 0; k0 < R; k0 += 32) {
-          float4 a[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            a[e] = live ? __ldcg(reinterpret_cast<const float4*>(ur + k0 + 4 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int sp = 1; live && sp < w.nsplit; ++sp) {
-            float4 b[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) b[e] = __ldcg(reinterpret_cast<const float4*>(ur + sp * w.plane_stride + k0 + 4 * e));
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              a[e].x += b[e].x;
-              a[e].y += b[e].y;
-              a[e].z += b[e].z;
-              a[e].w += b[e].w;
+        for (int m = 0; m < R / 8; ++m) {
+          uint4* ph = reinterpret_cast<uint4*>(Ub + sw128_offset(row, 8 * m));
+          uint4* pl = reinterpret_cast<uint4*>(Ub + sw128_offset(row, R + 8 * m));
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+          if (live) {
+            a = *reinterpret_cast<const float4*>(ph);
+            b = *reinterpret_cast<const float4*>(pl);
+            for (int sp = 1; sp < w.nsplit; ++sp) {
+              const float4 c = __ldcg(reinterpret_cast<const float4*>(ur + sp * w.plane_stride + 8 * m));
+              const float4 d = __ldcg(reinterpret_cast<const float4*>(ur + sp * w.plane_stride + 8 * m + 4));
+              a.x += c.x;
+              a.y += c.y;
+              a.z += c.z;
+              a.w += c.w;
+              b.x += d.x;
+              b.y += d.y;
+              b.z += d.z;
+              b.w += d.w;
             }
           }
+          const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // 8 columns -> one 16-byte hi chunk and one lo chunk
-            const float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w,
-                                a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z, a[2 * c + 1].w};
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
-              hi[e] = pack_bf16x2(h0, h1);
-              lo[e] = pack_bf16x2(__float2bfloat16_rn(v[2 * e] - __bfloat162float(h0)),
-                                  __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1)));
-            }
-            const int k = k0 + 8 * c;
-            *reinterpret_cast<uint4*>(Ub + sw128_offset(row, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(Ub + sw128_offset(row, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+            hi[e] = pack_bf16x2(h0, h1);
+            lo[e] = pack_bf16x2(__float2bfloat16_rn(v[2 * e] - __bfloat162float(h0)),
+                                __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1)));
           }
+          *ph = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         fence_proxy_async_smem();  // generic writes -> visible to the tensor cores
         mbar_arrive(&uready[s % NUB]);
@@ -741,14 +753,21 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
           cur_j = x.j;
           ++seg;
           kmax = slot_kmax(p, t.slot);
-          if (!PACKED && (NUB == 1 || seg == 0)) load_u(seg, t, x.j);
-          if (!PACKED && NUB == 2) {
-            const long long next = x.j + 1 < p.n_slices ? (long long)x.tile * w.nbt + w.blk_begin[x.j + 1]
-                                                        : (long long)(x.tile + 1) * w.nbt;
-            if (next < u1) {
-              const Unit nx = tx_unit(w, p.n_slices, next);
-              load_u(seg + 1, nx.tile == x.tile ? t : rc_tile(rc, G, nx.tile), nx.j);
+          if (!PACKED) {
+            if (NUB == 1 || seg == 0) stage_u(seg, t, x.j);
+            bool staged_next = false;
+            if (NUB == 2) {  // the next segment's u loads while this one is multiplied
+              const long long next = x.j + 1 < p.n_slices ? (long long)x.tile * w.nbt + w.blk_begin[x.j + 1]
+                                                          : (long long)(x.tile + 1) * w.nbt;
+              if (next < u1) {
+                const Unit nx = tx_unit(w, p.n_slices, next);
+                stage_u(seg + 1, nx.tile == x.tile ? t : rc_tile(rc, G, nx.tile), nx.j);
+                staged_next = true;
+              }
             }
+            if (staged_next) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            finish_u(seg, t, x.j);
           }
         }
         const SliceDesc& sl = p.sl[x.j];

@@ -420,6 +420,9 @@ namespace lora {
 namespace {
 
 constexpr int XB = 128;         // output columns per unit (MMA N)
+constexpr int XEPI = 8;         // epilogue warps: XEPI / 4 per TMEM lane quarter
+constexpr int XNH = XEPI / 4;   // ... each taking XB / XNH columns of a unit
+constexpr int XTHREADS = 32 * (2 + XEPI);
 constexpr int RC_MAX_G = 256;   // groups cached in shared memory
 
 template <int R>
@@ -496,7 +499,7 @@ __device__ __forceinline__ Unit tx_unit(const TxWork& w, int n_slices, long long
 // otherwise u is fp32 [end, n*R] (nsplit planes) and the epilogue warps
 // convert it.
 template <int R, bool PACKED>
-__global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __grid_constant__ ProblemDesc p,
+__global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __grid_constant__ ProblemDesc p,
                                                                     const __grid_constant__ TxMaps maps,
                                                                     const __grid_constant__ TxWork w,
                                                                     const float* __restrict__ u,
@@ -548,14 +551,14 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       s_fail = 0;
       for (int i = 0; i < NSLOT; ++i) {
         mbar_init(&full[i], 1);
-        mbar_init(&empty[i], 4);
+        mbar_init(&empty[i], XEPI);
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull[i], 1);
-        mbar_init(&tempty[i], 4);
+        mbar_init(&tempty[i], XEPI);
       }
       for (int i = 0; i < NUB; ++i) {
-        mbar_init(&uready[i], PACKED ? 1 : 4 * 32);
+        mbar_init(&uready[i], PACKED ? 1 : XEPI * 32);
         mbar_init(&ufree[i], 1);
       }
       fence_mbar_init();
@@ -670,8 +673,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       }
     }
   } else if (warp >= 2) {
-    // ---- epilogue warps: thread = one tile row = one TMEM lane
+    // ---- epilogue warps: thread = one tile row = one TMEM lane; warps w,
+    // w + 4, ... share lane quarter w % 4, warp w taking column part hf
     const int q = warp & 3;
+    const int hf = (warp - 2) >> 2;  // 0 .. XNH-1
     const int row = q * 32 + lane;
     const int nR = p.n_slices * R;
     if (ok) {
@@ -690,7 +695,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         if (!bad && row < ts.rows) {
           const float* ur = u + (long long)(ts.row0 + row) * nR + (long long)js * R;
 #pragma unroll
-          for (int m = 0; m < R / 8; ++m) {
+          for (int m = hf * R / (8 * XNH); m < (hf + 1) * R / (8 * XNH); ++m) {
             cp_async16(Ub + sw128_offset(row, 8 * m), ur + 8 * m);
             cp_async16(Ub + sw128_offset(row, R + 8 * m), ur + 8 * m + 4);
           }
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         uint8_t* Ub = smem + (s % NUB) * Cfg::U_BYTES;
         const bool live = !bad && row < ts.rows;
         const float* ur = u + (long long)(ts.row0 + (live ? row : 0)) * nR + (long long)js * R;
-        for (int m = 0; m < R / 8; ++m) {
+        for (int m = hf * R / (8 * XNH); m < (hf + 1) * R / (8 * XNH); ++m) {
           uint4* ph = reinterpret_cast<uint4*>(Ub + sw128_offset(row, 8 * m));
           uint4* pl = reinterpret_cast<uint4*>(Ub + sw128_offset(row, R + 8 * m));
           float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
@@ -783,7 +788,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const uint8_t* ys = slots + slot * Cfg::SLOT;
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
-        for (int c16 = 0; !bad && c16 < XB / 16; ++c16) {
+        for (int c16 = hf * XB / (16 * XNH); !bad && c16 < (hf + 1) * XB / (16 * XNH); ++c16) {
           float d[16];
           if (kmax > 0) {
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
@@ -898,7 +903,7 @@ cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& 
   const long long units_max = ((long long)p.G + p.end / TM) * w.nbt;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::max(1LL, std::min<long long>(sms, units_max)));
-  cfg.blockDim = dim3(TTHREADS);
+  cfg.blockDim = dim3(XTHREADS);
   cfg.dynamicSmemBytes = TxCfg<R>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

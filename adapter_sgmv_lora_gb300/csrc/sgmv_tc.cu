@@ -777,7 +777,6 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         }
         const SliceDesc& sl = p.sl[x.j];
         const bool live = row < t.rows;
-        __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(sl.y) + (long long)(t.row0 + (live ? row : 0)) * sl.y_row_stride;
         const int slot = i % NSLOT, buf = i & 1;
         if (!bad && !mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
           atomicOr(&s_fail, 1);
@@ -785,7 +784,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         }
         bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below needs the whole warp
         tc_fence_after_sync();
-        const uint8_t* ys = slots + slot * Cfg::SLOT;
+        uint8_t* ys = slots + slot * Cfg::SLOT;
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
         for (int c16 = hf * XB / (16 * XNH); !bad && c16 < (hf + 1) * XB / (16 * XNH); ++c16) {
@@ -809,24 +808,41 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
             }
           }
           if (live && c16 * 16 < ovalid) {
-            uint32_t out[8];
+            // y + delta, rounded once, written back over y in the slot.
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int cch = c16 * 2 + h;  // 16-byte chunk of the 128-column block
-              const uint4 yv = *reinterpret_cast<const uint4*>(ys + (cch >> 3) * TM * 128 + row * 128 +
-                                                               (((cch & 7) ^ (row & 7)) << 4));
+              uint4* py = reinterpret_cast<uint4*>(ys + (cch >> 3) * TM * 128 + row * 128 + (((cch & 7) ^ (row & 7)) << 4));
+              const uint4 yv = *py;
               const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+              uint32_t out[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xFFFF0000u);
-                out[h * 4 + e] = pack_bf16x2(__float2bfloat16_rn(y0 + d[h * 8 + 2 * e]),
-                                             __float2bfloat16_rn(y1 + d[h * 8 + 2 * e + 1]));
+                out[e] = pack_bf16x2(__float2bfloat16_rn(y0 + d[h * 8 + 2 * e]),
+                                     __float2bfloat16_rn(y1 + d[h * 8 + 2 * e + 1]));
               }
+              *py = make_uint4(out[0], out[1], out[2], out[3]);
             }
-            uint4* dst = reinterpret_cast<uint4*>(yrow + o0 + c16 * 16);
-            st_global_v4_hint(dst, make_uint4(out[0], out[1], out[2], out[3]), pol_stream);
-            if (c16 * 16 + 8 < ovalid)
-              st_global_v4_hint(dst + 1, make_uint4(out[4], out[5], out[6], out[7]), pol_stream);
+          }
+        }
+        __syncwarp();
+        // This warp's 32 rows x XB / XNH columns to y: eight lanes per row,
+        // so each store instruction writes whole 128-byte row segments.
+        if (!bad) {
+          constexpr int CPR = XB / XNH / 8;  // 16-byte chunks per row
+#pragma unroll
+          for (int it = 0; it < CPR; ++it) {
+            const int idx = it * 32 + lane;
+            const int tr = q * 32 + idx / CPR;           // tile row
+            const int cch = hf * CPR + idx % CPR;        // chunk of the 128-column block
+            if (tr < t.rows && cch * 8 < ovalid) {
+              const uint4 v = *reinterpret_cast<const uint4*>(ys + (cch >> 3) * TM * 128 + tr * 128 +
+                                                              (((cch & 7) ^ (tr & 7)) << 4));
+              st_global_v4_hint(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
+                                                         (long long)(t.row0 + tr) * sl.y_row_stride + o0 + cch * 8),
+                                v, pol_stream);
+            }
           }
         }
         tc_fence_before_sync();

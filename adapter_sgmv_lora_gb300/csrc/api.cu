@@ -218,7 +218,7 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
         return cuda_status(launch_expand_bf16(d, u, s, true, tcs));
       }
     }
-    const int splits = apply_splits(d.end, d.in_dim, d.n_slices * d.R);
+    const int splits = apply_splits_for(d);
     if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s))) != LORA_OK) return st;
     return cuda_status(launch_expand_bf16(d, u, s, true, splits));
   }

@@ -64,6 +64,9 @@ cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStrea
 cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit);
 // Partial planes the apply's shrink uses for this shape (1..8); shapes only.
 int apply_splits(int end, int in_dim, int nR);
+// The split the apply's partial-plane shrink actually uses (and its expand
+// sums): from the group count and CTA occupancy, at most apply_splits(...).
+int apply_splits_for(const ProblemDesc& p);
 
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
 // nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says

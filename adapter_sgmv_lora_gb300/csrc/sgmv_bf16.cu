@@ -508,7 +508,7 @@ cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int
   int C = 1;
   long long plane_stride = 0;
   if (partial) {
-    C = apply_splits(p.end, p.in_dim, p.n_slices * p.R);
+    C = apply_splits_for(p);
     if (C > 1) plane_stride = (long long)p.end * p.n_slices * p.R;
   } else {
     // Split the input dimension over a cluster until the grid covers the GPU.
@@ -583,6 +583,29 @@ bool fast_path_ok(const ProblemDesc& p, const void* u) {
     if (sl.bias && (!aligned16(sl.bias) || sl.bias_slot_stride % 8 != 0)) return false;
   }
   return true;
+}
+
+int apply_splits_for(const ProblemDesc& p) {
+  // At launch the group count is known: size the split on the upper bound
+  // of the tiles (G + end/64) and on how many of these CTAs share an SM, to
+  // about two waves; never above the shape-only bound the workspace holds.
+  const int cap = apply_splits(p.end, p.in_dim, p.n_slices * p.R);
+  int nblk = 1;
+  const int nb = pick_nb(p.n_slices * p.R, &nblk);
+  int smem = ShrinkCfg<128>::SMEM;
+  switch (nb) {
+    case 16: smem = ShrinkCfg<16>::SMEM; break;
+    case 32: smem = ShrinkCfg<32>::SMEM; break;
+    case 48: smem = ShrinkCfg<48>::SMEM; break;
+    case 64: smem = ShrinkCfg<64>::SMEM; break;
+    case 96: smem = ShrinkCfg<96>::SMEM; break;
+  }
+  const long long per_sm = std::max(1, (228 * 1024) / (smem + 1024));
+  const long long tiles = (long long)p.G + p.end / MT;
+  const int ksteps = p.in_dim / KS;
+  int C = 1;
+  while (C < cap && tiles * nblk * C * 2 <= 2LL * num_sms() * per_sm && ksteps % (C * 2) == 0) C *= 2;
+  return C;
 }
 
 int apply_splits(int end, int in_dim, int nR) {

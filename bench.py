@@ -84,6 +84,16 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: the apply is timed on its own)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def _names(proj):
     from workloads.synthetic import PROBLEMS
     return list(PROBLEMS[proj])
@@ -216,9 +226,16 @@ def cpu_baseline(workload, budget_s=12.0):
         done += run(nrows)
         reps += 1
     dt = time.perf_counter() - t0
+    from workloads.synthetic import SPECS
     return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d routed rows of one %s batch (qkv + o), %d repetitions, %.1f s, "
-                      "single-threaded C in double" % (nrows, end, workload, reps, dt)}
+            "sample": "%d of %d routed rows of one %s batch (%s), %d repetitions, %.1f s, "
+                      "single-threaded C in double" % (nrows, end, workload, " + ".join(SPECS[workload].problems),
+                                                       reps, dt)}
+
+
+def _spec_problems(workload):
+    from workloads.synthetic import SPECS
+    return SPECS[workload].problems
 
 
 def run_reference(args):
@@ -246,8 +263,8 @@ def run_reference(args):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload]},
            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                            "sample": "%d of %d routed rows per step (qkv + o), single-threaded C in double"
-                                      % (nrows, end)},
+                            "sample": "%d of %d routed rows per step (%s), single-threaded C in double"
+                                      % (nrows, end, " + ".join(_spec_problems(args.workload)))},
            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
     return 0
@@ -322,6 +339,13 @@ def run_ours(args):
     with torch.cuda.graph(g_qkv, stream=stream):
         for i in range(NS):
             sets[i]["call_qkv"].apply(torch.cuda.current_stream())
+    g_o = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_o, stream=stream):
+        for i in range(NS):
+            sets[i]["call_o"].apply(torch.cuda.current_stream())
+    g_warm = torch.cuda.CUDAGraph()  # one set's fused-qkv apply, replayed from L2
+    with torch.cuda.graph(g_warm, stream=stream):
+        sets[0]["call_qkv"].apply(torch.cuda.current_stream())
 
     def run_steps(k, start=0):
         i = 0
@@ -369,6 +393,32 @@ def run_ours(args):
     qkv_ms = r0.elapsed_time(r1) / (reps * NS)
     qkv_bytes = statistics.mean(algorithmic_bytes(s["p0"]["route_host"], s["raw"], P0, slot_ranks=args.slot_ranks)
                                 for s in sets)
+    qkv_flops = statistics.mean(algorithmic_flops(s["p0"]["route_host"], s["raw"], P0) for s in sets)
+
+    # ---- per projection: the second problem's apply alone, the same way
+    with torch.cuda.stream(stream):
+        g_o.replay()
+        r0.record(stream)
+        for _ in range(reps):
+            g_o.replay()
+        r1.record(stream)
+    torch.cuda.synchronize()
+    o_ms = r0.elapsed_time(r1) / (reps * NS)
+    o_bytes = statistics.mean(algorithmic_bytes(s["p1"]["route_host"], s["raw"], P1, slot_ranks=args.slot_ranks)
+                              for s in sets)
+
+    # ---- warm L2: set 0's fused-qkv apply replayed (its inputs stay in L2)
+    nwarm = 50
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_warm.replay()
+        r0.record(stream)
+        for _ in range(nwarm):
+            g_warm.replay()
+        r1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = r0.elapsed_time(r1) / nwarm
+    warm_bytes = algorithmic_bytes(sets[0]["p0"]["route_host"], sets[0]["raw"], P0, slot_ranks=args.slot_ranks)
     clocks = sampler.stop() if sampler else None
 
     (ms, qkv_ms), (tokens,) = reduce_across_ranks([ms, qkv_ms], [tokens], dist, "cuda")
@@ -381,6 +431,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
     peak, peak_kind = _peaks()
+    tpeak, tpeak_kind = _tensor_peak()
     achieved = qkv_bytes / (qkv_ms * 1e-3) / 1e9
     traffic = _profiled_traffic(args.workload)
     out = {
@@ -401,7 +452,19 @@ def run_ours(args):
                      "kernel": "%s SGMV apply (shrink + expand, PDL-chained)" % ("fused-" + P0 if len(_names(P0)) > 1 else P0),
                      "peak_source": "%s HBM copy bandwidth (MEASURED_PEAKS.json)" % peak_kind
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": int(qkv_bytes), "avg_launch_us": round(qkv_ms * 1e3, 3)},
+                     "algorithmic_bytes_per_launch": int(qkv_bytes), "avg_launch_us": round(qkv_ms * 1e3, 3),
+                     "flops_per_launch": int(qkv_flops),
+                     "t_hbm_us": round(qkv_bytes / (peak * 1e9) * 1e6, 3),
+                     "t_tensor_us": round(qkv_flops / (tpeak * 1e12) * 1e6, 3),
+                     "tensor_peak_tflops": tpeak, "tensor_peak_source": "%s bf16 dense (MEASURED_PEAKS.json)" % tpeak_kind
+                     if tpeak_kind == "measured" else "fallback 1.9 PFLOP/s"},
+        "per_projection": {
+            P0: {"avg_apply_us": round(qkv_ms * 1e3, 3), "GBps": round(qkv_bytes / (qkv_ms * 1e-3) / 1e9, 1)},
+            P1: {"avg_apply_us": round(o_ms * 1e3, 3), "GBps": round(o_bytes / (o_ms * 1e-3) / 1e9, 1)}},
+        "warm_l2": {"unit": "%s apply of input set 0 replayed %d times" % (P0, nwarm),
+                    "avg_apply_us": round(warm_ms * 1e3, 3),
+                    "GBps": round(warm_bytes / (warm_ms * 1e-3) / 1e9, 1),
+                    "note": "inputs resident in L2 after the first replay: not an HBM number"},
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,

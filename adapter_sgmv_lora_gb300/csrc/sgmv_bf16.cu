@@ -258,15 +258,21 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
 
 // ------------------------------------------------------------------ expand
 
-template <int R, int OB>
+// An expand tile is MR routed rows (64, or 32 for short groups) by OB output
+// columns; the 8 warps are MR/16 row blocks times 8/(MR/16) column groups.
+template <int R, int OB, int MR>
 struct ExpandCfg {
   static constexpr int YPITCH = OB * 2 + 16;  // bytes per staged y row
   static constexpr int BPITCH = R * 2 + 16;   // bytes per staged B row (conflict-free ldmatrix)
   static constexpr int UPITCH = 4 * R + 16;   // bytes per hi|lo row (2R bf16)
   static constexpr int Y_OFF = 0;
-  static constexpr int B_OFF = MT * YPITCH;
+  static constexpr int B_OFF = MR * YPITCH;
   static constexpr int H_OFF = B_OFF + OB * BPITCH;
-  static constexpr int SMEM = H_OFF + MT * UPITCH;
+  static constexpr int SMEM = H_OFF + MR * UPITCH;
+  static constexpr int MB = MR / 16;          // row blocks
+  static constexpr int NW = 8 / MB;           // column groups
+  static constexpr int CW = OB / NW;          // columns per warp
+  static_assert(CW % 16 == 0, "column group");
 };
 
 struct ExpandMap {
@@ -277,11 +283,11 @@ struct ExpandMap {
 };
 
 // GEN as for the shrink: token_rows, slot ranks or a bias in use.
-template <int R, int OB, bool GEN>
+template <int R, int OB, int MR, bool GEN>
 __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                const float* __restrict__ u,
                                                                const __grid_constant__ ExpandMap map) {
-  using Cfg = ExpandCfg<R, OB>;
+  using Cfg = ExpandCfg<R, OB, MR>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Tile s_tile;
   __shared__ int s_ok;
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 
   if (warp == 0) {
     Tile t{};
-    const bool ok = warp_locate_tile(p, MT, tile, t);
+    const bool ok = warp_locate_tile(p, MR, tile, t);
     if (lane == 0) {
       s_tile = t;
       s_ok = ok;
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 
   // Row of y holding each token of the tile (gathered batches map through
   // token_rows); an out-of-range entry skips the tile.
-  __shared__ int s_rows[MT];
+  __shared__ int s_rows[MR];
   if constexpr (GEN) {
     int bad_row = 0;
     for (int r = threadIdx.x; r < t.rows; r += blockDim.x) {
@@ -387,14 +393,14 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   cp_async_wait<0>();
   __syncthreads();
 
-  const int m = warp & 3, nh = warp >> 2;
-  constexpr int NT = OB / 16;  // n8 tiles per warp
+  const int m = warp % Cfg::MB, nh = warp / Cfg::MB;
+  constexpr int NT = Cfg::CW / 8;  // n8 tiles per warp
   const int g = lane >> 2, tq = lane & 3;
   if (m * 16 < t.rows) {
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int col = nh * (OB / 2) + nt * 8 + 2 * tq;
+      const int col = nh * Cfg::CW + nt * 8 + 2 * tq;
       const __nv_bfloat162 v0 =
           *reinterpret_cast<const __nv_bfloat162*>(Ys + (m * 16 + g) * Cfg::YPITCH + col * 2);
       const __nv_bfloat162 v1 =
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 #pragma unroll
       for (int np = 0; np < NT / 2; ++np) {
         uint32_t b0, b1, b2, b3;
-        const int nrow = nh * (OB / 2) + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int nrow = nh * Cfg::CW + np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int kcol = kb + ((lane >> 3) & 1) * 8;
         ldsm_x4(bs + nrow * Cfg::BPITCH + kcol * 2, b0, b1, b2, b3);
         mma_bf16_16816(acc[2 * np], a, b0, b1);
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int col = nh * (OB / 2) + nt * 8 + 2 * tq;
+      const int col = nh * Cfg::CW + nt * 8 + 2 * tq;
       *reinterpret_cast<__nv_bfloat162*>(Ys + (m * 16 + g) * Cfg::YPITCH + col * 2) =
           __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
       *reinterpret_cast<__nv_bfloat162*>(Ys + (m * 16 + g + 8) * Cfg::YPITCH + col * 2) =
@@ -534,10 +540,10 @@ cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int
   return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride);
 }
 
-template <int R, int OB, bool GEN>
+template <int R, int OB, int MR, bool GEN>
 cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
-  auto kernel = sgmv_expand_bf16_kernel<R, OB, GEN>;
-  const int smem = ExpandCfg<R, OB>::SMEM;
+  auto kernel = sgmv_expand_bf16_kernel<R, OB, MR, GEN>;
+  const int smem = ExpandCfg<R, OB, MR>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);
   if (e != cudaSuccess) return e;
@@ -551,7 +557,7 @@ cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s
   map.n_ob_total = acc;
   map.nsplit = nsplit;
   map.plane_stride = (long long)p.end * p.n_slices * R;
-  const long long tiles = (long long)p.G + p.end / MT;
+  const long long tiles = (long long)p.G + p.end / MR;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * acc));
   cfg.blockDim = dim3(256);
@@ -651,11 +657,17 @@ static cudaError_t dispatch_shrink(const ProblemDesc& p, float* u, cudaStream_t 
 
 template <bool GEN>
 static cudaError_t dispatch_expand_g(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
+  // Short groups (at most 32 routed rows each on average): 32-row tiles twice
+  // as wide, so a tile's fixed costs (routing lookup, u, B block) cover twice
+  // the outputs and the grid has half the CTAs.
+  const bool short_groups = (long long)p.end <= 32LL * p.G;
   switch (p.R) {
-    case 16: return launch_expand_r<16, 256, GEN>(p, u, s, pdl, nsplit);
-    case 32: return launch_expand_r<32, 256, GEN>(p, u, s, pdl, nsplit);
-    case 64: return launch_expand_r<64, 128, GEN>(p, u, s, pdl, nsplit);
-    default: return launch_expand_r<128, 64, GEN>(p, u, s, pdl, nsplit);
+    case 16:
+      return short_groups ? launch_expand_r<16, 512, 32, GEN>(p, u, s, pdl, nsplit)
+                          : launch_expand_r<16, 256, 64, GEN>(p, u, s, pdl, nsplit);
+    case 32: return launch_expand_r<32, 256, 64, GEN>(p, u, s, pdl, nsplit);
+    case 64: return launch_expand_r<64, 128, 64, GEN>(p, u, s, pdl, nsplit);
+    default: return launch_expand_r<128, 64, 64, GEN>(p, u, s, pdl, nsplit);
   }
 }
 

@@ -70,6 +70,9 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   __shared__ Tile s_tile;
   __shared__ int s_ok;
 
+  // Launched as a programmatic dependent of whatever kernel precedes it: no
+  // global memory is touched before that kernel has completed.
+  pdl_wait();
   pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -453,6 +456,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
       *reinterpret_cast<uint4*>(yg + y_row(r) * sl.y_row_stride + o0 + ch * 8) =
           *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
   }
+  pdl_launch_dependents();  // the next kernel may launch; it waits for this grid to finish
 }
 
 // ------------------------------------------------------------------ host
@@ -534,6 +538,11 @@ cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else if (partial) {  // the apply's shrink overlaps its launch with the previous kernel's tail
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }

@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   // 1024-byte aligned ring (the 128-byte swizzle repeats every 1024 bytes).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+  // Launched as a programmatic dependent of whatever kernel precedes it: no
+  // global memory is touched before that kernel has completed.
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = (int)(blockIdx.x % (unsigned)nsplit);
   const int cn = (int)((blockIdx.x / (unsigned)nsplit) % (unsigned)nsn);
@@ -335,6 +338,11 @@ cudaError_t launch_tc_t(const ProblemDesc& p, const TcMaps& maps, float* u, cuda
   cfg.blockDim = dim3(TTHREADS);
   cfg.dynamicSmemBytes = TcCfg<NR>::SMEM;
   cfg.stream = s;
+  cudaLaunchAttribute attr[1];  // overlap the launch with the previous kernel's tail
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, p, maps, u, nsplit, plane_stride, nsn, upk);
 }
 
@@ -854,6 +862,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       }
     }
   }
+  pdl_launch_dependents();  // the next kernel may launch; it waits for this grid to finish
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {

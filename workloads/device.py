@@ -33,7 +33,7 @@ def torch_to_storage(t: torch.Tensor, dtype: str) -> np.ndarray:
 
 
 def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y: bool = False,
-            slot_ranks: bool = False) -> dict:
+            slot_ranks: bool = False, shared_routing=None) -> dict:
     """Build one projection problem ("qkv", "o", "gateup" or "down") on the device.
 
     fused=True: one fused stack A [S, n*R, in], B [S, O, R] and y [T, O].
@@ -42,6 +42,8 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
     per projection.  When the workload carries a bias (synthetic.add_bias) the
     slices get bias stacks filled by lora_set_slot_bias; slot_ranks=True
     passes the slots' true ranks so the kernels skip the padding.
+    shared_routing=(route_host, routing) reuses another problem's routing (the
+    same batch): no new triple is built or uploaded.
     """
     dt = raw["dtype"]
     tdt = _TORCH_DT[dt]
@@ -95,8 +97,11 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
             if has_bias:
                 bias_raw = torch.from_numpy(np.ascontiguousarray(raw["bias"][nm][s], dtype=np.float32)).to(device)
                 lk.lora_set_slot_bias(prob, j, s, bias_raw)
-    rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], S)
-    routing = lk.routing_to_device(rt, device)
+    if shared_routing is None:
+        rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], S)
+        routing = lk.routing_to_device(rt, device)
+    else:
+        rt, routing = shared_routing
     ws = torch.empty(max(lk.lora_workspace_bytes(prob, rt["end"]), 256) // 4, dtype=torch.float32,
                      device=device)
     return {"problem": prob, "routing": routing, "route_host": rt, "x": x, "ys": ys, "y_all": y_all,

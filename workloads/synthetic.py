@@ -165,12 +165,19 @@ def to_storage(a32: np.ndarray, dtype: str) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16).copy()
 
 
-def draw(spec, seed: int = 0, with_weights: bool = True) -> dict:
-    """Draw one workload instance.  Deterministic in (spec, seed)."""
+def draw(spec, seed: int = 0, with_weights: bool = True, requests=None) -> dict:
+    """Draw one workload instance.  Deterministic in (spec, seed, requests).
+
+    requests=(slots, lens) reuses another instance's request list (another
+    layer of the same batch): adapters, x and y are still drawn from `seed`."""
     if isinstance(spec, str):
         spec = SPECS[spec]
     rng = np.random.default_rng(seed)
-    slots, lens = draw_requests(rng, spec)
+    if requests is None:
+        slots, lens = draw_requests(rng, spec)
+    else:
+        slots = np.asarray(requests[0], dtype=np.int32).copy()
+        lens = np.asarray(requests[1], dtype=np.int32).copy()
     S, R = spec.max_num_loras, spec.max_lora_rank
     if spec.fixed_ranks is not None:
         ranks = np.asarray(spec.fixed_ranks, dtype=np.int32)

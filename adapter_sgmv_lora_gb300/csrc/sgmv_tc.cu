@@ -827,8 +827,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xFFFF0000u);
-                out[e] = pack_bf16x2(__float2bfloat16_rn(y0 + d[h * 8 + 2 * e]),
-                                     __float2bfloat16_rn(y1 + d[h * 8 + 2 * e + 1]));
+                out[e] = round_pack_bf16x2(y0 + d[h * 8 + 2 * e], y1 + d[h * 8 + 2 * e + 1]);
               }
               *py = make_uint4(out[0], out[1], out[2], out[3]);
             }

@@ -167,11 +167,32 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Two fp32 additions in one packed instruction (each lane rounds to nearest
+// like a scalar add).
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+  float2 o;
+  asm("{\n\t.reg .b64 pa, pb, pr;\n\t"
+      "mov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pb, {%4, %5};\n\t"
+      "add.rn.f32x2 pr, pa, pb;\n\t"
+      "mov.b64 {%0, %1}, pr;\n\t}"
+      : "=f"(o.x), "=f"(o.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return o;
+}
+
 // Two floats rounded to nearest-even bf16 in one conversion, `lo` in the
 // low half (same bits as pack_bf16x2 of two separate roundings).
 __device__ __forceinline__ uint32_t round_pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Exact two-term bf16 split of two floats: hi = rn(v), lo = rn(v - hi), each
+// pair packed (first value in the low half), one conversion per pair.
+__device__ __forceinline__ void split_hi_lo_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = round_pack_bf16x2(a, b);
+  lo = round_pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 hi) {

@@ -383,14 +383,12 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
           v.z += part[q].z;
           v.w += part[q].w;
         }
-      const float vals[4] = {v.x, v.y, v.z, v.w};
       __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(vals[i]);
-        hrow[k + i] = hi;
-        hrow[R + k + i] = __float2bfloat16_rn(vals[i] - __bfloat162float(hi));
-      }
+      uint32_t hi[2], lo[2];
+      split_hi_lo_bf16x2(v.x, v.y, hi[0], lo[0]);
+      split_hi_lo_bf16x2(v.z, v.w, hi[1], lo[1]);
+      *reinterpret_cast<uint2*>(hrow + k) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(hrow + R + k) = make_uint2(lo[0], lo[1]);
     }
   }
   cp_async_wait<0>();

@@ -66,12 +66,7 @@ __device__ __forceinline__ void pack_u16(uint8_t* blk, int R, int r, int k0, con
   for (int h = 0; h < 2; ++h) {
     uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a = v[8 * h + 2 * e], b = v[8 * h + 2 * e + 1];
-      const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-      hi[e] = pack_bf16x2(ha, hb);
-      lo[e] = pack_bf16x2(__float2bfloat16_rn(a - __bfloat162float(ha)), __float2bfloat16_rn(b - __bfloat162float(hb)));
-    }
+    for (int e = 0; e < 4; ++e) split_hi_lo_bf16x2(v[8 * h + 2 * e], v[8 * h + 2 * e + 1], hi[e], lo[e]);
     const int k = k0 + 8 * h;
     *reinterpret_cast<uint4*>(blk + sw128_offset(r, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     *reinterpret_cast<uint4*>(blk + sw128_offset(r, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -737,12 +732,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
           const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
-            hi[e] = pack_bf16x2(h0, h1);
-            lo[e] = pack_bf16x2(__float2bfloat16_rn(v[2 * e] - __bfloat162float(h0)),
-                                __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1)));
-          }
+          for (int e = 0; e < 4; ++e) split_hi_lo_bf16x2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
           *ph = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
@@ -826,8 +816,9 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
               uint32_t out[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xFFFF0000u);
-                out[e] = round_pack_bf16x2(y0 + d[h * 8 + 2 * e], y1 + d[h * 8 + 2 * e + 1]);
+                const float2 yy = make_float2(__uint_as_float(yw[e] << 16), __uint_as_float(yw[e] & 0xFFFF0000u));
+                const float2 r = add_f32x2(yy, make_float2(d[h * 8 + 2 * e], d[h * 8 + 2 * e + 1]));
+                out[e] = round_pack_bf16x2(r.x, r.y);
               }
               *py = make_uint4(out[0], out[1], out[2], out[3]);
             }

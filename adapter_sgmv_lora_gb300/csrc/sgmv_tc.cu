@@ -44,7 +44,9 @@ struct TcCfg {
   static constexpr int X_BYTES = TM * TK * 2;  // 16 KB
   static constexpr int A_BYTES = NR * TK * 2;
   static constexpr int STAGE = X_BYTES + ((A_BYTES + 1023) / 1024) * 1024;
-  static constexpr int NSTAGE = (200 * 1024) / STAGE >= 4 ? 4 : (200 * 1024) / STAGE;
+  // As deep a ring as ~208 KB holds (up to 8 stages): with one CTA per SM the
+  // bytes in flight per SM are what sets the streaming rate.
+  static constexpr int NSTAGE = (208 * 1024) / STAGE >= 8 ? 8 : (208 * 1024) / STAGE;
   static constexpr int SMEM = NSTAGE * STAGE + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : NR <= 256 ? 256 : 512;
 };

@@ -119,8 +119,13 @@ def _stream_handle(stream) -> Optional[int]:
 
 # --------------------------------------------------------------- routing --
 
-def lora_build_routing(req_slot, req_num_tokens, max_num_loras: int) -> dict:
-    """Host sort + group (see include/lora_sgmv.h).  Returns numpy arrays."""
+def lora_build_routing(req_slot, req_num_tokens, max_num_loras: int, out_ids=None, out_offsets=None) -> dict:
+    """Host sort + group (see include/lora_sgmv.h).  Returns numpy arrays.
+
+    out_ids / out_offsets (optional): contiguous int32 arrays of at least
+    max_num_loras and max_num_loras + 1 elements (for instance views of
+    pinned host tensors) that receive lora_ids and grouped_offsets directly;
+    the returned entries are then views of them."""
     L = lib()
     slots = np.ascontiguousarray(np.asarray(req_slot, dtype=np.int32))
     lens = np.ascontiguousarray(np.asarray(req_num_tokens, dtype=np.int32))
@@ -129,15 +134,20 @@ def lora_build_routing(req_slot, req_num_tokens, max_num_loras: int) -> dict:
     n = int(slots.size)
     S = int(max_num_loras)
     perm = np.zeros(max(n, 1), dtype=np.int32)
-    ids = np.zeros(max(S, 1), dtype=np.int32)
-    offs = np.zeros(max(S, 1) + 1, dtype=np.int32)
+    for a, need, name in ((out_ids, max(S, 1), "out_ids"), (out_offsets, max(S, 1) + 1, "out_offsets")):
+        if a is not None and (a.dtype != np.int32 or a.ndim != 1 or a.size < need or not a.flags.c_contiguous):
+            raise ValueError("%s must be a contiguous int32 array of at least %d elements" % (name, need))
+    ids = out_ids if out_ids is not None else np.zeros(max(S, 1), dtype=np.int32)
+    offs = out_offsets if out_offsets is not None else np.zeros(max(S, 1) + 1, dtype=np.int32)
     G, end, T = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
     rc = L.lora_build_routing(n, p(slots), p(lens), S, p(perm), p(ids), p(offs), ctypes.byref(G),
                               ctypes.byref(end), ctypes.byref(T))
     _check(rc, "lora_build_routing")
     g = G.value
-    return {"perm": perm[:n].copy(), "lora_ids": ids[:g].copy(), "grouped_offsets": offs[:g + 1].copy(),
+    keep_ids = ids[:g] if out_ids is not None else ids[:g].copy()
+    keep_offs = offs[:g + 1] if out_offsets is not None else offs[:g + 1].copy()
+    return {"perm": perm[:n].copy(), "lora_ids": keep_ids, "grouped_offsets": keep_offs,
             "num_groups": g, "end": end.value, "total_tokens": T.value}
 
 
@@ -352,6 +362,12 @@ class CallBuilder:
         self.ws = workspace.data_ptr()
         self.nbytes = workspace.numel() * workspace.element_size()
         self._keep = (problem, routing, workspace)
+
+    def set_routing(self, num_groups: int, end: int) -> None:
+        """A new batch in the same device routing buffers: only the host
+        num_groups and end change."""
+        self.r.num_groups = int(num_groups)
+        self.r.end = int(end)
 
     def apply(self, stream=None) -> None:
         rc = self.L.lora_sgmv_apply(ctypes.byref(self.c), ctypes.byref(self.r), self.ws, self.nbytes,

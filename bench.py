@@ -501,7 +501,10 @@ def _profiled_traffic(workload):
 
 
 def run_e2e(args, sets, lk, torch, stream, dist):
-    """Host buffers -> device -> apply (qkv, o) -> host, through the Python API."""
+    """Host buffers -> device -> apply (both problems) -> host, through the Python API:
+    per step the host routing build (into pinned buffers), pinned H2D of x, y
+    and the triple, two lora_sgmv_apply calls (pre-marshalled CallBuilders
+    given the step's num_groups / end), D2H of both y."""
     n = min(len(sets), max(4, min(args.steps, 32)))
     host = []
     for s in sets[:n]:
@@ -516,8 +519,11 @@ def run_e2e(args, sets, lk, torch, stream, dist):
         h["out_p1"] = torch.empty_like(h["y_" + P1]).pin_memory()
         h["ids"] = torch.empty(raw["max_num_loras"], dtype=torch.int32).pin_memory()
         h["offs"] = torch.empty(raw["max_num_loras"] + 1, dtype=torch.int32).pin_memory()
+        h["ids_np"], h["offs_np"] = h["ids"].numpy(), h["offs"].numpy()
         h["ev"] = torch.cuda.Event()
         h["ev"].record()
+        h["calls"] = [(key, proj, lk.CallBuilder(s[key]["problem"], s[key]["routing"], s[key]["workspace"]))
+                      for key, proj in (("p0", P0), ("p1", P1))]
         host.append(h)
     h2d = d2h = 0
 
@@ -525,13 +531,12 @@ def run_e2e(args, sets, lk, torch, stream, dist):
         nonlocal h2d, d2h
         s, h = sets[i], host[i]
         raw = s["raw"]
-        rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], raw["max_num_loras"])
+        h["ev"].synchronize()  # the previous copies out of / into these pinned buffers have finished
+        rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], raw["max_num_loras"],
+                                   out_ids=h["ids_np"], out_offsets=h["offs_np"])
         G = rt["num_groups"]
-        h["ev"].synchronize()  # the previous copy out of these pinned buffers has finished
-        h["ids"][:G].copy_(torch.from_numpy(rt["lora_ids"]))
-        h["offs"][:G + 1].copy_(torch.from_numpy(rt["grouped_offsets"]))
         copied = []
-        for key, proj in (("p0", raw["problems"][0]), ("p1", raw["problems"][1])):
+        for key, proj, call in h["calls"]:
             d = s[key]
             d["x"].copy_(h["x_" + proj], non_blocking=True)
             d["y_all"].copy_(h["y_" + proj], non_blocking=True)
@@ -541,8 +546,8 @@ def run_e2e(args, sets, lk, torch, stream, dist):
                 d["routing"].grouped_offsets[:G + 1].copy_(h["offs"][:G + 1], non_blocking=True)
                 h2d += 4 * (2 * G + 1)
                 copied.append(d["routing"])
-            lk.lora_sgmv_apply(d["problem"], lk.Routing(d["routing"].lora_ids, d["routing"].grouped_offsets,
-                                                        G, rt["end"]), d["workspace"], st)
+            call.set_routing(G, rt["end"])
+            call.apply(st)
         for key in ("p0", "p1"):
             h["out_" + key].copy_(s[key]["y_all"], non_blocking=True)
             d2h += 2 * h["out_" + key].numel()
@@ -570,8 +575,8 @@ def run_e2e(args, sets, lk, torch, stream, dist):
     (ms,), (toks,) = reduce_across_ranks([ms], [toks], dist, "cuda")
     return {"value": toks / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d // k,
             "d2h_bytes_per_step": d2h // k, "steps": k,
-            "note": "per step: host routing build, pinned H2D of x/y/triple for qkv and o, two "
-                    "lora_sgmv_apply calls, D2H of both y"}
+            "note": "per step: host routing build into pinned buffers, pinned H2D of x/y (both problems) "
+                    "and the triple, two lora_sgmv_apply calls, D2H of both y"}
 
 
 def main():

@@ -83,6 +83,31 @@ def test_routing_matches_oracle_workloads():
             _cmp_routing(raw["req_slot"], raw["req_len"], raw["max_num_loras"])
 
 
+def test_routing_into_caller_buffers():
+    """out_ids / out_offsets receive exactly what the default path returns;
+    entries past num_groups are left alone; wrong buffers are refused."""
+    rng = np.random.default_rng(12)
+    for trial in range(50):
+        S = int(rng.integers(1, 40))
+        n = int(rng.integers(0, 200))
+        slots = rng.integers(-1, S, size=n).astype(np.int32)
+        lens = rng.integers(0, 20, size=n).astype(np.int32)
+        ref = lk.lora_build_routing(slots, lens, S)
+        ids = np.full(S + 3, -7, dtype=np.int32)
+        offs = np.full(S + 4, -7, dtype=np.int32)
+        got = lk.lora_build_routing(slots, lens, S, out_ids=ids, out_offsets=offs)
+        g = ref["num_groups"]
+        assert got["num_groups"] == g and got["end"] == ref["end"]
+        assert np.array_equal(ids[:g], ref["lora_ids"]) and np.array_equal(offs[:g + 1], ref["grouped_offsets"])
+        assert np.array_equal(got["lora_ids"], ref["lora_ids"])
+        assert g == 0 or np.shares_memory(got["lora_ids"], ids)
+        assert np.all(ids[S:] == -7) and np.all(offs[S + 1:] == -7)
+    with pytest.raises(ValueError):
+        lk.lora_build_routing([0], [1], 4, out_ids=np.zeros(3, dtype=np.int32))
+    with pytest.raises(ValueError):
+        lk.lora_build_routing([0], [1], 4, out_offsets=np.zeros(5, dtype=np.int64))
+
+
 def test_routing_errors():
     with pytest.raises(lk.LoraError) as e:
         lk.lora_build_routing([0, 5], [1, 1], 3)

@@ -95,7 +95,7 @@ size_t plane_bytes(const lora_problem_t* p, int32_t end) {
 }
 
 // lora_sgmv_apply's workspace: its shrink may split the input dimension into
-// up to 8 partial planes (apply_splits), summed by the expand; or, on the
+// up to 16 partial planes (apply_splits), summed by the expand; or, on the
 // tensor-core path for ranks 64 and 128, it holds u packed per 128-row tile
 // (at most max_num_loras + end / 128 tiles).
 size_t ws_bytes(const lora_problem_t* p, int32_t end) {

@@ -281,7 +281,7 @@ struct ExpandCfg {
 struct ExpandMap {
   int n_ob_total;                     // output blocks per tile, all slices
   int ob_begin[LORA_MAX_SLICES + 1];  // first output block of each slice
-  int nsplit;                         // partial planes of u to sum (1..8)
+  int nsplit;                         // partial planes of u to sum (1..16)
   long long plane_stride;             // elements between planes
 };
 
@@ -370,19 +370,27 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
     for (int e = threadIdx.x; e < t.rows * R4; e += blockDim.x) {
       const int r = e / R4, k = (e % R4) * 4;
       const float* src = ub + (long long)r * nR + k;
-      float4 part[8];
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      // Planes in order, eight loads in flight per batch (one batch for up
+      // to 8 planes).
+      for (int q0 = 0; q0 < map.nsplit; q0 += 8) {
+        float4 part[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q < map.nsplit) part[q] = __ldcg(reinterpret_cast<const float4*>(src + q * map.plane_stride));
-      float4 v = part[0];
+        for (int q = 0; q < 8; ++q)
+          if (q0 + q < map.nsplit) part[q] = __ldcg(reinterpret_cast<const float4*>(src + (q0 + q) * map.plane_stride));
 #pragma unroll
-      for (int q = 1; q < 8; ++q)
-        if (q < map.nsplit) {
-          v.x += part[q].x;
-          v.y += part[q].y;
-          v.z += part[q].z;
-          v.w += part[q].w;
-        }
+        for (int q = 0; q < 8; ++q)
+          if (q0 + q < map.nsplit) {
+            if (q0 + q == 0) {
+              v = part[0];
+            } else {
+              v.x += part[q].x;
+              v.y += part[q].y;
+              v.z += part[q].z;
+              v.w += part[q].w;
+            }
+          }
+      }
       __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
       uint32_t hi[2], lo[2];
       split_hi_lo_bf16x2(v.x, v.y, hi[0], lo[0]);
@@ -622,17 +630,19 @@ int apply_splits_for(const ProblemDesc& p) {
 }
 
 int apply_splits(int end, int in_dim, int nR) {
-  // Largest power of two <= 8 dividing the input stages such that the
-  // partial-plane shrink grid (a lower bound on its tiles: ceil(end / 64))
-  // stays within 256 CTAs.  Depends on shapes only, so the workspace bound
-  // can be computed without a device.
+  // Largest power of two <= 8 (16 for inputs of 8192 and more, whose K
+  // ranges are long) dividing the input stages such that the partial-plane
+  // shrink grid (a lower bound on its tiles: ceil(end / 64)) stays within 256
+  // CTAs.  Depends on shapes only, so the workspace bound can be computed
+  // without a device.
   if (end <= 0 || in_dim % KS != 0) return 1;
   int nblk = 1;
   (void)pick_nb(nR, &nblk);
   const long long tiles = (end + MT - 1) / MT;
   const int ksteps = in_dim / KS;
   int C = 1;
-  while (C < 8 && tiles * nblk * C * 2 <= 256 && ksteps % (C * 2) == 0) C *= 2;
+  const int cmax = in_dim >= 8192 ? 16 : 8;
+  while (C < cmax && tiles * nblk * C * 2 <= 256 && ksteps % (C * 2) == 0) C *= 2;
   return C;
 }
 

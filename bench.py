@@ -133,8 +133,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (arrival time, csv line)
         self.t = None
+        self.window = None
 
     def start(self):
         try:
@@ -148,7 +149,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        """The timed region ran from t0 to t1 (time.time()): only samples taken
+        in it (or the one right after) are summarised, when there are any."""
+        self.window = (t0, t1 + 0.25)
 
     def stop(self):
         if self.proc is None:
@@ -160,7 +166,11 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            inside = [(t, ln) for t, ln in lines if self.window[0] <= t <= self.window[1]]
+            lines = inside or lines
+        for _, ln in lines:
             p = [v.strip() for v in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -174,7 +184,8 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "timed region" if self.window is not None and
+                len([1 for t, _ in self.lines if self.window[0] <= t <= self.window[1]]) else "whole run"}
 
 
 # ----------------------------------------------------------------- oracle --
@@ -242,6 +253,8 @@ def run_reference(args):
     rank, world, _ = _env_rank()
     if rank != 0:
         return 0
+    if args.steps <= 0:
+        args.steps = 20
     run, end = oracle_step_sampler(args.workload, 0, 0)
     run(min(end, 4))
     t0 = time.perf_counter()
@@ -371,6 +384,23 @@ def run_ours(args):
         run_steps(max(args.warmup, 3))
     stream.synchronize()
 
+    if args.steps <= 0:
+        # Default: about one second of timed work (at least 640 steps), so
+        # the clock samples fall inside the timed region.
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            p0.record(stream)
+            run_steps(NS)
+            p1.record(stream)
+        torch.cuda.synchronize()
+        per_step = max(p0.elapsed_time(p1) / NS, 1e-4)
+        k = int(min(200000, max(640, 1000.0 / per_step)))
+        if dist:
+            kt = torch.tensor([k], device="cuda")
+            dist.all_reduce(kt, op=dist.ReduceOp.MAX)
+            k = int(kt.item())
+        args.steps = k
+
     # ---- timed region
     sampler = ClockSampler(dev_idx) if rank == 0 else None
     if sampler:
@@ -380,11 +410,14 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
     with torch.cuda.stream(stream):
         ev0.record(stream)
         run_steps(args.steps)
         ev1.record(stream)
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(wall0, time.time())
     if dist:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
@@ -559,7 +592,7 @@ def run_e2e(args, sets, lk, torch, stream, dist):
             one(i, stream)
     stream.synchronize()
     h2d = d2h = 0
-    k = max(args.steps // 4, n)
+    k = max(min(args.steps // 4, 400), n)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -582,7 +615,8 @@ def run_e2e(args, sets, lk, torch, stream, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=640)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (0: about one second of work, at least 640)")
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode8b", choices=sorted(WORKLOAD_DESC))

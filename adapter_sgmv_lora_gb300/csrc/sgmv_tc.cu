@@ -787,42 +787,48 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         uint8_t* ys = slots + slot * Cfg::SLOT;
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
-        for (int c16 = hf * XB / (16 * XNH); !bad && c16 < (hf + 1) * XB / (16 * XNH); ++c16) {
-          float d[16];
+        // 32 columns per TMEM load: two 16-column groups.
+        for (int c32 = hf * XB / (32 * XNH); !bad && c32 < (hf + 1) * XB / (32 * XNH); ++c32) {
+          float dd[32];
           if (kmax > 0) {
-            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c16 * 16), d);
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c32 * 32), dd);
           } else {  // rank 0: no MMA was issued for this unit, the delta is zero
 #pragma unroll
-            for (int e = 0; e < 16; ++e) d[e] = 0.f;
+            for (int e = 0; e < 32; ++e) dd[e] = 0.f;
           }
-          if (sl.bias && c16 * 16 < ovalid) {  // bias joins the delta before the one rounding
-            const uint4* bp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(sl.bias) +
-                                                             (long long)t.slot * sl.bias_slot_stride + o0 + c16 * 16);
-            const uint4 b0 = __ldg(bp);
-            const uint4 b1 = (c16 * 16 + 8 < ovalid) ? __ldg(bp + 1) : make_uint4(0, 0, 0, 0);
-            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              d[2 * e] += __uint_as_float(bw[e] << 16);
-              d[2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
-            }
-          }
-          if (live && c16 * 16 < ovalid) {
-            // y + delta, rounded once, written back over y in the slot.
+          for (int g16 = 0; g16 < 2; ++g16) {
+            const int c16 = c32 * 2 + g16;
+            float* d = dd + 16 * g16;
+            if (sl.bias && c16 * 16 < ovalid) {  // bias joins the delta before the one rounding
+              const uint4* bp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(sl.bias) +
+                                                               (long long)t.slot * sl.bias_slot_stride + o0 + c16 * 16);
+              const uint4 b0 = __ldg(bp);
+              const uint4 b1 = (c16 * 16 + 8 < ovalid) ? __ldg(bp + 1) : make_uint4(0, 0, 0, 0);
+              const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int cch = c16 * 2 + h;  // 16-byte chunk of the 128-column block
-              uint4* py = reinterpret_cast<uint4*>(ys + (cch >> 3) * TM * 128 + row * 128 + (((cch & 7) ^ (row & 7)) << 4));
-              const uint4 yv = *py;
-              const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-              uint32_t out[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 yy = make_float2(__uint_as_float(yw[e] << 16), __uint_as_float(yw[e] & 0xFFFF0000u));
-                const float2 r = add_f32x2(yy, make_float2(d[h * 8 + 2 * e], d[h * 8 + 2 * e + 1]));
-                out[e] = round_pack_bf16x2(r.x, r.y);
+              for (int e = 0; e < 8; ++e) {
+                d[2 * e] += __uint_as_float(bw[e] << 16);
+                d[2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
               }
-              *py = make_uint4(out[0], out[1], out[2], out[3]);
+            }
+            if (live && c16 * 16 < ovalid) {
+              // y + delta, rounded once, written back over y in the slot.
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int cch = c16 * 2 + h;  // 16-byte chunk of the 128-column block
+                uint4* py = reinterpret_cast<uint4*>(ys + (cch >> 3) * TM * 128 + row * 128 + (((cch & 7) ^ (row & 7)) << 4));
+                const uint4 yv = *py;
+                const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+                uint32_t out[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 yy = make_float2(__uint_as_float(yw[e] << 16), __uint_as_float(yw[e] & 0xFFFF0000u));
+                  const float2 r = add_f32x2(yy, make_float2(d[h * 8 + 2 * e], d[h * 8 + 2 * e + 1]));
+                  out[e] = round_pack_bf16x2(r.x, r.y);
+                }
+                *py = make_uint4(out[0], out[1], out[2], out[3]);
+              }
             }
           }
         }
@@ -830,18 +836,21 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         // This warp's 32 rows x XB / XNH columns to y: eight lanes per row,
         // so each store instruction writes whole 128-byte row segments.
         if (!bad) {
-          constexpr int CPR = XB / XNH / 8;  // 16-byte chunks per row
+          constexpr int CPR = XB / XNH / 8;   // 16-byte chunks per row
+          constexpr int RPI = 32 / CPR;       // rows per store instruction
+          const int cch = hf * CPR + lane % CPR;  // this lane's chunk of the 128-column block
+          const int r0 = q * 32 + lane / CPR;     // this lane's first tile row
+          const uint8_t* sbase = ys + (cch >> 3) * TM * 128;
+          uint4* gp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
+                                               (long long)(t.row0 + r0) * sl.y_row_stride + o0 + cch * 8);
+          const long long gstep = (long long)RPI * sl.y_row_stride / 8;  // uint4 per RPI rows
+          if (cch * 8 < ovalid) {
 #pragma unroll
-          for (int it = 0; it < CPR; ++it) {
-            const int idx = it * 32 + lane;
-            const int tr = q * 32 + idx / CPR;           // tile row
-            const int cch = hf * CPR + idx % CPR;        // chunk of the 128-column block
-            if (tr < t.rows && cch * 8 < ovalid) {
-              const uint4 v = *reinterpret_cast<const uint4*>(ys + (cch >> 3) * TM * 128 + tr * 128 +
-                                                              (((cch & 7) ^ (tr & 7)) << 4));
-              st_global_v4_hint(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
-                                                         (long long)(t.row0 + tr) * sl.y_row_stride + o0 + cch * 8),
-                                v, pol_stream);
+            for (int it = 0; it < CPR; ++it, gp += gstep) {
+              const int tr = r0 + it * RPI;
+              if (tr < t.rows)
+                st_global_v4_hint(gp, *reinterpret_cast<const uint4*>(sbase + tr * 128 + (((cch & 7) ^ (tr & 7)) << 4)),
+                                  pol_stream);
             }
           }
         }

@@ -42,9 +42,12 @@ constexpr int MT = kTileRows;        // token rows per tile
 constexpr int KS = 64;               // input elements per shrink stage
 constexpr int XPITCH = KS * 2 + 16;  // bytes per staged row (padding: conflict-free ldmatrix)
 
-template <int NB>
+// NSO: ring depth override (0: by NB).  A K split of at most 4 stages
+// (64-wide) uses the 4-stage ring: a third of the shared memory, so three
+// CTAs fit on an SM.
+template <int NB, int NSO = 0>
 struct ShrinkCfg {
-  static constexpr int NSTAGE = NB <= 48 ? 8 : (NB <= 64 ? 6 : 4);
+  static constexpr int NSTAGE = NSO ? NSO : (NB <= 48 ? 8 : (NB <= 64 ? 6 : 4));
   static constexpr int STAGE_BYTES = (MT + NB) * XPITCH;
   static constexpr int PPITCH = NB + 4;  // floats per partial row (16-byte aligned rows)
   static constexpr int SMEM = NSTAGE * STAGE_BYTES;
@@ -60,11 +63,11 @@ struct ShrinkCfg {
 // GEN: the problem uses token_rows, slot ranks or a bias.  The plain
 // instantiation compiles none of that bookkeeping (it costs registers and a
 // barrier ahead of the first loads, which decode-sized launches feel).
-template <int NB, bool GEN>
+template <int NB, bool GEN, int NSO>
 __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                float* __restrict__ u, int C,
                                                                int nblk, int Kc, long long plane_stride) {
-  using Cfg = ShrinkCfg<NB>;
+  using Cfg = ShrinkCfg<NB, NSO>;
   constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Tile s_tile;
@@ -513,10 +516,19 @@ int num_sms() {
   return sms[dev];
 }
 
+template <int NB, bool GEN, int NSO>
+cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial);
+
 template <int NB, bool GEN>
 cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
-  auto kernel = sgmv_shrink_bf16_kernel<NB, GEN>;
-  const int smem = ShrinkCfg<NB>::SMEM;
+  if (partial && p.in_dim / apply_splits_for(p) <= 4 * KS) return launch_shrink_ns<NB, GEN, 4>(p, u, s, nblk, partial);
+  return launch_shrink_ns<NB, GEN, 0>(p, u, s, nblk, partial);
+}
+
+template <int NB, bool GEN, int NSO>
+cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
+  auto kernel = sgmv_shrink_bf16_kernel<NB, GEN, NSO>;
+  const int smem = ShrinkCfg<NB, NSO>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);
   if (e != cudaSuccess) return e;
@@ -630,18 +642,19 @@ int apply_splits_for(const ProblemDesc& p) {
 }
 
 int apply_splits(int end, int in_dim, int nR) {
-  // Largest power of two <= 8 (16 for inputs of 8192 and more, whose K
-  // ranges are long) dividing the input stages such that the partial-plane
-  // shrink grid (a lower bound on its tiles: ceil(end / 64)) stays within 256
-  // CTAs.  Depends on shapes only, so the workspace bound can be computed
-  // without a device.
+  // Largest power of two <= 8 dividing the input stages such that the
+  // partial-plane shrink grid (a lower bound on its tiles: ceil(end / 64))
+  // stays within 256 CTAs; up to 16 for inputs of 8192 and more (long K
+  // ranges) and for rank blocks of 48 columns or more (long stage loops).
+  // Depends on shapes only, so the workspace bound can be computed without a
+  // device.
   if (end <= 0 || in_dim % KS != 0) return 1;
   int nblk = 1;
-  (void)pick_nb(nR, &nblk);
+  const int nb = pick_nb(nR, &nblk);
   const long long tiles = (end + MT - 1) / MT;
   const int ksteps = in_dim / KS;
   int C = 1;
-  const int cmax = in_dim >= 8192 ? 16 : 8;
+  const int cmax = (in_dim >= 8192 || nb >= 48) ? 16 : 8;
   while (C < cmax && tiles * nblk * C * 2 <= 256 && ksteps % (C * 2) == 0) C *= 2;
   return C;
 }

@@ -66,7 +66,7 @@ cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_
 int apply_splits(int end, int in_dim, int nR);
 // The split the apply's partial-plane shrink actually uses (and its expand
 // sums): from the group count and CTA occupancy, at most apply_splits(...).
-int apply_splits_for(const ProblemDesc& p);
+int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
 
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
 // nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says

@@ -521,7 +521,9 @@ cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int
 
 template <int NB, bool GEN>
 cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
-  if (partial && p.in_dim / apply_splits_for(p) <= 4 * KS) return launch_shrink_ns<NB, GEN, 4>(p, u, s, nblk, partial);
+  bool short_ring = false;
+  if (partial) (void)apply_splits_for(p, &short_ring);
+  if (short_ring) return launch_shrink_ns<NB, GEN, 4>(p, u, s, nblk, partial);
   return launch_shrink_ns<NB, GEN, 0>(p, u, s, nblk, partial);
 }
 
@@ -618,26 +620,34 @@ bool fast_path_ok(const ProblemDesc& p, const void* u) {
   return true;
 }
 
-int apply_splits_for(const ProblemDesc& p) {
+int apply_splits_for(const ProblemDesc& p, bool* short_ring) {
   // At launch the group count is known: size the split on the upper bound
   // of the tiles (G + end/64) and on how many of these CTAs share an SM, to
-  // about two waves; never above the shape-only bound the workspace holds.
+  // about two waves, never above the shape-only bound the workspace holds.
+  // With the 4-stage ring three times as many CTAs share an SM: it is taken
+  // when that allows more splits, or when a split is at most 4 stages long.
   const int cap = apply_splits(p.end, p.in_dim, p.n_slices * p.R);
   int nblk = 1;
   const int nb = pick_nb(p.n_slices * p.R, &nblk);
-  int smem = ShrinkCfg<128>::SMEM;
+  int smem = ShrinkCfg<128>::SMEM, smem4 = ShrinkCfg<128, 4>::SMEM;
   switch (nb) {
-    case 16: smem = ShrinkCfg<16>::SMEM; break;
-    case 32: smem = ShrinkCfg<32>::SMEM; break;
-    case 48: smem = ShrinkCfg<48>::SMEM; break;
-    case 64: smem = ShrinkCfg<64>::SMEM; break;
-    case 96: smem = ShrinkCfg<96>::SMEM; break;
+    case 16: smem = ShrinkCfg<16>::SMEM; smem4 = ShrinkCfg<16, 4>::SMEM; break;
+    case 32: smem = ShrinkCfg<32>::SMEM; smem4 = ShrinkCfg<32, 4>::SMEM; break;
+    case 48: smem = ShrinkCfg<48>::SMEM; smem4 = ShrinkCfg<48, 4>::SMEM; break;
+    case 64: smem = ShrinkCfg<64>::SMEM; smem4 = ShrinkCfg<64, 4>::SMEM; break;
+    case 96: smem = ShrinkCfg<96>::SMEM; smem4 = ShrinkCfg<96, 4>::SMEM; break;
   }
-  const long long per_sm = std::max(1, (228 * 1024) / (smem + 1024));
   const long long tiles = (long long)p.G + p.end / MT;
   const int ksteps = p.in_dim / KS;
-  int C = 1;
-  while (C < cap && tiles * nblk * C * 2 <= 2LL * num_sms() * per_sm && ksteps % (C * 2) == 0) C *= 2;
+  auto pick = [&](int sm_bytes) {
+    const long long per_sm = std::max(1, (228 * 1024) / (sm_bytes + 1024));
+    int C = 1;
+    while (C < cap && tiles * nblk * C * 2 <= 2LL * num_sms() * per_sm && ksteps % (C * 2) == 0) C *= 2;
+    return C;
+  };
+  const int c8 = pick(smem), c4 = pick(smem4);
+  const int C = c4 > c8 ? c4 : c8;
+  if (short_ring) *short_ring = c4 > c8 || ksteps / C <= 4;
   return C;
 }
 

@@ -365,6 +365,18 @@ def test_long_groups_tensor_core_shrink(R, mode):
     run_case(sy.draw(spec, 8), "o", mode=mode)
 
 
+@pytest.mark.parametrize("groups", [256, 260])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_many_long_groups(groups, mode):
+    """256 long groups fill the persistent tcgen05 expand's cached routing
+    exactly; 260 exceed it (the apply then pairs the tcgen05 shrink with the
+    mma.sync expand).  100 rows per group, rank 64."""
+    spec = _spec(max_num_loras=groups, max_lora_rank=64, rank_choices=(32, 64), kind="fixed",
+                 fixed_slots=tuple(range(groups - 1, -1, -1)) + (-1,), fixed_lens=(100,) * groups + (5,),
+                 hidden=128, n_heads=4, n_kv_heads=4, head_dim=32)
+    run_case(sy.draw(spec, 21), "qkv", mode=mode)
+
+
 def test_all_base_is_noop():
     spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(3, 4))
     dev = run_case(sy.draw(spec, 0), "qkv")

@@ -101,6 +101,8 @@ def lib():
     L.lora_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.lora_status_string.restype = ctypes.c_char_p
     L.lora_status_string.argtypes = [ctypes.c_int]
+    L.lora_selftest_wait_timeout.restype = ctypes.c_int
+    L.lora_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     _lib = L
     return L
 
@@ -344,6 +346,12 @@ def lora_get_device_status(stream=None) -> int:
     _check(L.lora_get_device_status(_stream_handle(stream), ctypes.byref(flags)),
            "lora_get_device_status")
     return int(flags.value)
+
+
+def lora_selftest_wait_timeout(polls: int, stream=None) -> None:
+    """Launch the failure-path self test: a bounded wait that runs out and
+    sets LORA_DEV_TIMEOUT in the device status word (see include/lora_sgmv.h)."""
+    _check(lib().lora_selftest_wait_timeout(int(polls), _stream_handle(stream)), "lora_selftest_wait_timeout")
 
 
 def lora_status_string(status: int) -> str:

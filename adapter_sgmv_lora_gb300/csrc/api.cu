@@ -240,6 +240,12 @@ extern "C" lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* 
   return LORA_OK;
 }
 
+extern "C" lora_status_t lora_selftest_wait_timeout(uint32_t polls, lora_stream_t stream) {
+  unsigned* p = status_ptr();
+  if (!p) return LORA_ERR_CUDA;
+  return cuda_status(launch_selftest_timeout(p, polls, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 extern "C" const char* lora_status_string(lora_status_t status) {
   switch (status) {
     case LORA_OK: return "LORA_OK";

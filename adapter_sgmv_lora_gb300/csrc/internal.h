@@ -50,6 +50,8 @@ cudaError_t launch_shrink_simple(const ProblemDesc& p, float* u, cudaStream_t s)
 cudaError_t launch_expand_simple(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl);
 cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, float scale,
                             const void* A_raw, const void* B_raw, int raw_dtype, cudaStream_t s);
+// Failure-path self test (lora_selftest_wait_timeout).
+cudaError_t launch_selftest_timeout(unsigned* status, uint32_t limit, cudaStream_t s);
 cudaError_t launch_set_bias(const ProblemDesc& p, int slice, int slot, const void* bias_raw, int raw_dtype,
                             cudaStream_t s);
 

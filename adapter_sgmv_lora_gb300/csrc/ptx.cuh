@@ -10,9 +10,12 @@
 
 namespace lora {
 
-// Bounded-wait budget for an mbarrier phase (each try_wait already blocks
-// for a hardware-defined window, so this is seconds of wall time).
-constexpr uint32_t kWaitLimit = 1u << 24;
+// Bounded-wait budget for an mbarrier phase.  A try_wait on a phase that
+// does not complete blocks for a hardware-defined window (measured 3.8 us on
+// this GPU), so 2^18 polls give up after about one second -- far beyond any
+// wait these kernels make (the longest, an expand waiting out its shrink, is
+// milliseconds).
+constexpr uint32_t kWaitLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,6 +55,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for phase `parity` of `bar`; false if the budget ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// mbar_wait with an explicit poll budget.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "tiles.cuh"
 
 namespace lora {
@@ -220,6 +221,23 @@ cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, fl
       set_slot_kernel<float, float><<<g, 256, 0, s>>>(p, slice, slot, r, scale,
                                                        (const float*)A_raw, (const float*)B_raw);
   }
+  return cudaGetLastError();
+}
+
+// Failure-path self test: one thread waits on a fresh barrier that nothing
+// ever completes, gives up after `limit` polls and records the timeout in the
+// status word, exactly as the pipelined kernels do when a wait expires.
+__global__ void selftest_timeout_kernel(unsigned* status, uint32_t limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_limit(&bar, 0, limit)) atomicOr(status, LORA_DEV_TIMEOUT);
+  }
+}
+
+cudaError_t launch_selftest_timeout(unsigned* status, uint32_t limit, cudaStream_t s) {
+  selftest_timeout_kernel<<<1, 32, 0, s>>>(status, limit);
   return cudaGetLastError();
 }
 

@@ -63,7 +63,7 @@ typedef enum { LORA_DTYPE_F32 = 0, LORA_DTYPE_BF16 = 1 } lora_dtype_t;
 #define LORA_DEV_BAD_SLOT 1u     /* lora_ids[g] outside [0, max_num_loras) */
 #define LORA_DEV_BAD_OFFSETS 2u  /* grouped_offsets[0] != 0 or a decreasing offset */
 #define LORA_DEV_BAD_END 4u      /* grouped_offsets[num_groups] != end */
-#define LORA_DEV_TIMEOUT 8u      /* a kernel gave up waiting for its own copies */
+#define LORA_DEV_TIMEOUT 8u      /* a kernel gave up (after ~1 s) waiting for its own copies */
 #define LORA_DEV_BAD_ROW 16u     /* a token_rows entry outside [0, num_tokens) */
 
 #define LORA_MAX_SLICES 3
@@ -299,6 +299,17 @@ lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem, const lora_
  * synchronization or copy fails.
  */
 lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* flags);
+
+/*
+ * lora_selftest_wait_timeout -- exercises the failure path of the pipelined
+ * kernels without faulting the GPU (no counterpart on the pages).  One thread
+ * waits on a fresh shared-memory barrier that nothing completes, gives up
+ * after `polls` polls of mbarrier.try_wait (bounded), sets LORA_DEV_TIMEOUT
+ * in the device status word and exits; the context stays usable.  Read the
+ * flag with lora_get_device_status.  Returns LORA_ERR_CUDA if the launch
+ * fails.
+ */
+lora_status_t lora_selftest_wait_timeout(uint32_t polls, lora_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* lora_status_string(lora_status_t status);

@@ -377,6 +377,22 @@ def test_many_long_groups(groups, mode):
     run_case(sy.draw(spec, 21), "qkv", mode=mode)
 
 
+def test_wait_timeout_is_reported_and_context_survives():
+    """A bounded wait that runs out (a barrier nothing completes) sets
+    LORA_DEV_TIMEOUT, no fault; afterwards the context still computes."""
+    lk = _lk()
+    assert lk.lora_get_device_status() == 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    lk.lora_selftest_wait_timeout(1 << 12)
+    t1.record()
+    torch.cuda.synchronize()
+    assert lk.lora_get_device_status() == 8  # LORA_DEV_TIMEOUT, read and cleared
+    assert lk.lora_get_device_status() == 0
+    assert t0.elapsed_time(t1) < 5000.0
+    run_case(sy.draw("tiny", 0), "qkv")
+
+
 def test_all_base_is_noop():
     spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(3, 4))
     dev = run_case(sy.draw(spec, 0), "qkv")

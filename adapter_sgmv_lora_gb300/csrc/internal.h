@@ -55,7 +55,8 @@ cudaError_t launch_selftest_timeout(unsigned* status, uint32_t limit, cudaStream
 cudaError_t launch_set_bias(const ProblemDesc& p, int slice, int slot, const void* bias_raw, int raw_dtype,
                             cudaStream_t s);
 
-// bf16 fast path (tensor cores + bulk copies + clusters).  `fast_path_ok`
+// bf16 fast path (mma.sync tensor cores, 16-byte async copies, clusters for
+// lora_shrink's reduction).  `fast_path_ok`
 // tells whether a problem meets its alignment / size preconditions.
 bool fast_path_ok(const ProblemDesc& p, const void* u);
 // launch_shrink_bf16 writes the final u (cluster reduction);
@@ -64,10 +65,12 @@ bool fast_path_ok(const ProblemDesc& p, const void* u);
 cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
 cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
 cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit);
-// Partial planes the apply's shrink uses for this shape (1..8); shapes only.
+// Upper bound on the partial planes the apply's shrink uses for this shape
+// (1..16); shapes only (it sizes the workspace).
 int apply_splits(int end, int in_dim, int nR);
 // The split the apply's partial-plane shrink actually uses (and its expand
-// sums): from the group count and CTA occupancy, at most apply_splits(...).
+// sums): from the group count and CTA occupancy, at most apply_splits(...);
+// *short_ring tells whether the shrink runs its 4-stage ring.
 int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
 
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes

@@ -7,20 +7,21 @@
 // "max.pipelines.lora.LoRAManagerV3" page, get_lora_graph_inputs).
 //
 // Work decomposition.  The routed rows are cut into 64-row tiles per group
-// (tiles.cuh).  The shrink gives each (tile, rank-column block) to a
-// thread-block cluster of C CTAs that split the input dimension; every CTA
-// streams its K range of the tile's x rows and of the slot's A rows into
-// shared memory through a multistage ring of 16-byte asynchronous copies
-// issued by all threads (exactly the group's own rows: nothing outside the
-// group is fetched), and multiplies on the tensor cores (mma.sync m16n8k16,
-// fp32 accumulate).  The C partial tiles are summed through distributed
-// shared memory in a fixed order (deterministic) and written once to u.  The
-// expand gives each (tile, slice, output block) to one CTA: it starts the
-// loads of the y block and of the slot's B block, waits (programmatic
-// dependent launch) for the shrink grid, loads u, splits it into hi + lo
-// bf16 terms, multiplies with the y block as the initial accumulator, rounds
-// once and writes exactly the routed rows back with 16-byte stores.  Rows at
-// or past `end` are never read or written.
+// (tiles.cuh).  The shrink gives each (tile, rank-column block, K split) to
+// one CTA; every CTA streams its K range of the tile's x rows and of the
+// slot's A rows into shared memory through a ring of 16-byte asynchronous
+// copies issued by all threads (exactly the group's own rows: nothing outside
+// the group is fetched), and multiplies on the tensor cores (mma.sync
+// m16n8k16, fp32 accumulate).  In the apply each K split writes its partial
+// tile into its own plane of u and the expand sums the planes in plane order;
+// for lora_shrink the K splits form a thread-block cluster and sum through
+// distributed shared memory in rank order (both deterministic).  The expand
+// gives each (tile of 64 or 32 rows, slice, output block) to one CTA: it
+// starts the loads of the y block and of the slot's B block, waits
+// (programmatic dependent launch) for the shrink grid, loads u, splits it
+// into hi + lo bf16 terms, multiplies with the y block as the initial
+// accumulator, rounds once and writes exactly the routed rows back with
+// 16-byte stores.  Rows at or past `end` are never read or written.
 //
 // Row gathers use per-thread 16-byte copies rather than one bulk (TMA)
 // request per row: a tile is tens of short row segments, and per-request

@@ -5,17 +5,23 @@
 // ("vLLM LoRA 实现深度解析" sections 1 and 6; routing triple of the
 // "max.pipelines.lora.LoRAManagerV3" page, get_lora_graph_inputs).
 //
-// One CTA per (128-row tile of a group, K split).  Warp-specialised:
+// Shrink: one CTA per (128-row tile of a group, column part, K split).
+// Warp-specialised:
 //   warp 0  TMA producer: per 64-wide K stage, one box of the tile's x rows
-//           (128 x 64) and one box per slice of the slot's A rows (R x 64),
-//           both with the 128-byte swizzle, into a ring of stages;
-//   warp 1  TMEM owner and MMA issuer: tcgen05.mma M=128, N=n*R (two MMAs of
-//           N/2 when n*R > 256), K=16 per instruction, accumulating in TMEM;
-//           a tcgen05.commit per stage hands the slot back to the producer;
+//           (128 x 64) and the slot's A rows of the CTA's columns (R-row,
+//           64-row or 16-row boxes), 128-byte swizzle, into a ring of stages;
+//   warp 1  TMEM owner and MMA issuer: tcgen05.mma M=128, N = the CTA's
+//           columns (two MMAs of N/2 when N > 256), K=16 per instruction,
+//           accumulating in TMEM; a tcgen05.commit per stage hands the slot
+//           back to the producer;
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= rows) and
-//           16-byte stores of the routed rows of u (partial plane per split).
+//           stores of u: fp32 rows (a K split's plane), or for the apply on
+//           ranks 64/128 the packed intermediate (bf16 hi + lo in the
+//           expand's swizzled operand layout, see pack_u16).
+// Expand (further down): persistent, one CTA per SM over (tile, slice,
+// 128-column block) units, TMEM accumulators, 8 epilogue warps.
 // Rows of the 128-row box past the group (other groups, base rows, or past
-// the tensor: zero-filled) are read but their u rows are never stored.
+// the tensor: zero-filled) are read but their u / y rows are never stored.
 // Every mbarrier wait is bounded; on expiry the CTA records LORA_DEV_TIMEOUT,
 // skips its stores and still releases its TMEM.
 #include <cuda.h>

@@ -366,41 +366,78 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
 
   pdl_wait();  // the shrink grid (if any) has finished and its u is visible
 
-  // u (sum of the nsplit planes, in plane order) -> hi + lo bf16: u = hi + lo
-  // to 16 significant bits; the subtraction is exact.  Read through L2 only.
+  // u (sum of the nsplit planes) -> hi + lo bf16: u = hi + lo to 16
+  // significant bits; the subtraction is exact.  Read through L2 only.  The
+  // planes are dependent L2 round trips, so a thread keeps up to 8 float4
+  // loads in flight across its items (plane-major, each item summed in plane
+  // order).  Where a tile has fewer float4 items than threads (R = 16 with
+  // 32-row tiles), two threads share an item: one sums the first half of the
+  // planes, the other the second, and the halves meet in shared memory.
   {
     constexpr int R4 = R / 4;
+    constexpr int ITEMS = MR * R4;                     // float4 items of a full tile's u
+    constexpr int TPI = ITEMS < 256 ? 256 / ITEMS : 1;  // threads sharing an item
+    constexpr int IPT = ITEMS > 256 ? ITEMS / 256 : 1;  // items per thread
+    constexpr int PB = IPT < 8 ? 8 / IPT : 1;          // planes per round
+    static_assert(TPI <= 2, "plane halves");
+    __shared__ float4 s_uhalf[TPI > 1 ? ITEMS : 1];
     const float* ub = u + (long long)t.row0 * nR + (long long)j * R;
-    for (int e = threadIdx.x; e < t.rows * R4; e += blockDim.x) {
-      const int r = e / R4, k = (e % R4) * 4;
-      const float* src = ub + (long long)r * nR + k;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      // Planes in order, eight loads in flight per batch (one batch for up
-      // to 8 planes).
-      for (int q0 = 0; q0 < map.nsplit; q0 += 8) {
-        float4 part[8];
+    const int sub = TPI > 1 ? (int)threadIdx.x / ITEMS : 0;
+    const int e0 = TPI > 1 ? (int)threadIdx.x % ITEMS : (int)threadIdx.x;
+    const int share = (map.nsplit + TPI - 1) / TPI;
+    const int q_lo = sub * share, q_hi = min(map.nsplit, q_lo + share);
+    float4 v[IPT];
+    const float* src[IPT];
+    bool live[IPT];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q0 + q < map.nsplit) part[q] = __ldcg(reinterpret_cast<const float4*>(src + (q0 + q) * map.plane_stride));
+    for (int i = 0; i < IPT; ++i) {
+      const int e = e0 + i * 256, r = e / R4, k = (e % R4) * 4;
+      live[i] = r < t.rows;
+      src[i] = ub + (long long)r * nR + k;
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int q0 = q_lo; q0 < q_hi; q0 += PB) {
+      float4 part[IPT][PB];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q0 + q < map.nsplit) {
-            if (q0 + q == 0) {
-              v = part[0];
-            } else {
-              v.x += part[q].x;
-              v.y += part[q].y;
-              v.z += part[q].z;
-              v.w += part[q].w;
-            }
+      for (int q = 0; q < PB; ++q)
+#pragma unroll
+        for (int i = 0; i < IPT; ++i)
+          if (live[i] && q0 + q < q_hi)
+            part[i][q] = __ldcg(reinterpret_cast<const float4*>(src[i] + (q0 + q) * map.plane_stride));
+#pragma unroll
+      for (int q = 0; q < PB; ++q)
+#pragma unroll
+        for (int i = 0; i < IPT; ++i)
+          if (live[i] && q0 + q < q_hi) {
+            v[i].x += part[i][q].x;
+            v[i].y += part[i][q].y;
+            v[i].z += part[i][q].z;
+            v[i].w += part[i][q].w;
           }
+    }
+    if constexpr (TPI > 1) {
+      if (sub == 1) s_uhalf[e0] = v[0];
+      __syncthreads();
+      if (sub == 0) {
+        const float4 w = s_uhalf[e0];
+        v[0].x += w.x;
+        v[0].y += w.y;
+        v[0].z += w.z;
+        v[0].w += w.w;
       }
-      __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
-      uint32_t hi[2], lo[2];
-      split_hi_lo_bf16x2(v.x, v.y, hi[0], lo[0]);
-      split_hi_lo_bf16x2(v.z, v.w, hi[1], lo[1]);
-      *reinterpret_cast<uint2*>(hrow + k) = make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(hrow + R + k) = make_uint2(lo[0], lo[1]);
+    }
+    if (sub == 0) {
+#pragma unroll
+      for (int i = 0; i < IPT; ++i) {
+        if (!live[i]) continue;
+        const int e = e0 + i * 256, r = e / R4, k = (e % R4) * 4;
+        __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(Hs + r * Cfg::UPITCH);
+        uint32_t hi[2], lo[2];
+        split_hi_lo_bf16x2(v[i].x, v[i].y, hi[0], lo[0]);
+        split_hi_lo_bf16x2(v[i].z, v[i].w, hi[1], lo[1]);
+        *reinterpret_cast<uint2*>(hrow + k) = make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2*>(hrow + R + k) = make_uint2(lo[0], lo[1]);
+      }
     }
   }
   cp_async_wait<0>();

@@ -244,13 +244,13 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
       v = *reinterpret_cast<const float4*>(&P[r * Cfg::PPITCH + c]);
     } else {
       const uint32_t la = smem_addr(&P[r * Cfg::PPITCH + c]);
-      float4 part[8];
+      float4 part[16];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < 16; ++q)
         if (q < C) part[q] = ld_shared_cluster_f32x4(map_shared_rank(la, (uint32_t)q));
       v = part[0];
 #pragma unroll
-      for (int q = 1; q < 8; ++q)
+      for (int q = 1; q < 16; ++q)
         if (q < C) {
           v.x += part[q].x;
           v.y += part[q].y;
@@ -554,13 +554,28 @@ int num_sms() {
   return sms[dev];
 }
 
+// lora_shrink's cluster size: the input dimension is split over up to 16
+// CTAs while the grid stays within two CTAs per SM (decode-sized launches
+// have few tiles, and shorter K ranges per CTA put more loads in flight).
+static int cluster_splits(const ProblemDesc& p, int nblk) {
+  const long long tiles = (long long)p.G + p.end / MT;
+  const int ksteps = p.in_dim / KS;
+  const long long target = 2LL * num_sms();
+  int C = 1;
+  while (C < 16 && tiles * nblk * C * 2 <= target && ksteps % (C * 2) == 0) C *= 2;
+  return C;
+}
+
 template <int NB, bool GEN, int NSO>
 cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial);
 
 template <int NB, bool GEN>
 cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
   bool short_ring = false;
-  if (partial) (void)apply_splits_for(p, &short_ring);
+  if (partial)
+    (void)apply_splits_for(p, &short_ring);
+  else
+    short_ring = cluster_splits(p, nblk) == 16;  // smaller CTAs: a 16-CTA cluster packs into a GPC
   if (short_ring) return launch_shrink_ns<NB, GEN, 4>(p, u, s, nblk, partial);
   return launch_shrink_ns<NB, GEN, 0>(p, u, s, nblk, partial);
 }
@@ -579,10 +594,38 @@ cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int
     C = apply_splits_for(p);
     if (C > 1) plane_stride = (long long)p.end * p.n_slices * p.R;
   } else {
-    // Split the input dimension over a cluster until the grid covers the GPU.
-    const int ksteps = p.in_dim / KS;
-    const long long target = 2LL * num_sms();
-    while (C < 8 && tiles * nblk * C * 2 <= target && ksteps % (C * 2) == 0) C *= 2;
+    C = cluster_splits(p, nblk);
+    if (C == 16) {
+      // 16 CTAs per cluster is beyond the portable 8: opt in, and fall back
+      // to 8 if a cluster of this kernel cannot be placed.
+      static unsigned long long big_ok = 0, big_no = 0;
+      int dev = 0;
+      e = cudaGetDevice(&dev);
+      if (e != cudaSuccess) return e;
+      const unsigned long long bit = 1ull << (dev & 63);
+      std::lock_guard<std::mutex> lk(g_attr_mu);
+      if (!((big_ok | big_no) & bit)) {
+        int clusters = 0;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(16);
+        q.blockDim = dim3(128);
+        q.dynamicSmemBytes = smem;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = 16;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        q.attrs = a;
+        q.numAttrs = 1;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            cudaOccupancyMaxActiveClusters(&clusters, kernel, &q) == cudaSuccess && clusters > 0)
+          big_ok |= bit;
+        else
+          big_no |= bit;
+        (void)cudaGetLastError();  // a refused query leaves no sticky error
+      }
+      if (big_no & bit) C = 8;
+    }
   }
   const int Kc = p.in_dim / C;
   cudaLaunchConfig_t cfg = {};

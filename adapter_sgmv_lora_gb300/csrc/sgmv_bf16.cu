@@ -780,12 +780,21 @@ template <bool GEN>
 static cudaError_t dispatch_expand_g(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
   // Short groups (at most 32 routed rows each on average): 32-row tiles twice
   // as wide, so a tile's fixed costs (routing lookup, u, B block) cover twice
-  // the outputs and the grid has half the CTAs.
+  // the outputs and the grid has half the CTAs -- unless that leaves fewer
+  // than two CTAs per SM (decode-sized batches: o_proj's 4096 columns, fused
+  // qkv's 6144), where 256-wide blocks give twice the CTAs, each with half the
+  // y and B to load, and more loads in flight per SM.
   const bool short_groups = (long long)p.end <= 32LL * p.G;
   switch (p.R) {
     case 16:
-      return short_groups ? launch_expand_r<16, 512, 32, GEN>(p, u, s, pdl, nsplit)
-                          : launch_expand_r<16, 256, 64, GEN>(p, u, s, pdl, nsplit);
+      if (short_groups) {
+        long long blocks = 0;
+        for (int j = 0; j < p.n_slices; ++j) blocks += (p.sl[j].out_dim + 511) / 512;
+        const long long tiles = (long long)p.G + p.end / 32;
+        return tiles * blocks < 2LL * num_sms() ? launch_expand_r<16, 256, 32, GEN>(p, u, s, pdl, nsplit)
+                                                : launch_expand_r<16, 512, 32, GEN>(p, u, s, pdl, nsplit);
+      }
+      return launch_expand_r<16, 256, 64, GEN>(p, u, s, pdl, nsplit);
     case 32: return launch_expand_r<32, 256, 64, GEN>(p, u, s, pdl, nsplit);
     case 64: return launch_expand_r<64, 128, 64, GEN>(p, u, s, pdl, nsplit);
     default: return launch_expand_r<128, 64, 64, GEN>(p, u, s, pdl, nsplit);

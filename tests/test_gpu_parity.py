@@ -331,15 +331,29 @@ def test_rank_variants_ragged_tiles(R, mode):
 @pytest.mark.parametrize("mode", ["apply", "split"])
 @pytest.mark.parametrize("ranks", [False, True])
 def test_short_groups_wide_expand_tiles(mode, ranks):
-    """Groups of at most 32 rows on average take the expand's 32-row x
-    512-column tiles: lengths 1, 31, 32, 33, 40, 3, 8 and 0 (tiles of 32 with
-    ragged ends), slices narrower than one 512-column block; also with the
-    true ranks passed (the general kernels)."""
+    """Groups of at most 32 rows on average take the expand's 32-row tiles,
+    here 256 columns wide (a small grid): lengths 1, 31, 32, 33, 40, 3, 8 and
+    0 (tiles of 32 with ragged ends), slices narrower than one block; also
+    with the true ranks passed (the general kernels)."""
     spec = _spec(max_num_loras=8, max_lora_rank=16, rank_choices=(8, 16), kind="fixed",
                  fixed_slots=(7, 6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 31, 32, 33, 40, 3, 8, 0, 6),
                  hidden=1024, n_heads=16, n_kv_heads=4, head_dim=64)
     run_case(sy.draw(spec, 11), "qkv", mode=mode, slot_ranks=ranks, poison=ranks)
     run_case(sy.draw(spec, 12), "o", mode=mode, slot_ranks=ranks, poison=ranks)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+@pytest.mark.parametrize("ranks", [False, True])
+def test_short_groups_wide_outputs(mode, ranks):
+    """Short groups with outputs wide enough (gate + up of 2 x 8192 columns)
+    that 32-row x 512-column expand tiles already give two CTAs per SM; the
+    down projection (1024 columns) takes the 256-column tiles.  Same ragged
+    lengths as above; plain and general kernels."""
+    spec = _spec(family="mlp", intermediate=8192, max_num_loras=8, max_lora_rank=16, rank_choices=(8, 16),
+                 kind="fixed", fixed_slots=(7, 6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 31, 32, 33, 40, 3, 8, 0, 6),
+                 hidden=1024)
+    run_case(sy.draw(spec, 13), "gateup", mode=mode, slot_ranks=ranks, poison=ranks)
+    run_case(sy.draw(spec, 14), "down", mode=mode, slot_ranks=ranks, poison=ranks)
 
 
 @pytest.mark.parametrize("R", [16, 32])

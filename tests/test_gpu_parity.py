@@ -356,6 +356,17 @@ def test_short_groups_wide_outputs(mode, ranks):
     run_case(sy.draw(spec, 14), "down", mode=mode, slot_ranks=ranks, poison=ranks)
 
 
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_short_groups_many_adapters_wide_outputs(mode):
+    """40 adapters, 300 one-token requests, gate + up of 2 x 4096 columns: a
+    grid of several waves of 32 x 512 expand tiles over many small groups,
+    checked on every routed row."""
+    spec = _spec(family="mlp", intermediate=4096, hidden=512, max_num_loras=40, max_lora_rank=16,
+                 rank_choices=(8, 16), n_requests=300, base_prob=0.1)
+    for seed in (21, 22):
+        run_case(sy.draw(spec, seed), "gateup", mode=mode)
+
+
 @pytest.mark.parametrize("R", [16, 32])
 def test_apply_split_planes_ragged_groups(R):
     """The apply's shrink splits K into partial planes for small batches;

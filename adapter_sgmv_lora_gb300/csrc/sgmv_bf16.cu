@@ -726,7 +726,15 @@ int apply_splits_for(const ProblemDesc& p, bool* short_ring) {
     while (C < cap && tiles * nblk * C * 2 <= 2LL * num_sms() * per_sm && ksteps % (C * 2) == 0) C *= 2;
     return C;
   };
-  const int c8 = pick(smem), c4 = pick(smem4);
+  int c8 = pick(smem), c4 = pick(smem4);
+  // A single rank-16 block over an input below 8192 goes past 8 splits only
+  // while 8 would leave SMs without a CTA (decode-sized batches: o_proj apply
+  // 7.07 -> 6.69 us); with more tiles the extra planes cost the expand more
+  // than the shorter K ranges save (many64's o_proj 17.6 -> 17.9 us).
+  if (nb == 16 && p.in_dim < 8192 && tiles * nblk * 8 >= num_sms()) {
+    c8 = std::min(c8, 8);
+    c4 = std::min(c4, 8);
+  }
   const int C = c4 > c8 ? c4 : c8;
   if (short_ring) *short_ring = c4 > c8 || ksteps / C <= 4;
   return C;
@@ -736,7 +744,8 @@ int apply_splits(int end, int in_dim, int nR) {
   // Largest power of two <= 8 dividing the input stages such that the
   // partial-plane shrink grid (a lower bound on its tiles: ceil(end / 64))
   // stays within 256 CTAs; up to 16 for inputs of 8192 and more (long K
-  // ranges) and for rank blocks of 48 columns or more (long stage loops).
+  // ranges), for rank blocks of 48 columns or more (long stage loops) and for
+  // a single 16-column block (decode-sized o_proj grids).
   // Depends on shapes only, so the workspace bound can be computed without a
   // device.
   if (end <= 0 || in_dim % KS != 0) return 1;
@@ -745,7 +754,7 @@ int apply_splits(int end, int in_dim, int nR) {
   const long long tiles = (end + MT - 1) / MT;
   const int ksteps = in_dim / KS;
   int C = 1;
-  const int cmax = (in_dim >= 8192 || nb >= 48) ? 16 : 8;
+  const int cmax = (in_dim >= 8192 || nb >= 48 || nb == 16) ? 16 : 8;
   while (C < cmax && tiles * nblk * C * 2 <= 256 && ksteps % (C * 2) == 0) C *= 2;
   return C;
 }

@@ -270,7 +270,15 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
 template <int R, int OB, int MR>
 struct ExpandCfg {
   static constexpr int YPITCH = OB * 2 + 16;  // bytes per staged y row
-  static constexpr int BPITCH = R * 2 + 16;   // bytes per staged B row (conflict-free ldmatrix)
+  // Bytes per staged B row.  Rank 16: 32 bytes, unpadded, with the two
+  // 16-byte chunks of a row swapped when bit 2 of the row is set (rows r and
+  // r + 4 would share banks otherwise); the 8 rows of an ldmatrix phase then
+  // hit 8 different bank groups.  Higher ranks: padded by 16 bytes.
+  static constexpr bool BSWZ = R == 16;
+  static constexpr int BPITCH = BSWZ ? 32 : R * 2 + 16;
+  __device__ static constexpr int b_off(int o, int ch) {
+    return o * BPITCH + (BSWZ ? (ch ^ ((o >> 2) & 1)) : ch) * 16;
+  }
   static constexpr int UPITCH = 4 * R + 16;   // bytes per hi|lo row (2R bf16)
   static constexpr int Y_OFF = 0;
   static constexpr int B_OFF = MR * YPITCH;
@@ -291,9 +299,8 @@ struct ExpandMap {
 
 // GEN as for the shrink: token_rows, slot ranks or a bias in use.
 template <int R, int OB, int MR, bool GEN>
-__global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
-                                                               const float* __restrict__ u,
-                                                               const __grid_constant__ ExpandMap map) {
+__device__ __forceinline__ void expand_bf16_body(const ProblemDesc& p, const float* __restrict__ u,
+                                                 const ExpandMap& map) {
   using Cfg = ExpandCfg<R, OB, MR>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Tile s_tile;
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
   const int kmax = GEN ? slot_kmax(p, t.slot) : R;  // B columns past this are not read
   for (int c = threadIdx.x; c < ovalid * BW; c += blockDim.x) {
     const int o = c / BW, ch = c % BW;
-    if (!GEN || ch * 8 < kmax) cp_async16(Bs + o * Cfg::BPITCH + ch * 16, bg + (long long)o * R + ch * 8);
+    if (!GEN || ch * 8 < kmax) cp_async16(Bs + Cfg::b_off(o, ch), bg + (long long)o * R + ch * 8);
   }
   cp_async_commit();
 
@@ -481,7 +488,7 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
         uint32_t b0, b1, b2, b3;
         const int nrow = nh * Cfg::CW + np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int kcol = kb + ((lane >> 3) & 1) * 8;
-        ldsm_x4(bs + nrow * Cfg::BPITCH + kcol * 2, b0, b1, b2, b3);
+        ldsm_x4(bs + Cfg::b_off(nrow, kcol / 8), b0, b1, b2, b3);
         mma_bf16_16816(acc[2 * np], a, b0, b1);
         mma_bf16_16816(acc[2 * np + 1], a, b2, b3);
       }
@@ -504,6 +511,21 @@ __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_cons
           *reinterpret_cast<const uint4*>(Ys + r * Cfg::YPITCH + ch * 16);
   }
   pdl_launch_dependents();  // the next kernel may launch; it waits for this grid to finish
+}
+
+template <int R, int OB, int MR, bool GEN>
+__global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
+                                                               const float* __restrict__ u,
+                                                               const __grid_constant__ ExpandMap map) {
+  expand_bf16_body<R, OB, MR, GEN>(p, u, map);
+}
+
+// The plain 32 x 512 rank-16 tile (short groups over wide outputs, grids of
+// several waves) held to 64 registers, so four CTAs share an SM.
+__global__ void __launch_bounds__(256, 4) sgmv_expand_bf16_w4_kernel(const __grid_constant__ ProblemDesc p,
+                                                                     const float* __restrict__ u,
+                                                                     const __grid_constant__ ExpandMap map) {
+  expand_bf16_body<16, 512, 32, false>(p, u, map);
 }
 
 // ------------------------------------------------------------------ host
@@ -653,6 +675,7 @@ cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int
 template <int R, int OB, int MR, bool GEN>
 cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
   auto kernel = sgmv_expand_bf16_kernel<R, OB, MR, GEN>;
+  if constexpr (R == 16 && OB == 512 && MR == 32 && !GEN) kernel = sgmv_expand_bf16_w4_kernel;
   const int smem = ExpandCfg<R, OB, MR>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);

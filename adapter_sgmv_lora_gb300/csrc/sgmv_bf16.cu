@@ -14,14 +14,17 @@
 // the group is fetched), and multiplies on the tensor cores (mma.sync
 // m16n8k16, fp32 accumulate).  In the apply each K split writes its partial
 // tile into its own plane of u and the expand sums the planes in plane order;
-// for lora_shrink the K splits form a thread-block cluster and sum through
-// distributed shared memory in rank order (both deterministic).  The expand
-// gives each (tile of 64 or 32 rows, slice, output block) to one CTA: it
-// starts the loads of the y block and of the slot's B block, waits
-// (programmatic dependent launch) for the shrink grid, loads u, splits it
-// into hi + lo bf16 terms, multiplies with the y block as the initial
-// accumulator, rounds once and writes exactly the routed rows back with
-// 16-byte stores.  Rows at or past `end` are never read or written.
+// for lora_shrink the K splits form a thread-block cluster (up to 16 CTAs)
+// and sum through distributed shared memory in rank order (both
+// deterministic).  The expand gives each (tile of 64 or 32 rows, slice,
+// output block of 64..512 columns) to one CTA: it starts the loads of the y
+// block and of the slot's B block, waits (programmatic dependent launch) for
+// the shrink grid, sums the u planes, splits u into hi + lo bf16 terms,
+// multiplies with the y block as the initial accumulator, rounds once and
+// writes exactly the routed rows back with 16-byte stores.  Rows at or past
+// `end` are never read or written.  Rank-16 B blocks are staged unpadded with
+// swizzled 16-byte chunks; the plain 32 x 512 rank-16 tile has its own
+// kernel held to four CTAs per SM.
 //
 // Row gathers use per-thread 16-byte copies rather than one bulk (TMA)
 // request per row: a tile is tens of short row segments, and per-request

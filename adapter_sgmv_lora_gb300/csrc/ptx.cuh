@@ -78,16 +78,6 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
-// Shared -> global bulk store, tracked by the issuing thread's bulk group.
-__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
-               "r"(smem_addr(smem_src)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 // Make generic-proxy shared-memory writes visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -114,12 +104,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-
 // D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0,
                                                uint32_t b1) {
@@ -131,12 +115,6 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
 }
 
 // ------------------------------------------------- clusters / DSMEM / PDL
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -152,11 +130,6 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local_addr, uint32_
 // Remote shared-memory loads.  Volatile (kept in order after the cluster
 // barrier) but without a memory clobber, so a run of them issues back to
 // back and their latencies overlap.
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -171,11 +144,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_barrier_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 // Two fp32 additions in one packed instruction (each lane rounds to nearest
 // like a scalar add).
@@ -192,7 +160,7 @@ __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
 }
 
 // Two floats rounded to nearest-even bf16 in one conversion, `lo` in the
-// low half (same bits as pack_bf16x2 of two separate roundings).
+// low half (the same bits as two separate roundings, packed).
 __device__ __forceinline__ uint32_t round_pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -205,32 +173,7 @@ __device__ __forceinline__ void split_hi_lo_bf16x2(float a, float b, uint32_t& h
   lo = round_pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
-}
-
 // ------------------------------------------------ TMA tensor copies (tiled)
-// Box load described by a tensor map (a __grid_constant__ kernel parameter);
-// completion counted in bytes on `bar`.  The innermost coordinate times the
-// element size must be a multiple of 16 bytes.
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int c0, int c1,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4}], [%2];" ::"r"(smem_addr(smem_dst)),
-      "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int c0, int c1, int c2,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4, %5}], [%2];" ::"r"(smem_addr(smem_dst)),
-      "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // L2 cache policies for TMA and stores: streamed data first out, reused
 // weights last out.
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -243,6 +186,10 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// Box load described by a tensor map (a __grid_constant__ kernel parameter)
+// under an L2 cache policy; completion counted in bytes on `bar`.  The
+// innermost coordinate times the element size must be a multiple of 16
+// bytes.
 __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* tmap, int c0, int c1, uint64_t* bar,
                                                  uint64_t policy) {
   asm volatile(

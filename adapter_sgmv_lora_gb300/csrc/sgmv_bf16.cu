@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
     }
   }
   __syncthreads();
-  if (!s_ok) return;  // the whole cluster sees the same tile and verdict
+  if (!s_ok) return;  // the whole cluster sees the same tile and the same outcome
   const Tile t = s_tile;
 
   const int R = p.R;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   (void)warp;
 
   // Every CTA of the tile (and of its cluster) checks all of the tile's rows
-  // and reaches the same verdict.
+  // and reaches the same outcome.
   if (GEN && __syncthreads_or(bad_row)) {
     if (threadIdx.x == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
     return;

@@ -5,7 +5,7 @@
 // lora_ids[g] ("max.pipelines.lora.LoRAManagerV3", get_lora_graph_inputs).
 // Each group is cut into ceil(len / tile_rows) tiles; tiles are numbered
 // group by group.  Every CTA scans the whole (small: G <= max_num_loras)
-// triple, so every CTA of a launch reaches the same verdict on validity and
+// triple, so every CTA of a launch reaches the same outcome on validity and
 // an invalid triple makes the whole launch skip its work.
 #pragma once
 

@@ -36,6 +36,18 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, n), n
 
 
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without liblora_sgmv.so every call raises: there is no CPU fallback."""
+    monkeypatch.setattr(lk, "_lib", None)
+    monkeypatch.setattr(lk, "LIB_PATH", str(tmp_path / "liblora_sgmv.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        lk.lora_build_routing([0, 1], [1, 1], 2)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        lk.lora_status_string(0)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        lk.lib()
+
+
 def test_status_strings():
     for code, name in lk.STATUS_NAMES.items():
         assert lk.lora_status_string(code).startswith(name)

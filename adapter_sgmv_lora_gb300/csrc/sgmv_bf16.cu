@@ -675,10 +675,18 @@ cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int
   return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride);
 }
 
+// The kernel of an expand tile shape (only the one that runs is instantiated).
+template <int R, int OB, int MR, bool GEN>
+constexpr auto expand_kernel() {
+  if constexpr (R == 16 && OB == 512 && MR == 32 && !GEN)
+    return &sgmv_expand_bf16_w4_kernel;
+  else
+    return &sgmv_expand_bf16_kernel<R, OB, MR, GEN>;
+}
+
 template <int R, int OB, int MR, bool GEN>
 cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
-  auto kernel = sgmv_expand_bf16_kernel<R, OB, MR, GEN>;
-  if constexpr (R == 16 && OB == 512 && MR == 32 && !GEN) kernel = sgmv_expand_bf16_w4_kernel;
+  auto kernel = expand_kernel<R, OB, MR, GEN>();
   const int smem = ExpandCfg<R, OB, MR>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);

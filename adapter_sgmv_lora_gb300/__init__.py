@@ -9,7 +9,7 @@ library cannot be loaded, every call raises.
 Names follow the C ABI: ``lora_build_routing``, ``lora_set_slot``,
 ``lora_shrink``, ``lora_expand``, ``lora_workspace_bytes``,
 ``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_get_device_status``,
-``lora_status_string``.
+``lora_last_call_path``, ``lora_status_string``.
 """
 from __future__ import annotations
 
@@ -27,9 +27,14 @@ LORA_OK = 0
 STATUS_NAMES = {0: "LORA_OK", 1: "LORA_ERR_NULL", 2: "LORA_ERR_SHAPE", 3: "LORA_ERR_RANK",
                 4: "LORA_ERR_SLOT_RANGE", 5: "LORA_ERR_ROUTING", 6: "LORA_ERR_DTYPE",
                 7: "LORA_ERR_ALIGN", 8: "LORA_ERR_WORKSPACE", 9: "LORA_ERR_CUDA",
-                10: "LORA_ERR_DEVICE_CHECK"}
+                10: "LORA_ERR_TOO_MANY_GROUPS"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 DEV_BAD_SLOT, DEV_BAD_OFFSETS, DEV_BAD_END, DEV_TIMEOUT, DEV_BAD_ROW = 1, 2, 4, 8, 16
+# Kernel families of lora_last_call_path (include/lora_sgmv.h).
+PATH_GENERIC_SHRINK, PATH_GENERIC_EXPAND = 0x1, 0x2
+PATH_MMA_SHRINK, PATH_MMA_EXPAND = 0x4, 0x8
+PATH_TC_SHRINK, PATH_TC_EXPAND = 0x10, 0x20
+PATH_DECODE_FUSED, PATH_PREP, PATH_BASE_GEMM = 0x40, 0x80, 0x100
 MAX_SLICES = 3
 
 
@@ -101,6 +106,8 @@ def lib():
     L.lora_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.lora_status_string.restype = ctypes.c_char_p
     L.lora_status_string.argtypes = [ctypes.c_int]
+    L.lora_last_call_path.restype = ctypes.c_uint32
+    L.lora_last_call_path.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.lora_selftest_wait_timeout.restype = ctypes.c_int
     L.lora_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     _lib = L
@@ -346,6 +353,14 @@ def lora_get_device_status(stream=None) -> int:
     _check(L.lora_get_device_status(_stream_handle(stream), ctypes.byref(flags)),
            "lora_get_device_status")
     return int(flags.value)
+
+
+def lora_last_call_path():
+    """(path bits, kernel launches) of the most recent library call made on
+    this host thread; see lora_last_call_path in include/lora_sgmv.h."""
+    n = ctypes.c_uint32(0)
+    bits = lib().lora_last_call_path(ctypes.byref(n))
+    return int(bits), int(n.value)
 
 
 def lora_selftest_wait_timeout(polls: int, stream=None) -> None:

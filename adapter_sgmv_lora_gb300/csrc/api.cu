@@ -12,19 +12,70 @@ namespace lora {
 // Device status word: an OR of LORA_DEV_* flags raised by the kernels.
 __device__ unsigned g_status_word;
 
+// Where lora_get_device_status's exchange leaves the old value of the word.
+__device__ unsigned g_status_snapshot;
+
+// Kernel families and launch count of the current entry-point call on this
+// host thread (lora_last_call_path).
+thread_local unsigned t_path_bits = 0;
+thread_local unsigned t_launches = 0;
+
+void note_launch(unsigned path_bits) {
+  t_path_bits |= path_bits;
+  ++t_launches;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!sms[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
+    sms[dev] = v;
+  }
+  return sms[dev];
+}
+
 namespace {
 
-unsigned* status_ptr() {
-  static unsigned* ptrs[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned*>(p);
-  }
-  return ptrs[dev];
+void begin_call() {
+  t_path_bits = 0;
+  t_launches = 0;
 }
+
+std::mutex g_sym_mu;
+unsigned* g_status_ptr[64] = {nullptr};
+unsigned* g_snapshot_ptr[64] = {nullptr};
+
+// Device addresses of the status word and its snapshot on the current
+// device, looked up once per device (with that device current).
+bool status_ptrs(unsigned** word, unsigned** snap) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(g_sym_mu);
+  if (!g_status_ptr[dev] || !g_snapshot_ptr[dev]) {
+    void* p = nullptr;
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || !p) return false;
+    if (cudaGetSymbolAddress(&q, g_status_snapshot) != cudaSuccess || !q) return false;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+    g_snapshot_ptr[dev] = static_cast<unsigned*>(q);
+  }
+  *word = g_status_ptr[dev];
+  if (snap) *snap = g_snapshot_ptr[dev];
+  return true;
+}
+
+unsigned* status_ptr() {
+  unsigned* w = nullptr;
+  return status_ptrs(&w, nullptr) ? w : nullptr;
+}
+
+// One thread: read and clear the status word in one atomic exchange.
+__global__ void status_exchange_kernel(unsigned* word, unsigned* snap) { *snap = atomicExch(word, 0u); }
 
 lora_status_t validate_problem(const lora_problem_t* p) {
   if (!p) return LORA_ERR_NULL;
@@ -50,7 +101,8 @@ lora_status_t validate_problem(const lora_problem_t* p) {
 
 lora_status_t validate_routing(const lora_problem_t* p, const lora_routing_t* r) {
   if (!r) return LORA_ERR_NULL;
-  if (r->num_groups < 0 || r->num_groups > p->max_num_loras) return LORA_ERR_ROUTING;
+  if (r->num_groups > p->max_num_loras) return LORA_ERR_TOO_MANY_GROUPS;
+  if (r->num_groups < 0) return LORA_ERR_ROUTING;
   if (r->end < 0 || r->end > p->num_tokens) return LORA_ERR_ROUTING;
   if (r->num_groups == 0 && r->end != 0) return LORA_ERR_ROUTING;
   if (r->num_groups > 0 && (!r->lora_ids || !r->grouped_offsets)) return LORA_ERR_NULL;
@@ -100,7 +152,7 @@ size_t plane_bytes(const lora_problem_t* p, int32_t end) {
 // (at most max_num_loras + end / 128 tiles).
 size_t ws_bytes(const lora_problem_t* p, int32_t end) {
   int splits = apply_splits(end, p->in_dim, p->num_slices * p->max_lora_rank);
-  const int tc = tc_shrink_splits(end, p->in_dim);
+  const int tc = tc_shrink_splits(end, p->in_dim, kMaxSmsForWorkspace);
   if (tc > splits) splits = tc;
   size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
                (size_t)p->max_lora_rank * 4;
@@ -118,6 +170,7 @@ extern "C" lora_status_t lora_set_slot(const lora_problem_t* problem, int32_t sl
                                        int32_t r, double lora_alpha, int32_t use_rslora,
                                        const void* A_raw, const void* B_raw,
                                        lora_dtype_t raw_dtype, lora_stream_t stream) {
+  begin_call();
   lora_status_t st = validate_problem(problem);
   if (st != LORA_OK) return st;
   if (slice < 0 || slice >= problem->num_slices) return LORA_ERR_SHAPE;
@@ -137,6 +190,7 @@ extern "C" lora_status_t lora_set_slot(const lora_problem_t* problem, int32_t sl
 
 extern "C" lora_status_t lora_set_slot_bias(const lora_problem_t* problem, int32_t slice, int32_t slot,
                                             const void* bias_raw, lora_dtype_t raw_dtype, lora_stream_t stream) {
+  begin_call();
   lora_status_t st = validate_problem(problem);
   if (st != LORA_OK) return st;
   if (slice < 0 || slice >= problem->num_slices) return LORA_ERR_SHAPE;
@@ -149,6 +203,7 @@ extern "C" lora_status_t lora_set_slot_bias(const lora_problem_t* problem, int32
 
 extern "C" lora_status_t lora_shrink(const lora_problem_t* problem, const lora_routing_t* routing,
                                      float* u, lora_stream_t stream) {
+  begin_call();
   lora_status_t st = validate_problem(problem);
   if (st != LORA_OK) return st;
   if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
@@ -169,6 +224,7 @@ extern "C" lora_status_t lora_shrink(const lora_problem_t* problem, const lora_r
 
 extern "C" lora_status_t lora_expand(const lora_problem_t* problem, const lora_routing_t* routing,
                                      const float* u, lora_stream_t stream) {
+  begin_call();
   lora_status_t st = validate_problem(problem);
   if (st != LORA_OK) return st;
   if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
@@ -195,6 +251,7 @@ extern "C" size_t lora_workspace_bytes(const lora_problem_t* problem, int32_t en
 extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_t* routing,
                                          void* workspace, size_t workspace_bytes,
                                          lora_stream_t stream) {
+  begin_call();
   lora_status_t st = validate_problem(problem);
   if (st != LORA_OK) return st;
   if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
@@ -211,7 +268,7 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
       if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     if (tc_shrink_ok(d)) {
-      const int tcs = tc_shrink_splits(d.end, d.in_dim);
+      const int tcs = tc_shrink_splits(d.end, d.in_dim, device_sm_count());
       const cudaError_t e = launch_tc_shrink(d, u, s, tcs);
       if (e != cudaErrorNotSupported) {
         if (e != cudaSuccess) return LORA_ERR_CUDA;
@@ -227,20 +284,30 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
 }
 
 extern "C" lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* flags) {
+  begin_call();
   if (!flags) return LORA_ERR_NULL;
-  unsigned* p = status_ptr();
-  if (!p) return LORA_ERR_CUDA;
+  unsigned *word = nullptr, *snap = nullptr;
+  if (!status_ptrs(&word, &snap)) return LORA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ERR_CUDA;
+  // The snapshot word is shared by the device's callers: one at a time.
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  status_exchange_kernel<<<1, 1, 0, s>>>(word, snap);
+  if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
   unsigned v = 0;
-  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ERR_CUDA;
-  const unsigned zero = 0;
-  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, snap, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ERR_CUDA;
   *flags = v;
   return LORA_OK;
 }
 
+extern "C" uint32_t lora_last_call_path(uint32_t* num_launches) {
+  if (num_launches) *num_launches = t_launches;
+  return t_path_bits;
+}
+
 extern "C" lora_status_t lora_selftest_wait_timeout(uint32_t polls, lora_stream_t stream) {
+  begin_call();
   unsigned* p = status_ptr();
   if (!p) return LORA_ERR_CUDA;
   return cuda_status(launch_selftest_timeout(p, polls, reinterpret_cast<cudaStream_t>(stream)));
@@ -258,7 +325,7 @@ extern "C" const char* lora_status_string(lora_status_t status) {
     case LORA_ERR_ALIGN: return "LORA_ERR_ALIGN: pointer or stride misaligned";
     case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing or too small";
     case LORA_ERR_CUDA: return "LORA_ERR_CUDA: a CUDA call failed";
-    case LORA_ERR_DEVICE_CHECK: return "LORA_ERR_DEVICE_CHECK: device-side routing check failed";
+    case LORA_ERR_TOO_MANY_GROUPS: return "LORA_ERR_TOO_MANY_GROUPS: more groups than adapter slots";
   }
   return "unknown lora_status_t";
 }
@@ -306,6 +373,7 @@ float* static_workspace_ptr() {
 extern "C" lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem,
                                                  const lora_routing_t* routing,
                                                  lora_stream_t stream) {
+  begin_call();
   lora_status_t st = validate_problem(problem);
   if (st != LORA_OK) return st;
   if ((st = validate_routing(problem, routing)) != LORA_OK) return st;

@@ -42,6 +42,23 @@ struct ProblemDesc {
   unsigned* status;  // device status word (LORA_DEV_* flags)
 };
 
+// Records a successful kernel launch of the current entry-point call
+// (LORA_PATH_* bits; see lora_last_call_path).  Defined in api.cu.
+void note_launch(unsigned path_bits);
+// Returns e, recording the launch when it succeeded.
+inline cudaError_t noted(cudaError_t e, unsigned path_bits) {
+  if (e == cudaSuccess) note_launch(path_bits);
+  return e;
+}
+
+// Streaming multiprocessors of the current device (cached per device; 0 if
+// the query fails, which makes the split heuristics fall back to no split).
+int device_sm_count();
+// The workspace bound (lora_workspace_bytes) depends on shapes only, so
+// where a split count grows with the SM count it is bounded assuming this
+// many SMs; launches use the device's own count, which is at most this.
+constexpr int kMaxSmsForWorkspace = 256;
+
 // Token rows per tile of the bf16 SGMV kernels.
 constexpr int kTileRows = 64;
 
@@ -75,11 +92,11 @@ int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
 
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
 // nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says
-// whether the shape and routing suit it; tc_shrink_splits(end, in) is its
-// plane count (shape-only).  Returns cudaErrorNotSupported when the tensor
+// whether the shape and routing suit it; tc_shrink_splits(end, in, sms) is
+// its plane count for a device of `sms` SMs (shapes and SM count only).  Returns cudaErrorNotSupported when the tensor
 // maps cannot be encoded (nothing launched).
 bool tc_shrink_ok(const ProblemDesc& p);
-int tc_shrink_splits(int end, int in_dim);
+int tc_shrink_splits(int end, int in_dim, int sms);
 cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int nsplit);
 // tcgen05 expand for long groups with R = 64 or 128 (sums nsplit planes of u).
 bool tc_expand_ok(const ProblemDesc& p);

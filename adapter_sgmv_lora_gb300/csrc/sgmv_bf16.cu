@@ -567,17 +567,7 @@ cudaError_t ensure_smem(K kernel, int bytes, unsigned long long* done) {
   return e;
 }
 
-int num_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (!sms[dev]) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    sms[dev] = v > 0 ? v : 152;
-  }
-  return sms[dev];
-}
+int num_sms() { return device_sm_count(); }
 
 // lora_shrink's cluster size: the input dimension is split over up to 16
 // CTAs while the grid stays within two CTAs per SM (decode-sized launches
@@ -672,7 +662,7 @@ cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride), LORA_PATH_MMA_SHRINK);
 }
 
 // The kernel of an expand tile shape (only the one that runs is instantiated).
@@ -714,7 +704,7 @@ cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, p, u, map);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, u, map), LORA_PATH_MMA_EXPAND);
 }
 
 }  // namespace

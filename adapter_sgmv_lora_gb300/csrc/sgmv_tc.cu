@@ -20,8 +20,9 @@
 //           expand's swizzled operand layout, see pack_u16).
 // Expand (further down): persistent, one CTA per SM over (tile, slice,
 // 128-column block) units, TMEM accumulators, 8 epilogue warps.
-// Rows of the 128-row box past the group (other groups, base rows, or past
-// the tensor: zero-filled) are read but their u / y rows are never stored.
+// Rows of the 128-row box past the group are other groups' rows (read, never
+// stored) or rows at or past `end`, which the tensor maps zero-fill: base
+// rows are never read.
 // Every mbarrier wait is bounded; on expiry the CTA records LORA_DEV_TIMEOUT,
 // skips its stores and still releases its TMEM.
 #include <cuda.h>
@@ -288,7 +289,9 @@ bool encode_maps(const ProblemDesc& p, TcMaps* m) {
   if (!enc) return false;
   const cuuint32_t es[3] = {1, 1, 1};
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.in_dim, (cuuint64_t)p.num_tokens};
+    // The map ends at row `end`: boxes reaching past it are zero-filled, so
+    // base rows are never read.
+    const cuuint64_t dims[2] = {(cuuint64_t)p.in_dim, (cuuint64_t)p.end};
     const cuuint64_t strides[1] = {(cuuint64_t)p.x_row_stride * 2};
     const cuuint32_t box[2] = {(cuuint32_t)TK, (cuuint32_t)TM};
     if (enc(&m->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, es,
@@ -346,7 +349,7 @@ cudaError_t launch_tc_t(const ProblemDesc& p, const TcMaps& maps, float* u, cuda
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p, maps, u, nsplit, plane_stride, nsn, upk);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, maps, u, nsplit, plane_stride, nsn, upk), LORA_PATH_TC_SHRINK);
 }
 
 template <int NR>
@@ -358,13 +361,13 @@ cudaError_t launch_tc_nr(const ProblemDesc& p, const TcMaps& maps, float* u, cud
 
 }  // namespace
 
-int tc_shrink_splits(int end, int in_dim) {
-  // Shape-only: split K (1, 2 or 4 planes) while a lower bound on the tiles
-  // times the split stays within 152 CTAs and each split is whole stages.
+int tc_shrink_splits(int end, int in_dim, int sms) {
+  // Split K (1, 2 or 4 planes) while a lower bound on the tiles times the
+  // split stays within one CTA per SM and each split is whole stages.
   if (end <= 0 || in_dim % TK != 0) return 1;
   const long long tiles = (end + TM - 1) / TM;
   int n = 1;
-  while (n < 4 && tiles * n * 2 <= 152 && (in_dim / TK) % (n * 2) == 0) n *= 2;
+  while (n < 4 && tiles * n * 2 <= sms && (in_dim / TK) % (n * 2) == 0) n *= 2;
   return n;
 }
 
@@ -891,7 +894,8 @@ bool encode_tx_maps(const ProblemDesc& p, TxMaps* m) {
   for (int j = 0; j < p.n_slices; ++j) {
     const SliceDesc& sl = p.sl[j];
     {
-      const cuuint64_t dims[2] = {(cuuint64_t)sl.out_dim, (cuuint64_t)p.num_tokens};
+      // Ends at row `end` (zero-filled past it): base rows are never read.
+      const cuuint64_t dims[2] = {(cuuint64_t)sl.out_dim, (cuuint64_t)p.end};
       const cuuint64_t strides[1] = {(cuuint64_t)sl.y_row_stride * 2};
       const cuuint32_t box[2] = {64, (cuuint32_t)TM};
       if (enc(&m->y[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, sl.y, dims, strides, box, es,
@@ -945,7 +949,7 @@ cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, p, maps, w, u, upk);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, maps, w, u, upk), LORA_PATH_TC_EXPAND);
 }
 
 TxWork make_tx_work(const ProblemDesc& p, int nsplit) {
@@ -992,11 +996,12 @@ size_t tc_packed_bytes(int S, int end, int n_slices, int R) {
 int tc_pack_splits(const ProblemDesc& p) {
   // Column parts of the packed shrink: split the n*R columns (whole 16-column
   // groups, a supported tile width) while a lower bound on the tiles times
-  // the parts stays within 152 CTAs.
+  // the parts stays within one CTA per SM of this device.
   const int nR = p.n_slices * p.R;
   const long long tiles = (p.end + TM - 1) / TM;
+  const int sms = device_sm_count();
   int n = 1;
-  while (n < 4 && tiles * n * 2 <= 152 && nR % (32 * n) == 0 && nr_supported(nR / (2 * n))) n *= 2;
+  while (n < 4 && tiles * n * 2 <= sms && nR % (32 * n) == 0 && nr_supported(nR / (2 * n))) n *= 2;
   return n;
 }
 

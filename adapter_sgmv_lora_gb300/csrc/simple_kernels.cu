@@ -166,7 +166,7 @@ cudaError_t launch_set_bias(const ProblemDesc& p, int slice, int slot, const voi
     else
       set_bias_kernel<float, float><<<g, 256, 0, s>>>(p, slice, slot, (const float*)bias_raw);
   }
-  return cudaGetLastError();
+  return noted(cudaGetLastError(), LORA_PATH_PREP);
 }
 
 cudaError_t launch_shrink_simple(const ProblemDesc& p, float* u, cudaStream_t s) {
@@ -176,7 +176,7 @@ cudaError_t launch_shrink_simple(const ProblemDesc& p, float* u, cudaStream_t s)
     shrink_simple_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(p, u);
   else
     shrink_simple_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(p, u);
-  return cudaGetLastError();
+  return noted(cudaGetLastError(), LORA_PATH_GENERIC_SHRINK);
 }
 
 cudaError_t launch_expand_simple(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl) {
@@ -195,8 +195,8 @@ cudaError_t launch_expand_simple(const ProblemDesc& p, const float* u, cudaStrea
     cfg.numAttrs = 1;
   }
   if (p.dtype == LORA_DTYPE_BF16)
-    return cudaLaunchKernelEx(&cfg, expand_simple_kernel<__nv_bfloat16>, p, u);
-  return cudaLaunchKernelEx(&cfg, expand_simple_kernel<float>, p, u);
+    return noted(cudaLaunchKernelEx(&cfg, expand_simple_kernel<__nv_bfloat16>, p, u), LORA_PATH_GENERIC_EXPAND);
+  return noted(cudaLaunchKernelEx(&cfg, expand_simple_kernel<float>, p, u), LORA_PATH_GENERIC_EXPAND);
 }
 
 cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, float scale,
@@ -221,7 +221,7 @@ cudaError_t launch_set_slot(const ProblemDesc& p, int slice, int slot, int r, fl
       set_slot_kernel<float, float><<<g, 256, 0, s>>>(p, slice, slot, r, scale,
                                                        (const float*)A_raw, (const float*)B_raw);
   }
-  return cudaGetLastError();
+  return noted(cudaGetLastError(), LORA_PATH_PREP);
 }
 
 // Failure-path self test: one thread waits on a fresh barrier that nothing
@@ -238,7 +238,7 @@ __global__ void selftest_timeout_kernel(unsigned* status, uint32_t limit) {
 
 cudaError_t launch_selftest_timeout(unsigned* status, uint32_t limit, cudaStream_t s) {
   selftest_timeout_kernel<<<1, 32, 0, s>>>(status, limit);
-  return cudaGetLastError();
+  return noted(cudaGetLastError(), 0);
 }
 
 }  // namespace lora

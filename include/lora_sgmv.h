@@ -11,7 +11,11 @@
  * Routing follows the triple of the "max.pipelines.lora.LoRAManagerV3" API
  * page (get_lora_graph_inputs): lora_ids and grouped_offsets live on the
  * device, end on the host.  Rows at or past `end` (base requests, which the
- * sort puts last) are never read or written.
+ * sort puts last) are never read or written.  Within [0, end) every kernel
+ * writes only the rows of the group it is working on; the tensor-core
+ * kernels for long groups load whole 128-row boxes of x and y, so they may
+ * READ rows of neighbouring groups (never rows at or past `end`: their
+ * tensor maps end there).
  *
  * Conventions for every entry point:
  *   - Every buffer is owned by the caller.  No entry point allocates or frees
@@ -53,7 +57,7 @@ typedef enum {
   LORA_ERR_ALIGN = 7,         /* pointer/stride alignment required by the call */
   LORA_ERR_WORKSPACE = 8,     /* workspace NULL or smaller than lora_workspace_bytes() */
   LORA_ERR_CUDA = 9,          /* a CUDA runtime call or kernel launch failed */
-  LORA_ERR_DEVICE_CHECK = 10  /* reserved: returned by no call; see lora_get_device_status */
+  LORA_ERR_TOO_MANY_GROUPS = 10 /* num_groups > max_num_loras ("No free lora slots") */
 } lora_status_t;
 
 /* Storage type of x, y and the A/B stacks of one problem. */
@@ -132,7 +136,12 @@ typedef struct {
  * grouped_offsets[num_groups + 1] are DEVICE int32 arrays; num_groups and end
  * are host values.  Group g covers sorted-batch rows
  * [grouped_offsets[g], grouped_offsets[g+1]) and uses slot lora_ids[g].
- * num_groups == 0 or end == 0 is a valid no-op.
+ * num_groups == 0 or end == 0 is a valid no-op.  num_groups > max_num_loras
+ * returns LORA_ERR_TOO_MANY_GROUPS (a batch needs a slot per group: "No free
+ * lora slots", "vLLM LoRA 实现深度解析" section 5.3); other inconsistent host
+ * values (end < 0, end > num_tokens, end > 0 with no group) LORA_ERR_ROUTING.
+ * The same slot may appear in two groups (each group uses its slot); the
+ * routing builder never produces that.
  */
 typedef struct {
   const int32_t* lora_ids;
@@ -293,12 +302,38 @@ lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem, const lora_
                                       lora_stream_t stream);
 
 /*
- * lora_get_device_status -- synchronizes `stream`, then reads and clears the
- * device status word of the current device (an OR of LORA_DEV_* flags from
- * every launch since the last read).  Returns LORA_ERR_CUDA if the
- * synchronization or copy fails.
+ * lora_get_device_status -- reads and clears, in one atomic exchange ordered
+ * after the work already on `stream`, the device status word of the current
+ * device (an OR of LORA_DEV_* flags from every launch since the last read,
+ * on any stream), then synchronizes `stream` and returns the flags.  A flag
+ * raised by a kernel on another stream is never lost: it is either returned
+ * by this call or kept for the next.  Returns LORA_ERR_CUDA if the exchange,
+ * the copy or the synchronization fails.
  */
 lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* flags);
+
+/*
+ * Kernel families (bits of lora_last_call_path).  The pages have no
+ * counterpart; this is an introspection aid for tests and profiling.
+ */
+#define LORA_PATH_GENERIC_SHRINK 0x1u  /* one warp per u element (fp32, odd shapes) */
+#define LORA_PATH_GENERIC_EXPAND 0x2u  /* one thread per y element */
+#define LORA_PATH_MMA_SHRINK 0x4u      /* mma.sync shrink (short groups) */
+#define LORA_PATH_MMA_EXPAND 0x8u      /* mma.sync expand (short groups) */
+#define LORA_PATH_TC_SHRINK 0x10u      /* tcgen05 + TMA shrink (long groups) */
+#define LORA_PATH_TC_EXPAND 0x20u      /* persistent tcgen05 + TMA expand (long groups) */
+#define LORA_PATH_DECODE_FUSED 0x40u   /* one-launch shrink + expand (decode-sized batches) */
+#define LORA_PATH_PREP 0x80u           /* load-time slot / bias preparation */
+#define LORA_PATH_BASE_GEMM 0x100u     /* base projection GEMM with the delta as K tail */
+
+/*
+ * lora_last_call_path -- the OR of LORA_PATH_* bits of the kernels launched
+ * by the most recent entry-point call made on the calling host thread (0 if
+ * it launched nothing: a no-op, or an error before any launch), and, when
+ * num_launches is not NULL, how many kernels that call launched.  Host only;
+ * reads thread-local state, no CUDA call.
+ */
+uint32_t lora_last_call_path(uint32_t* num_launches);
 
 /*
  * lora_selftest_wait_timeout -- exercises the failure path of the pipelined

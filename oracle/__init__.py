@@ -41,6 +41,7 @@ import numpy as np
 from . import build as _build
 
 _LIB = None
+_LIB_OMP = None
 
 OK, BAD_ARG, BAD_SLOT, BAD_ROW, BAD_ROUTE = 0, 1, 2, 3, 4
 
@@ -61,27 +62,41 @@ class _Slice(ctypes.Structure):
     ]
 
 
-def lib():
-    """Load (building first if needed) the C oracle."""
-    global _LIB
+def _bind(L):
+    """Declare the oracle's C signatures on a loaded build."""
+    i32p = ctypes.POINTER(ctypes.c_int)
+    L.oracle_build_routing.restype = ctypes.c_int
+    L.oracle_build_routing.argtypes = [ctypes.c_int, i32p, i32p, ctypes.c_int, i32p, i32p, i32p,
+                                       i32p, i32p, i32p]
+    L.oracle_sgmv_rows.restype = ctypes.c_int
+    L.oracle_sgmv_rows.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
+                                   ctypes.c_longlong, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_void_p]
+    L.oracle_sgmv_token_slots.restype = ctypes.c_int
+    L.oracle_sgmv_token_slots.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
+                                          ctypes.c_longlong, ctypes.c_void_p]
+    return L
+
+
+def lib(parallel: bool = False):
+    """Load (building first if needed) the C oracle: the single-threaded
+    build, or with parallel=True the OpenMP build (bit-identical results;
+    falls back to the single-threaded build where OpenMP is missing)."""
+    global _LIB, _LIB_OMP
+    if parallel:
+        if _LIB_OMP is None:
+            path = _build.omp_path()
+            _LIB_OMP = _bind(ctypes.CDLL(path)) if path else lib(False)
+        return _LIB_OMP
     if _LIB is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        i32p = ctypes.POINTER(ctypes.c_int)
-        L.oracle_build_routing.restype = ctypes.c_int
-        L.oracle_build_routing.argtypes = [ctypes.c_int, i32p, i32p, ctypes.c_int, i32p, i32p, i32p,
-                                           i32p, i32p, i32p]
-        L.oracle_sgmv_rows.restype = ctypes.c_int
-        L.oracle_sgmv_rows.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
-                                       ctypes.c_longlong, i32p, i32p, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_void_p]
-        L.oracle_sgmv_token_slots.restype = ctypes.c_int
-        L.oracle_sgmv_token_slots.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                              ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
-                                              ctypes.c_longlong, ctypes.c_void_p]
-        _LIB = L
+        _LIB = _bind(ctypes.CDLL(_build.build()))
     return _LIB
+
+
+def omp_available() -> bool:
+    return _build.omp_path() is not None
 
 
 def _i32(a):
@@ -230,7 +245,7 @@ def _bias_args(sl, keep):
 
 
 def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim: int, R: int,
-              max_num_loras: int):
+              max_num_loras: int, parallel: bool = False):
     """Delta for the listed rows, in double.
 
     rows           int array, batch row index of each listed row (< end)
@@ -241,9 +256,11 @@ def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim:
                         A[s*A_slot_stride + k*in_dim : +in_dim]
                      B  float64 stack; element (s, o, k) at B[s*B_slot_stride + o*R + k]
                      out_dim, y_in float64 [n_rows, out_dim] (listed rows)
+    parallel       use the OpenMP build (rows shared out among threads; the
+                   same numbers)
     Returns (u [n_rows, n*R] float64, [y_out_j [n_rows, out_j] float64]).
     """
-    L = lib()
+    L = lib(parallel)
     rows = _i32(rows)
     n = int(rows.size)
     x_rows = np.ascontiguousarray(x_rows, dtype=np.float64)
@@ -279,7 +296,7 @@ def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim:
     return u, outs
 
 
-def problem_rows(prob, rows):
+def problem_rows(prob, rows, parallel: bool = False):
     """Run ``sgmv_rows`` on a prepared problem (see ``prepare_problem``) for the given rows."""
     rows = _i32(rows)
     dt = prob["dtype"]
@@ -290,7 +307,7 @@ def problem_rows(prob, rows):
         d["y_in"] = to_f64(sl["y"][rows][:, sl["y_col0"]:sl["y_col0"] + sl["out_dim"]], dt)
         slices.append(d)
     return sgmv_rows(rows, x_rows, slices, prob["lora_ids"], prob["grouped_offsets"], prob["end"],
-                     prob["in_dim"], prob["R"], prob["S"])
+                     prob["in_dim"], prob["R"], prob["S"], parallel=parallel)
 
 
 def prepare_problem(raw, proj: str, fused: bool = True) -> dict:
@@ -380,9 +397,10 @@ def row_slots(req_slot, req_len) -> np.ndarray:
     return np.repeat(np.asarray(req_slot, dtype=np.int32), np.asarray(req_len, dtype=np.int64))
 
 
-def sgmv_token_slots(row_slot, x_rows, slices, in_dim: int, R: int, max_num_loras: int):
+def sgmv_token_slots(row_slot, x_rows, slices, in_dim: int, R: int, max_num_loras: int,
+                     parallel: bool = False):
     """Per-token definition (C): listed rows with their slots; see lora_oracle.c."""
-    L = lib()
+    L = lib(parallel)
     rs = _i32(row_slot)
     n = int(rs.size)
     x_rows = np.ascontiguousarray(x_rows, dtype=np.float64)
@@ -408,7 +426,7 @@ def sgmv_token_slots(row_slot, x_rows, slices, in_dim: int, R: int, max_num_lora
     return u, outs
 
 
-def problem_token_rows(prob, rows, row_slot):
+def problem_token_rows(prob, rows, row_slot, parallel: bool = False):
     """Per-token oracle on a prepared problem whose x / y are in arrival order."""
     rows = _i32(rows)
     dt = prob["dtype"]
@@ -418,4 +436,4 @@ def problem_token_rows(prob, rows, row_slot):
         d = dict(sl)
         d["y_in"] = to_f64(sl["y"][rows][:, sl["y_col0"]:sl["y_col0"] + sl["out_dim"]], dt)
         slices.append(d)
-    return sgmv_token_slots(row_slot, x_rows, slices, prob["in_dim"], prob["R"], prob["S"])
+    return sgmv_token_slots(row_slot, x_rows, slices, prob["in_dim"], prob["R"], prob["S"], parallel=parallel)

@@ -31,6 +31,10 @@
  * caller decides how (and whether) to round it to the storage type.
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math).
+ * A second build adds -fopenmp: the listed rows are then shared out among
+ * threads (each row is computed by one thread, in the same order as above),
+ * so both builds return bit-identical results; the single-threaded build
+ * ignores the pragmas.
  */
 #include <limits.h>
 #include <stddef.h>
@@ -171,18 +175,23 @@ int oracle_sgmv_rows(int n_rows, const int* rows, int in_dim, int R, int max_num
   if (num_groups > 0 && grouped_offsets[num_groups] != end) return ORACLE_BAD_ROUTE;
   if (num_groups == 0 && end != 0) return ORACLE_BAD_ROUTE;
 
+  if (R > 1024) return ORACLE_BAD_ARG;
   for (int r = 0; r < n_rows; ++r) {
     int t = rows[r];
     if (t < 0 || t >= end) return ORACLE_BAD_ROW;
+    if (group_of_row(t, grouped_offsets, num_groups) < 0) return ORACLE_BAD_ROW;
+  }
+
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int r = 0; r < n_rows; ++r) {
+    int t = rows[r];
     int g = group_of_row(t, grouped_offsets, num_groups);
-    if (g < 0) return ORACLE_BAD_ROW;
     int s = lora_ids[g];
     const double* xt = x_rows + (long long)r * x_row_stride;
     for (int j = 0; j < n_slices; ++j) {
       const oracle_slice* sl = &slices[j];
       /* shrink: u_j = A_j[s] . x_t */
       double uj[1024];
-      if (R > 1024) return ORACLE_BAD_ARG;
       for (int k = 0; k < R; ++k) {
         const double* a = sl->A + (long long)s * sl->A_slot_stride + (long long)k * in_dim;
         double acc = 0.0;
@@ -219,9 +228,11 @@ int oracle_sgmv_token_slots(int n_rows, const int* row_slot, int in_dim, int R, 
                             long long x_row_stride, double* u) {
   if (n_rows < 0 || in_dim <= 0 || R <= 0 || R > 1024 || n_slices <= 0) return ORACLE_BAD_ARG;
   if (n_rows > 0 && (!row_slot || !slices || !x_rows)) return ORACLE_BAD_ARG;
+  for (int r = 0; r < n_rows; ++r)
+    if (row_slot[r] < -1 || row_slot[r] >= max_num_loras) return ORACLE_BAD_SLOT;
+#pragma omp parallel for schedule(dynamic, 4)
   for (int r = 0; r < n_rows; ++r) {
     const int s = row_slot[r];
-    if (s < -1 || s >= max_num_loras) return ORACLE_BAD_SLOT;
     const double* xt = x_rows + (long long)r * x_row_stride;
     for (int j = 0; j < n_slices; ++j) {
       const oracle_slice* sl = &slices[j];

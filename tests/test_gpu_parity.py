@@ -89,9 +89,21 @@ def _poison_padding(dev, raw):
             b[s, :, k16:].fill_(float("nan"))
 
 
+# Kernel families (lora_last_call_path) each call is expected to take.
+GEN = 0x1 | 0x2        # generic shrink + expand
+MMA = 0x4 | 0x8        # mma.sync shrink + expand
+TC = 0x10 | 0x20       # tcgen05 shrink + expand
+TC_MMA = 0x10 | 0x8    # tcgen05 shrink, mma.sync expand
+
+
 def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0,
-             slot_ranks=False, poison=False):
-    """Prepare on the device, run, compare with the oracle.  Returns the device dict."""
+             slot_ranks=False, poison=False, path=None, parallel=False):
+    """Prepare on the device, run, compare with the oracle.  Returns the device dict.
+
+    path: the exact OR of kernel-family bits the call(s) must have launched
+    (both calls together in split mode), or None for no check.
+    parallel: check with the OpenMP build of the oracle (same numbers,
+    shared out over the host's cores; for full-size workloads)."""
     lk, device = _lk(), _dev()
     dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y, slot_ranks=slot_ranks)
     ref = oracle.prepare_problem(raw, proj, fused=fused)
@@ -126,12 +138,17 @@ def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=F
     u = None
     if mode == "apply":
         lk.lora_sgmv_apply(prob, routing, dev["workspace"])
+        taken = lk.lora_last_call_path()[0]
     else:
         nR = len(dev["names"]) * raw["max_lora_rank"]
         u = torch.full((max(end, 1), nR), float("nan"), dtype=torch.float32, device="cuda")
         lk.lora_shrink(prob, routing, u)
+        taken = lk.lora_last_call_path()[0]
         lk.lora_expand(prob, routing, u)
+        taken |= lk.lora_last_call_path()[0]
     torch.cuda.synchronize()
+    if path is not None and end > 0:
+        assert taken == path, ("kernel path", hex(taken), hex(path))
     assert lk.lora_get_device_status() == 0
     y_after = device.y_host(dev)
     # rows >= end: bit-identical (compare bit patterns: the sentinels are NaNs)
@@ -140,7 +157,7 @@ def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=F
         return dev
     rng = np.random.default_rng(seed)
     rr = np.arange(end, dtype=np.int32) if rows == "all" else _sample_rows(rt["grouped_offsets"], end, rng)
-    u_ref, ys_ref = oracle.problem_rows(ref, rr)
+    u_ref, ys_ref = oracle.problem_rows(ref, rr, parallel=parallel)
     got = oracle.to_f64(y_after[rr], dt)
     col = 0
     for yj in ys_ref:
@@ -160,33 +177,38 @@ def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=F
 @pytest.mark.parametrize("proj", ["qkv", "o"])
 @pytest.mark.parametrize("mode", ["apply", "split"])
 def test_tiny_fp32(proj, mode):
-    run_case(sy.draw("tiny", 0), proj, mode=mode)
+    run_case(sy.draw("tiny", 0), proj, mode=mode, path=GEN)
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
 @pytest.mark.parametrize("mode", ["apply", "split"])
 def test_decode8b_full(proj, mode):
-    run_case(sy.draw("decode8b", 0), proj, mode=mode)
+    run_case(sy.draw("decode8b", 0), proj, mode=mode, path=MMA)
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
 def test_many64_unfused_full(proj):
-    run_case(sy.draw("many64", 0), proj, fused=False, mode="split")
+    run_case(sy.draw("many64", 0), proj, fused=False, mode="split", path=MMA)
 
 
 def test_many64_separate_outputs():
-    run_case(sy.draw("many64", 1), "qkv", fused=False, separate_y=True)
+    run_case(sy.draw("many64", 1), "qkv", fused=False, separate_y=True, path=MMA)
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
 @pytest.mark.parametrize("mode", ["apply", "split"])
-def test_prefill8b_sampled(proj, mode):
-    run_case(sy.draw("prefill8b", 0), proj, mode=mode, rows="sample")
+def test_prefill8b_every_row(proj, mode):
+    """Full-size ragged prefill (R = 64, 4 slots): every routed row against
+    the oracle, on the tensor-core path."""
+    run_case(sy.draw("prefill8b", 0), proj, mode=mode, path=TC, parallel=True)
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
-def test_mixed70b_sampled(proj):
-    run_case(sy.draw("mixed70b", 0), proj, rows="sample")
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_mixed70b_every_row(proj, mode):
+    """Full-size mixed 70B batch (R = 128, 16 slots, 8192 rows): every routed
+    row against the oracle, on the tensor-core path."""
+    run_case(sy.draw("mixed70b", 0), proj, mode=mode, path=TC, parallel=True)
 
 
 @pytest.mark.parametrize("proj", ["gateup", "down"])
@@ -194,7 +216,41 @@ def test_mixed70b_sampled(proj):
 def test_mlp8b_full(proj, mode):
     """MLP projections (gate + up fused as two slices; down over the 14336-wide
     intermediate activations)."""
-    run_case(sy.draw("mlp8b", 0), proj, mode=mode)
+    run_case(sy.draw("mlp8b", 0), proj, mode=mode, path=MMA)
+
+
+# -------------------------------------- checks dominated by the LoRA delta --
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_delta_dominated_decode(mode):
+    """y_in = 0 and B scaled so the delta is of order one or more: the
+    2e-2 (1 + |ref|) bar then measures the delta itself (decode shapes,
+    mma.sync path)."""
+    raw = sy.emphasize_delta(sy.draw("decode8b", 31), 40.0)
+    run_case(raw, "qkv", mode=mode, path=MMA)
+    run_case(raw, "o", mode=mode, path=MMA)
+
+
+@pytest.mark.parametrize("R", [16, 64, 128])
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_delta_dominated_long_groups(R, mode):
+    """As above on the tensor-core path for long groups (ragged 128-row
+    tiles), ranks 16, 64 and 128."""
+    spec = _spec(max_num_loras=5, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
+                 fixed_slots=(4, 3, 2, 1, 0, -1), fixed_lens=(130, 255, 128, 300, 97, 7),
+                 hidden=512, n_heads=8, n_kv_heads=2, head_dim=64)
+    raw = sy.emphasize_delta(sy.draw(spec, 32 + R), 40.0)
+    run_case(raw, "qkv", mode=mode, path=TC if R >= 64 else TC_MMA)
+    run_case(raw, "o", mode=mode, path=TC if R >= 64 else TC_MMA)
+
+
+def test_delta_dominated_fp32_and_bias():
+    """fp32 generic kernels, and the general mma.sync kernels with a bias and
+    true ranks, with y_in = 0 and an order-one delta."""
+    spec = _spec(dtype="f32", max_lora_rank=32, rank_choices=(8, 32), n_requests=25)
+    run_case(sy.emphasize_delta(sy.draw(spec, 41), 40.0), "qkv", mode="split", path=GEN)
+    raw = sy.add_bias(sy.emphasize_delta(sy.draw("decode8b", 42), 40.0), 42, scale=1.0)
+    run_case(raw, "qkv", mode="apply", slot_ranks=True, poison=True, path=MMA)
 
 
 @pytest.mark.parametrize("mode", ["apply", "split"])
@@ -202,8 +258,8 @@ def test_mlp_long_groups_tensor_core_path(mode):
     spec = _spec(family="mlp", hidden=512, intermediate=1024, max_num_loras=3, max_lora_rank=64,
                  rank_choices=(32, 64), kind="fixed", fixed_slots=(2, 0, 1, -1),
                  fixed_lens=(300, 513, 200, 11))
-    run_case(sy.draw(spec, 9), "gateup", mode=mode)
-    run_case(sy.draw(spec, 10), "down", mode=mode)
+    run_case(sy.draw(spec, 9), "gateup", mode=mode, path=TC)
+    run_case(sy.draw(spec, 10), "down", mode=mode, path=TC)
 
 
 def run_unsorted(raw, proj="qkv", mode="apply"):
@@ -288,8 +344,8 @@ def test_bias_and_ranks_long_groups(mode):
                  n_kv_heads=2, head_dim=64)
     for seed in (1, 2):
         raw = sy.add_bias(sy.draw(spec, seed), seed)
-        run_case(raw, "qkv", mode=mode, slot_ranks=True, poison=True)
-        run_case(raw, "o", mode=mode, slot_ranks=True, poison=True)
+        run_case(raw, "qkv", mode=mode, slot_ranks=True, poison=True, path=TC)
+        run_case(raw, "o", mode=mode, slot_ranks=True, poison=True, path=TC)
 
 
 @pytest.mark.parametrize("mode", ["apply", "split"])
@@ -324,8 +380,8 @@ def test_rank_variants_ragged_tiles(R, mode):
     spec = _spec(max_num_loras=7, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
                  fixed_slots=(0, 1, 2, 3, 4, 5, 6, -1), fixed_lens=(1, 63, 64, 65, 127, 130, 200, 9),
                  hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
-    run_case(sy.draw(spec, 3), "qkv", mode=mode)
-    run_case(sy.draw(spec, 4), "o", mode=mode)
+    run_case(sy.draw(spec, 3), "qkv", mode=mode, path=MMA)
+    run_case(sy.draw(spec, 4), "o", mode=mode, path=MMA)
 
 
 @pytest.mark.parametrize("mode", ["apply", "split"])
@@ -386,8 +442,9 @@ def test_long_groups_tensor_core_shrink(R, mode):
     spec = _spec(max_num_loras=6, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
                  fixed_slots=(5, 4, 3, 2, 1, 0, -1), fixed_lens=(100, 127, 128, 129, 300, 1000, 7),
                  hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
-    run_case(sy.draw(spec, 7), "qkv", mode=mode)
-    run_case(sy.draw(spec, 8), "o", mode=mode)
+    want = TC if R >= 64 else TC_MMA
+    run_case(sy.draw(spec, 7), "qkv", mode=mode, path=want)
+    run_case(sy.draw(spec, 8), "o", mode=mode, path=want)
 
 
 @pytest.mark.parametrize("groups", [256, 260])
@@ -399,7 +456,7 @@ def test_many_long_groups(groups, mode):
     spec = _spec(max_num_loras=groups, max_lora_rank=64, rank_choices=(32, 64), kind="fixed",
                  fixed_slots=tuple(range(groups - 1, -1, -1)) + (-1,), fixed_lens=(100,) * groups + (5,),
                  hidden=128, n_heads=4, n_kv_heads=4, head_dim=32)
-    run_case(sy.draw(spec, 21), "qkv", mode=mode)
+    run_case(sy.draw(spec, 21), "qkv", mode=mode, path=TC if groups <= 256 else TC_MMA)
 
 
 def test_wait_timeout_is_reported_and_context_survives():

@@ -148,6 +148,9 @@ def test_host_validation_without_gpu():
     prob.x, prob.x_row_stride, prob.num_slices = 16, 64, 1
     prob.slices[0] = lk._Slice(16, 16 * 64, 16, 16 * 16, 16, 16, 16)
     rr.num_groups, rr.end = 3, 4          # more groups than slots
+    assert L.lora_expand(ctypes.byref(prob), ctypes.byref(rr), None, None) == 10
+    assert L.lora_last_call_path(None) == 0   # nothing was launched
+    rr.num_groups, rr.end = -1, 0         # negative group count
     assert L.lora_expand(ctypes.byref(prob), ctypes.byref(rr), None, None) == 5
     rr.num_groups, rr.end = 1, 9          # end past num_tokens
     assert L.lora_expand(ctypes.byref(prob), ctypes.byref(rr), None, None) == 5

@@ -460,3 +460,29 @@ def test_bias_merged_weight():
     _, (yt,) = oracle.sgmv_token_slots([1, 1, 2, 2, 2, -1], x, sl, k, R, S)
     np.testing.assert_allclose(yt[:5], yo, rtol=0, atol=0)
     assert np.array_equal(yt[5], y[5])
+
+
+def test_openmp_build_matches_single_thread_bitwise():
+    """The OpenMP build of the oracle shares the listed rows out among
+    threads but computes each row exactly as the single-threaded build does:
+    the results are bit-identical (routed rows and per-token rows)."""
+    if not oracle.omp_available():
+        pytest.skip("no OpenMP compiler here")
+    spec = sy.custom_spec(max_num_loras=5, max_lora_rank=32, rank_choices=(16, 32), kind="prefill",
+                          n_requests=12, len_range=(1, 40), slot_dist="uniform+base", hidden=256,
+                          n_heads=8, n_kv_heads=2, head_dim=32)
+    raw = sy.add_bias(sy.draw(spec, 3), 3)
+    for proj in ("qkv", "o"):
+        prob = oracle.prepare_problem(raw, proj)
+        rows = np.arange(prob["end"], dtype=np.int32)
+        u1, y1 = oracle.problem_rows(prob, rows)
+        u2, y2 = oracle.problem_rows(prob, rows, parallel=True)
+        assert np.array_equal(u1, u2)
+        for a, b in zip(y1, y2):
+            assert np.array_equal(a, b)
+        slots = oracle.row_slots(raw["req_slot"], raw["req_len"])
+        allr = np.arange(raw["T"], dtype=np.int32)
+        _, t1 = oracle.problem_token_rows(prob, allr, slots)
+        _, t2 = oracle.problem_token_rows(prob, allr, slots, parallel=True)
+        for a, b in zip(t1, t2):
+            assert np.array_equal(a, b)

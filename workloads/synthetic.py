@@ -226,6 +226,20 @@ def custom_spec(**kw) -> Spec:
     return Spec(**base)
 
 
+def emphasize_delta(raw: dict, b_factor: float = 40.0) -> dict:
+    """A variant of a drawn workload whose check is dominated by the LoRA
+    delta: every base output y is zero and the raw B matrices are multiplied
+    by b_factor (B ~ 0.02 * b_factor * N(0, 1) before the scale is folded in,
+    so the delta is of order one or more instead of about 0.1).  Only the
+    drawn data change; no part of the method is applied here."""
+    spec = raw["spec"]
+    for prob in spec.problems:
+        raw["y_" + prob] = to_storage(np.zeros(raw["y_" + prob].shape, dtype=np.float32), spec.dtype)
+    for p in spec.projs:
+        raw["B"][p] = [np.float32(b_factor) * b for b in raw["B"][p]]
+    return raw
+
+
 def add_bias(raw: dict, seed: int = 0, scale: float = 0.1) -> dict:
     """Draw a LoRA bias vector per (projection, slot): scale * N(0, 1), fp32.
     Drawn from its own stream so the rest of the workload is unchanged."""

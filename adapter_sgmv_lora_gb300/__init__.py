@@ -385,6 +385,9 @@ class CallBuilder:
         self.ws = workspace.data_ptr()
         self.nbytes = workspace.numel() * workspace.element_size()
         self._keep = (problem, routing, workspace)
+        self._n = ctypes.c_uint32(0)
+        self.last_path = 0       # kernel families of the latest apply (lora_last_call_path)
+        self.last_launches = 0   # kernels it launched
 
     def set_routing(self, num_groups: int, end: int) -> None:
         """A new batch in the same device routing buffers: only the host
@@ -396,3 +399,5 @@ class CallBuilder:
         rc = self.L.lora_sgmv_apply(ctypes.byref(self.c), ctypes.byref(self.r), self.ws, self.nbytes,
                                     _stream_handle(stream))
         _check(rc, "lora_sgmv_apply")
+        self.last_path = int(self.L.lora_last_call_path(ctypes.byref(self._n)))
+        self.last_launches = int(self._n.value)

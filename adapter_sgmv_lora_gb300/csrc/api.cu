@@ -276,7 +276,10 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
       }
     }
     const int splits = apply_splits_for(d);
-    if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s))) != LORA_OK) return st;
+    cudaError_t e = cudaErrorNotSupported;
+    if (dec_shrink_ok(d)) e = launch_dec_shrink(d, u, s, splits);
+    if (e == cudaErrorNotSupported) e = launch_shrink_partial_bf16(d, u, s);
+    if ((st = cuda_status(e)) != LORA_OK) return st;
     return cuda_status(launch_expand_bf16(d, u, s, true, splits));
   }
   if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;

@@ -90,6 +90,14 @@ int apply_splits(int end, int in_dim, int nR);
 // *short_ring tells whether the shrink runs its 4-stage ring.
 int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
 
+// The apply's partial-plane shrink for short groups with TMA-fed stages
+// (sgmv_decode.cu): plain batches (no token_rows, no slot ranks), R = 16 or
+// 32, n*R <= 96.  Writes C planes like launch_shrink_partial_bf16.  Returns
+// cudaErrorNotSupported, having launched nothing, when the tensor maps cannot
+// be encoded.
+bool dec_shrink_ok(const ProblemDesc& p);
+cudaError_t launch_dec_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int C);
+
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
 // nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says
 // whether the shape and routing suit it; tc_shrink_splits(end, in, sms) is

@@ -1,32 +1,50 @@
 """SGMV LoRA benchmark: LoRA-routed tokens/s and HBM GB/s vs roofline.
 
-One step = one batch through the whole path: routing (sort + group, built
-per batch on the host), then the SGMV delta on the fused q/k/v projection and
-on o_proj (shrink + boundary-aware expand each).  The default workload is the
-Llama-3-8B-shaped decode batch: hidden 4096, 32 heads, 8 KV heads, head_dim
-128 (fused qkv out 6144, o 4096 -> 4096), 8 adapter slots, max rank 16 (ranks
-8/16), 256 one-token requests, 25% base.
+One step = the SGMV delta of one batch on both problems of a layer: the
+fused q/k/v projection and o_proj (gate+up and down for the MLP workload),
+each one lora_sgmv_apply (shrink + boundary-aware expand).  The batch's
+routing triple is built on the host (lora_build_routing) and uploaded once
+when the inputs are prepared; the timed `value` region holds only the
+applies.  The routing build is timed in `e2e`.
 
-value: device-resident inputs (x, y, stacks, routing triple in HBM); K steps
-       replayed from CUDA graphs over NSETS independent input sets (each set is
-       one layer: its own x, y and A/B stacks) whose total footprint exceeds
-       4x L2, so every step streams from HBM.
-e2e:   the same steps through the Python API with host buffers: per step the
-       host routing build, pinned-host -> device copies of x, y and the triple,
-       the two applies and a device -> host read of both y outputs.
-roofline: the fused-qkv apply (shrink + expand, chained with programmatic
-       dependent launch) timed alone with CUDA events over the rotated sets.
-cpu_baseline / --impl reference: the CPU oracle (plain C, double, one thread)
-       on a bounded sample of the same workload.
+Workloads (seeded synthetic data; see workloads/synthetic.py):
+  mixed70b   the N=1 line (the largest configuration): Llama-3-70B-shaped
+             attention (hidden 8192, 64/8 heads, hd 128; fused qkv 10240,
+             o 8192 -> 8192), 16 slots, max rank 128 (ranks 16/64/128),
+             8192 tokens = 6 prefill requests of 512-1024 plus 1-token
+             decodes, 20% base, bf16.
+  decode8b   secondary block: Llama-3-8B decode (hidden 4096; qkv 6144,
+             o 4096), 8 slots, max rank 16, 256 one-token requests, 25% base.
+  prefill8b  secondary block: ragged prefill, 8B shapes, 4 slots + base,
+             max rank 64, 16 requests of 128-2048 tokens.
+  (many64, mlp8b: --workload only.)
+
+value:   K steps timed exactly, with CUDA events on the launching stream,
+         replayed from CUDA graphs of several steps each (floor(K/NS)
+         replays of one graph over all NS input sets plus one graph of the
+         remaining steps), inputs resident in HBM; NS input sets (the layers
+         of one batch: own x, y, A/B each, one shared routing triple) whose
+         footprint exceeds 4x L2, so each step streams from HBM.
+roofline: per workload, the fused-qkv apply (the larger unit of a step)
+         timed over the rotated sets in 5 trials of >= 30 ms each; achieved
+         = its algorithmic bytes / its median duration.
+e2e:     the main workload's steps through the Python API with host
+         buffers: per step the host routing build, one pinned host->device
+         copy of x, y and the triple, the two applies, one device->host copy
+         of both y outputs.
+cpu_baseline / --impl reference: the CPU oracle (plain C in double) on a
+         bounded sample of the same workload: the OpenMP build on every core
+         of the process's affinity mask, and the single-threaded build.
 
 Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-     [--workload decode8b|many64|prefill8b|mixed70b]
+     [--workload mixed70b|decode8b|prefill8b|many64|mlp8b] [--no-secondary]
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -39,6 +57,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LoRA-routed tokens/sec for SGMV shrink+expand; achieved HBM GB/s vs roofline"
+MAIN_WORKLOAD = "mixed70b"
+SECONDARY = ("decode8b", "prefill8b")
 
 WORKLOAD_DESC = {
     "decode8b": "decode, Llama-3-8B attention (hidden 4096, 32/8 heads, hd 128; fused qkv 6144 + o 4096), "
@@ -123,8 +143,27 @@ def algorithmic_flops(route_host, raw, proj):
     return E * (2 * len(names) * R * k + 2 * R * O)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 class ClockSampler:
-    """nvidia-smi clocks + throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks + throttle reasons sampled every 200 ms while running;
+    summarised over the samples that fall inside the marked timed regions."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -135,7 +174,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []  # (arrival time, csv line)
         self.t = None
-        self.window = None
+        self.windows = []
 
     def start(self):
         try:
@@ -152,9 +191,8 @@ class ClockSampler:
             self.lines.append((time.time(), line.strip()))
 
     def mark(self, t0, t1):
-        """The timed region ran from t0 to t1 (time.time()): only samples taken
-        in it (or the one right after) are summarised, when there are any."""
-        self.window = (t0, t1 + 0.25)
+        """A timed region ran from t0 to t1 (time.time())."""
+        self.windows.append((t0, t1 + 0.25))
 
     def stop(self):
         if self.proc is None:
@@ -166,10 +204,8 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        lines = self.lines
-        if self.window is not None:
-            inside = [(t, ln) for t, ln in lines if self.window[0] <= t <= self.window[1]]
-            lines = inside or lines
+        inside = [(t, ln) for t, ln in self.lines if any(a <= t <= b for a, b in self.windows)]
+        lines = inside or self.lines
         for _, ln in lines:
             p = [v.strip() for v in ln.split(",")]
             if len(p) < 9:
@@ -184,15 +220,15 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm), "window": "timed region" if self.window is not None and
-                len([1 for t, _ in self.lines if self.window[0] <= t <= self.window[1]]) else "whole run"}
+                "samples": len(sm),
+                "window": "timed regions (the K steps and the roofline trials)" if inside else "whole run"}
 
 
 # ----------------------------------------------------------------- oracle --
 
-def oracle_step_sampler(workload, seed, target_s, max_rows=None):
-    """Prepared oracle problems and a callable running the oracle on a sample
-    of routed rows.  Returns (run(rows_per_proj) -> routed rows done, full_rows)."""
+def oracle_step_sampler(workload, seed):
+    """Prepared oracle problems and run(nrows, parallel) running the oracle on
+    the first nrows routed rows of both problems.  Returns (run, end)."""
     import oracle
     from workloads import synthetic as sy
 
@@ -201,10 +237,9 @@ def oracle_step_sampler(workload, seed, target_s, max_rows=None):
     p0, p1 = spec.problems
     probs = [oracle.prepare_problem(raw, p0, fused=spec.fused_qkv), oracle.prepare_problem(raw, p1, fused=True)]
     end = probs[0]["end"]
-    # pre-convert the rows the oracle will read (conversion is not timed)
-    cache = {}
+    cache = {}  # converted rows (conversion is not timed)
 
-    def run(nrows):
+    def run(nrows, parallel=False):
         rows = np.arange(min(nrows, end), dtype=np.int32)
         for p in probs:
             key = (id(p), rows.size)
@@ -218,30 +253,97 @@ def oracle_step_sampler(workload, seed, target_s, max_rows=None):
                 cache[key] = (x_rows, sl)
             x_rows, sl = cache[key]
             oracle.sgmv_rows(rows, x_rows, sl, p["lora_ids"], p["grouped_offsets"], p["end"], p["in_dim"],
-                             p["R"], p["S"])
+                             p["R"], p["S"], parallel=parallel)
         return rows.size
 
     return run, end
 
 
-def cpu_baseline(workload, budget_s=12.0):
-    run, end = oracle_step_sampler(workload, 0, budget_s)
-    run(min(end, 8))  # warm (builds the oracle, converts rows)
+def _time_oracle(run, end, parallel, budget_s):
+    """Routed rows per second of one oracle build on a bounded sample."""
+    probe = min(end, 64 if parallel else 8)
+    run(probe, parallel)  # warm (builds/loads the oracle, converts rows)
     t0 = time.perf_counter()
-    run(min(end, 8))
-    per_row = max((time.perf_counter() - t0) / min(end, 8), 1e-7)
+    run(probe, parallel)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-7)
     nrows = int(max(1, min(end, budget_s / 3 / per_row)))
-    run(nrows)  # convert
+    run(nrows, parallel)  # convert
     reps, done, t0 = 0, 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s and reps < 1000:
-        done += run(nrows)
+        done += run(nrows, parallel)
         reps += 1
     dt = time.perf_counter() - t0
+    return done / dt, nrows, reps, dt
+
+
+def cpu_baseline(workload, budget_s=12.0):
+    """The oracle on the host: the OpenMP build on every core of the affinity
+    mask (the reported value) and the single-threaded build beside it."""
+    import oracle
     from workloads.synthetic import SPECS
-    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d routed rows of one %s batch (%s), %d repetitions, %.1f s, "
-                      "single-threaded C in double" % (nrows, end, workload, " + ".join(SPECS[workload].problems),
-                                                       reps, dt)}
+
+    cores = len(os.sched_getaffinity(0))
+    run, end = oracle_step_sampler(workload, 0)
+    probs = " + ".join(SPECS[workload].problems)
+    v1, n1, r1, d1 = _time_oracle(run, end, False, budget_s / 2)
+    single = {"value": v1, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+              "sample": "first %d of %d routed rows of one %s batch (%s), %d repetitions, %.1f s, "
+                        "single-threaded C in double" % (n1, end, workload, probs, r1, d1)}
+    model = cpu_model()
+    if not oracle.omp_available():
+        single["cpu_model"] = model
+        single["note"] = "no OpenMP build on this host"
+        return single
+    threads = oracle.threads(True, cores)
+    vp, n_p, rp, dp = _time_oracle(run, end, True, budget_s / 2)
+    return {"value": vp, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "first %d of %d routed rows of one %s batch (%s), %d repetitions, %.1f s, OpenMP build "
+                      "of the C oracle (double) over rows on %d threads" % (n_p, end, workload, probs, rp, dp, threads),
+            "cpu_model": model, "affinity_cores": cores, "single_thread": single}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle (OpenMP build, all cores of the
+    affinity mask) timed on a bounded per-step sample of the workload."""
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return 0
+    import oracle
+    if args.steps <= 0:
+        args.steps = 20
+    cores = len(os.sched_getaffinity(0))
+    parallel = oracle.omp_available()
+    threads = oracle.threads(True, cores) if parallel else 1
+    run, end = oracle_step_sampler(args.workload, 0)
+    probe = min(end, 64 if parallel else 4)
+    run(probe, parallel)
+    t0 = time.perf_counter()
+    run(probe, parallel)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-7)
+    steps_total = args.steps + args.warmup
+    nrows = int(max(1, min(end, 150.0 / steps_total / per_row)))
+    run(nrows, parallel)
+    for _ in range(args.warmup):
+        run(nrows, parallel)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += run(nrows, parallel)
+    dt = time.perf_counter() - t0
+    val = done / dt
+    kind = ("OpenMP build of the C oracle (double) on %d threads" % threads) if parallel else \
+        "single-threaded C oracle (double)"
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload]},
+           "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                            "sample": "first %d of %d routed rows per step (%s), %s"
+                                      % (nrows, end, " + ".join(_spec_problems(args.workload)), kind),
+                            "cpu_model": cpu_model()},
+           "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
 
 
 def _spec_problems(workload):
@@ -249,46 +351,202 @@ def _spec_problems(workload):
     return SPECS[workload].problems
 
 
-def run_reference(args):
-    rank, world, _ = _env_rank()
-    if rank != 0:
-        return 0
-    if args.steps <= 0:
-        args.steps = 20
-    run, end = oracle_step_sampler(args.workload, 0, 0)
-    run(min(end, 4))
-    t0 = time.perf_counter()
-    run(min(end, 4))
-    per_row = max((time.perf_counter() - t0) / min(end, 4), 1e-7)
-    steps_total = args.steps + args.warmup
-    nrows = int(max(1, min(end, 150.0 / steps_total / per_row)))
-    run(nrows)
-    for _ in range(args.warmup):
-        run(nrows)
-    t0 = time.perf_counter()
-    done = 0
-    for _ in range(args.steps):
-        done += run(nrows)
-    dt = time.perf_counter() - t0
-    val = done / dt
-    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload]},
-           "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                            "sample": "%d of %d routed rows per step (%s), single-threaded C in double"
-                                      % (nrows, end, " + ".join(_spec_problems(args.workload)))},
-           "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(out))
-    return 0
-
-
 # -------------------------------------------------------------- GPU arm --
+
+class WorkloadBench:
+    """Input sets, pre-marshalled calls and CUDA graphs of one workload."""
+
+    def __init__(self, name, args, rank, lk, torch, stream, l2, max_sets=64):
+        from workloads import device, synthetic as sy
+        self.name, self.torch, self.stream, self.lk = name, torch, stream, lk
+        spec = sy.SPECS[name]
+        self.P0, self.P1 = spec.problems
+        sets, foot = [], 0
+        # Input sets are the layers of one batch: each has its own x, y and
+        # adapter stacks, and (as in one decode step) all share the batch's
+        # routing triple, built and uploaded once.
+        while len(sets) < max_sets:
+            share = bool(sets)
+            raw = sy.draw(spec, rank_seed(rank, len(sets)),
+                          requests=(sets[0]["raw"]["req_slot"], sets[0]["raw"]["req_len"]) if share else None)
+            shared = (sets[0]["p0"]["route_host"], sets[0]["p0"]["routing"]) if share else None
+            d0 = device.prepare(raw, self.P0, fused=spec.fused_qkv, slot_ranks=args.slot_ranks,
+                                shared_routing=shared)
+            d1 = device.prepare(raw, self.P1, slot_ranks=args.slot_ranks,
+                                shared_routing=(d0["route_host"], d0["routing"]))
+            b0 = algorithmic_bytes(d0["route_host"], raw, self.P0, slot_ranks=args.slot_ranks)
+            b1 = algorithmic_bytes(d1["route_host"], raw, self.P1, slot_ranks=args.slot_ranks)
+            sets.append({"raw": raw, "p0": d0, "p1": d1, "bytes": b0 + b1, "b0": b0, "b1": b1,
+                         "f0": algorithmic_flops(d0["route_host"], raw, self.P0), "E": d0["route_host"]["end"]})
+            foot += b0 + b1
+            if foot >= 4 * l2 and len(sets) >= 2:
+                break
+        self.sets, self.NS, self.foot = sets, len(sets), foot
+        for s in sets:
+            s["call0"] = lk.CallBuilder(s["p0"]["problem"], s["p0"]["routing"], s["p0"]["workspace"])
+            s["call1"] = lk.CallBuilder(s["p1"]["problem"], s["p1"]["routing"], s["p1"]["workspace"])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):  # eager warm (first-launch attribute setup)
+            for s in sets:
+                s["call0"].apply(stream)
+                s["call1"].apply(stream)
+        stream.synchronize()
+        self.launches_per_step = sets[0]["call0"].last_launches + sets[0]["call1"].last_launches
+        self.path_bits = (sets[0]["call0"].last_path, sets[0]["call1"].last_path)
+        self.g_all = self._graph(lambda st: [self._step(i, st) for i in range(self.NS)])
+        self.g_p0 = self._graph(lambda st: [s["call0"].apply(st) for s in sets])
+        self.g_p1 = self._graph(lambda st: [s["call1"].apply(st) for s in sets])
+        self.nwarm = 20  # set 0's first-problem apply, back to back: inputs stay in L2
+        self.g_warm = self._graph(lambda st: [sets[0]["call0"].apply(st) for _ in range(self.nwarm)])
+        self.g_rem = {}
+
+    def _step(self, i, st):
+        s = self.sets[i % self.NS]
+        s["call0"].apply(st)
+        s["call1"].apply(st)
+
+    def _graph(self, body):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            body(torch.cuda.current_stream())
+        return g
+
+    def prepare_steps(self, k):
+        """Capture (outside any timed region) the graph of k mod NS steps."""
+        r = k % self.NS
+        if r and r not in self.g_rem:
+            self.g_rem[r] = self._graph(lambda st: [self._step(i, st) for i in range(r)])
+
+    def run_steps(self, k):
+        """k steps over sets 0, 1, ..., from multi-step graphs (k // NS replays
+        of the all-sets graph, then one graph of the remaining steps)."""
+        for _ in range(k // self.NS):
+            self.g_all.replay()
+        r = k % self.NS
+        if r:
+            self.g_rem[r].replay()
+
+    def steps_tokens_bytes(self, k):
+        return (sum(self.sets[i % self.NS]["E"] for i in range(k)),
+                sum(self.sets[i % self.NS]["bytes"] for i in range(k)))
+
+    def trials(self, graph, units, min_ms=30.0, n=5, sampler=None):
+        """n trials, each replaying `graph` (units apply/step units per replay)
+        enough times to last >= min_ms; per-unit ms of each trial."""
+        torch, st = self.torch, self.stream
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            graph.replay()
+            e0.record(st)
+            graph.replay()
+            e1.record(st)
+        torch.cuda.synchronize()
+        one = max(e0.elapsed_time(e1), 1e-3)
+        reps = int(max(1, min(100000, min_ms / one)))
+        out = []
+        for _ in range(n):
+            w0 = time.time()
+            with torch.cuda.stream(st):
+                e0.record(st)
+                for _ in range(reps):
+                    graph.replay()
+                e1.record(st)
+            torch.cuda.synchronize()
+            if sampler:
+                sampler.mark(w0, time.time())
+            out.append(e0.elapsed_time(e1) / (reps * units))
+        return out
+
+
+def roofline_block(wb, trials_ms, peak, peak_kind, tpeak, tpeak_kind, traffic):
+    med = statistics.median(trials_ms)
+    qbytes = statistics.mean(s["b0"] for s in wb.sets)
+    qflops = statistics.mean(s["f0"] for s in wb.sets)
+    achieved = qbytes / (med * 1e-3) / 1e9
+    multi = len(_names(wb.P0)) > 1
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": "%s SGMV apply (shrink + expand)" % (("fused-" + wb.P0) if multi else wb.P0),
+            "peak_source": ("%s HBM copy bandwidth (MEASURED_PEAKS.json)" % peak_kind) if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": int(qbytes), "avg_launch_us": round(med * 1e3, 3),
+            "trials_us": [round(t * 1e3, 3) for t in trials_ms],
+            "spread_us": round((max(trials_ms) - min(trials_ms)) * 1e3, 3),
+            "flops_per_launch": int(qflops),
+            "t_hbm_us": round(qbytes / (peak * 1e9) * 1e6, 3),
+            "t_tensor_us": round(qflops / (tpeak * 1e12) * 1e6, 3),
+            "tensor_peak_tflops": tpeak,
+            "tensor_peak_source": ("%s bf16 dense (MEASURED_PEAKS.json)" % tpeak_kind) if tpeak_kind == "measured"
+            else "fallback 1.9 PFLOP/s"}
+
+
+def _profiled_traffic(workload):
+    """DRAM bytes per fused-qkv apply from the committed ncu summary, if present
+    and taken on the kernels as they are now."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.json" % workload)
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+        except (OSError, ValueError):
+            return None
+        if d.get("stale"):
+            return None
+        return d.get("dram_bytes_per_qkv_apply")
+    return None
+
+
+def workload_summary(wb, sampler, peaks):
+    """Secondary block: step and per-projection times, roofline of the first
+    problem's apply (median of 5 trials), warm-L2 time."""
+    peak, peak_kind, tpeak, tpeak_kind = peaks
+    step_ms = wb.trials(wb.g_all, wb.NS, sampler=sampler)
+    q_ms = wb.trials(wb.g_p0, wb.NS, sampler=sampler)
+    o_ms = wb.trials(wb.g_p1, wb.NS, sampler=sampler)
+    w_ms = wb.trials(wb.g_warm, wb.nwarm, min_ms=10.0, n=3)
+    med_step = statistics.median(step_ms)
+    tokens = statistics.mean(s["E"] for s in wb.sets)
+    ob = statistics.mean(s["b1"] for s in wb.sets)
+    med_o = statistics.median(o_ms)
+    med_w = statistics.median(w_ms)
+    return {
+        "desc": WORKLOAD_DESC[wb.name],
+        "tokens_per_s": round(tokens / (med_step * 1e-3), 1), "routed_tokens_per_step": tokens,
+        "ms_per_step": round(med_step, 5), "step_trials_us": [round(t * 1e3, 3) for t in step_ms],
+        "input_sets": wb.NS, "footprint_MB": round(wb.foot / 1e6, 1),
+        "roofline": roofline_block(wb, q_ms, peak, peak_kind, tpeak, tpeak_kind, _profiled_traffic(wb.name)),
+        "per_projection": {
+            wb.P0: {"avg_apply_us": round(statistics.median(q_ms) * 1e3, 3),
+                    "GBps": round(statistics.mean(s["b0"] for s in wb.sets) / (statistics.median(q_ms) * 1e-3) / 1e9,
+                                  1)},
+            wb.P1: {"avg_apply_us": round(med_o * 1e3, 3), "GBps": round(ob / (med_o * 1e-3) / 1e9, 1)}},
+        "warm_l2": {"avg_apply_us": round(med_w * 1e3, 3),
+                    "GBps": round(wb.sets[0]["b0"] / (med_w * 1e-3) / 1e9, 1),
+                    "note": "%s apply of input set 0, %d back to back per graph replay: inputs in L2, not an HBM "
+                            "number" % (wb.P0, wb.nwarm)},
+        "kernel_paths": [hex(b) for b in wb.path_bits], "launches_per_step": wb.launches_per_step,
+    }
+
+
+def spawn_replicas(args):
+    """--gpus N > 1 without a launcher: start N ranks with torch.distributed.run."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(args.gpus),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.run(cmd).returncode
+
 
 def run_ours(args):
     import torch
 
     rank, world, local = _env_rank()
+    if args.gpus > 1 and world == 1:
+        return spawn_replicas(args)
+    if world > 1 and args.gpus != world:
+        raise SystemExit("--gpus %d but WORLD_SIZE=%d" % (args.gpus, world))
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -300,108 +558,36 @@ def run_ours(args):
     import __graft_entry__ as ge
     ge.build()
     import adapter_sgmv_lora_gb300 as lk
-    from workloads import device, synthetic as sy
 
-    spec = sy.SPECS[args.workload]
-    P0, P1 = spec.problems  # e.g. fused qkv and o_proj, or fused gate+up and down
     props = torch.cuda.get_device_properties(dev_idx)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20)
-
-    # ---- input sets (one per simulated layer), sized to exceed 4x L2
-    sets = []
-    foot = 0
-    max_sets = args.sets or 64
-    while len(sets) < max_sets:
-        # Input sets are the layers of one batch: each has its own x, y and
-        # adapter stacks, and (as in a decode step) all share the batch's
-        # routing triple, built and uploaded once.  --per-set-routing draws an
-        # independent batch per set instead.
-        share = bool(sets) and not args.per_set_routing
-        raw = sy.draw(spec, rank_seed(rank, len(sets)),
-                      requests=(sets[0]["raw"]["req_slot"], sets[0]["raw"]["req_len"]) if share else None)
-        shared = (sets[0]["p0"]["route_host"], sets[0]["p0"]["routing"]) if share else None
-        d0 = device.prepare(raw, P0, fused=spec.fused_qkv, slot_ranks=args.slot_ranks, shared_routing=shared)
-        if not args.per_set_routing:
-            shared = (d0["route_host"], d0["routing"])
-        d1 = device.prepare(raw, P1, slot_ranks=args.slot_ranks, shared_routing=shared)
-        b = (algorithmic_bytes(d0["route_host"], raw, P0, slot_ranks=args.slot_ranks) +
-             algorithmic_bytes(d1["route_host"], raw, P1, slot_ranks=args.slot_ranks))
-        sets.append({"raw": raw, "p0": d0, "p1": d1, "bytes": b, "E": d0["route_host"]["end"]})
-        foot += b
-        if not args.sets and foot >= 4 * l2 and len(sets) >= 2:
-            break
-    NS = len(sets)
-    for s in sets:
-        s["call_qkv"] = lk.CallBuilder(s["p0"]["problem"], s["p0"]["routing"], s["p0"]["workspace"])
-        s["call_o"] = lk.CallBuilder(s["p1"]["problem"], s["p1"]["routing"], s["p1"]["workspace"])
     stream = torch.cuda.Stream()
-    torch.cuda.synchronize()
+    peak, peak_kind = _peaks()
+    tpeak, tpeak_kind = _tensor_peak()
+    peaks = (peak, peak_kind, tpeak, tpeak_kind)
 
-    def step(i, st):
-        s = sets[i % NS]
-        s["call_qkv"].apply(st)
-        s["call_o"].apply(st)
-
-    # ---- CUDA graphs: one over all NS sets, plus one per set for remainders
+    wb = WorkloadBench(args.workload, args, rank, lk, torch, stream, l2, max_sets=args.sets or 64)
+    NS = wb.NS
     with torch.cuda.stream(stream):
-        for i in range(NS):  # eager warm (first-launch attribute setup)
-            step(i, stream)
-    stream.synchronize()
-    g_all = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_all, stream=stream):
-        for i in range(NS):
-            step(i, torch.cuda.current_stream())
-    g_one = []
-    for i in range(NS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(i, torch.cuda.current_stream())
-        g_one.append(g)
-    g_qkv = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_qkv, stream=stream):
-        for i in range(NS):
-            sets[i]["call_qkv"].apply(torch.cuda.current_stream())
-    g_o = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_o, stream=stream):
-        for i in range(NS):
-            sets[i]["call_o"].apply(torch.cuda.current_stream())
-    nwarm = 20  # set 0's fused-qkv apply, nwarm times in one graph: inputs stay in L2
-    g_warm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_warm, stream=stream):
-        for _ in range(nwarm):
-            sets[0]["call_qkv"].apply(torch.cuda.current_stream())
-
-    def run_steps(k, start=0):
-        i = 0
-        while k - i >= NS and (start + i) % NS == 0:
-            g_all.replay()
-            i += NS
-        while i < k:
-            g_one[(start + i) % NS].replay()
-            i += 1
-
-    with torch.cuda.stream(stream):
-        run_steps(max(args.warmup, 3))
+        for _ in range(max(args.warmup, 3)):
+            wb.g_all.replay()
     stream.synchronize()
 
     if args.steps <= 0:
-        # Default: about one second of timed work (at least 640 steps), so
-        # the clock samples fall inside the timed region.
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            p0.record(stream)
-            run_steps(NS)
-            p1.record(stream)
-        torch.cuda.synchronize()
-        per_step = max(p0.elapsed_time(p1) / NS, 1e-4)
-        k = int(min(200000, max(640, 1000.0 / per_step)))
+        # Default: about one second of timed work (at least 640 steps).
+        per = statistics.median(wb.trials(wb.g_all, NS, min_ms=20.0, n=3))
+        k = int(min(200000, max(640, 1000.0 / max(per, 1e-4))))
         if dist:
             kt = torch.tensor([k], device="cuda")
             dist.all_reduce(kt, op=dist.ReduceOp.MAX)
             k = int(kt.item())
         args.steps = k
+    wb.prepare_steps(args.steps)
+    with torch.cuda.stream(stream):  # warm-up steps, W >= 3
+        wb.run_steps(max(args.warmup, 3))
+    stream.synchronize()
 
-    # ---- timed region
+    # ---- timed region: exactly K steps
     sampler = ClockSampler(dev_idx) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -413,7 +599,7 @@ def run_ours(args):
     wall0 = time.time()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        run_steps(args.steps)
+        wb.run_steps(args.steps)
         ev1.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -421,97 +607,57 @@ def run_ours(args):
     if dist:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
-    tokens = sum(sets[i % NS]["E"] for i in range(args.steps))
-    bytes_steps = sum(sets[i % NS]["bytes"] for i in range(args.steps))
+    tokens, bytes_steps = wb.steps_tokens_bytes(args.steps)
 
-    # ---- roofline unit: fused-qkv apply alone, over the rotated sets
-    reps = max(1, (args.steps + NS - 1) // NS)
-    with torch.cuda.stream(stream):
-        g_qkv.replay()
-        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        r0.record(stream)
-        for _ in range(reps):
-            g_qkv.replay()
-        r1.record(stream)
-    torch.cuda.synchronize()
-    qkv_ms = r0.elapsed_time(r1) / (reps * NS)
-    qkv_bytes = statistics.mean(algorithmic_bytes(s["p0"]["route_host"], s["raw"], P0, slot_ranks=args.slot_ranks)
-                                for s in sets)
-    qkv_flops = statistics.mean(algorithmic_flops(s["p0"]["route_host"], s["raw"], P0) for s in sets)
-
-    # ---- per projection: the second problem's apply alone, the same way
-    with torch.cuda.stream(stream):
-        g_o.replay()
-        r0.record(stream)
-        for _ in range(reps):
-            g_o.replay()
-        r1.record(stream)
-    torch.cuda.synchronize()
-    o_ms = r0.elapsed_time(r1) / (reps * NS)
-    o_bytes = statistics.mean(algorithmic_bytes(s["p1"]["route_host"], s["raw"], P1, slot_ranks=args.slot_ranks)
-                              for s in sets)
-
-    # ---- warm L2: set 0's fused-qkv apply back to back (its inputs stay in L2)
-    wreps = 5
-    with torch.cuda.stream(stream):
-        g_warm.replay()
-        r0.record(stream)
-        for _ in range(wreps):
-            g_warm.replay()
-        r1.record(stream)
-    torch.cuda.synchronize()
-    warm_ms = r0.elapsed_time(r1) / (wreps * nwarm)
-    warm_bytes = algorithmic_bytes(sets[0]["p0"]["route_host"], sets[0]["raw"], P0, slot_ranks=args.slot_ranks)
-    clocks = sampler.stop() if sampler else None
-
-    (ms, qkv_ms), (tokens,) = reduce_across_ranks([ms, qkv_ms], [tokens], dist, "cuda")
+    # ---- roofline and per-projection figures of the main workload
+    main = workload_summary(wb, sampler, peaks)
+    (ms,), (tokens,) = reduce_across_ranks([ms], [tokens], dist, "cuda")
 
     # ---- e2e through the public API with host buffers
-    e2e = run_e2e(args, sets, lk, torch, stream, dist)
+    e2e = run_e2e(args, wb.sets, lk, torch, stream, dist)
+
+    # ---- secondary workloads (rank 0 of N=1 runs only: the scaling run times the main one)
+    secondary = {}
+    if not args.no_secondary and world == 1:
+        for name in SECONDARY:
+            if name == args.workload:
+                continue
+            sb = WorkloadBench(name, args, rank, lk, torch, stream, l2)
+            secondary[name] = workload_summary(sb, sampler, peaks)
+            del sb
+            torch.cuda.empty_cache()
+    clocks = sampler.stop() if sampler else None
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
-    peak, peak_kind = _peaks()
-    tpeak, tpeak_kind = _tensor_peak()
-    achieved = qkv_bytes / (qkv_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic(args.workload)
+    cfg = {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload], "input_sets": NS,
+           "footprint_MB": round(wb.foot / 1e6, 1), "l2_MB": round(l2 / 2 ** 20, 1),
+           "l2_policy": "inputs larger than L2: %d rotated input sets, %.0f MB > 4x L2" % (NS, wb.foot / 1e6),
+           "routing": "one batch: the input sets are its layers (own x, y, A/B each) sharing one routing triple",
+           "parallelism": "replicas" if world > 1 else "single GPU",
+           "slot_ranks": "true ranks passed (A/B bytes counted at ceil16(rank))" if args.slot_ranks
+           else "padded to max_lora_rank",
+           "timing": "K steps from multi-step CUDA graphs: %d replays of a %d-step graph + one %d-step graph"
+                     % (args.steps // NS, NS, args.steps % NS),
+           "hbm_GBps_step": round(bytes_steps / (ms * 1e-3) / 1e9, 1),
+           "routed_tokens_per_step": tokens / args.steps / max(world, 1)}
     out = {
         "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random adapters, activations and base outputs)",
-        "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload], "input_sets": NS,
-                   "footprint_MB": round(foot / 1e6, 1), "l2_MB": round(l2 / 2 ** 20, 1),
-                   "l2_policy": "inputs larger than L2: %d rotated input sets, %.0f MB > 4x L2" % (NS, foot / 1e6),
-                   "routing": "independent batch per input set" if args.per_set_routing else
-                   "one batch: the input sets are its layers (own x, y, A/B each) sharing one routing triple",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "slot_ranks": "true ranks passed (A/B bytes counted at ceil16(rank))" if args.slot_ranks
-                   else "padded to max_lora_rank",
-                   "hbm_GBps_step": round(bytes_steps / (ms * 1e-3) / 1e9, 1),
-                   "routed_tokens_per_step": tokens / args.steps / max(world, 1)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "%s SGMV apply (shrink + expand, PDL-chained)" % ("fused-" + P0 if len(_names(P0)) > 1 else P0),
-                     "peak_source": "%s HBM copy bandwidth (MEASURED_PEAKS.json)" % peak_kind
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": int(qkv_bytes), "avg_launch_us": round(qkv_ms * 1e3, 3),
-                     "flops_per_launch": int(qkv_flops),
-                     "t_hbm_us": round(qkv_bytes / (peak * 1e9) * 1e6, 3),
-                     "t_tensor_us": round(qkv_flops / (tpeak * 1e12) * 1e6, 3),
-                     "tensor_peak_tflops": tpeak, "tensor_peak_source": "%s bf16 dense (MEASURED_PEAKS.json)" % tpeak_kind
-                     if tpeak_kind == "measured" else "fallback 1.9 PFLOP/s"},
-        "per_projection": {
-            P0: {"avg_apply_us": round(qkv_ms * 1e3, 3), "GBps": round(qkv_bytes / (qkv_ms * 1e-3) / 1e9, 1)},
-            P1: {"avg_apply_us": round(o_ms * 1e3, 3), "GBps": round(o_bytes / (o_ms * 1e-3) / 1e9, 1)}},
-        "warm_l2": {"unit": "%s apply of input set 0, %d back to back per graph replay" % (P0, nwarm),
-                    "avg_apply_us": round(warm_ms * 1e3, 3),
-                    "GBps": round(warm_bytes / (warm_ms * 1e-3) / 1e9, 1),
-                    "note": "inputs resident in L2 after the first replay: not an HBM number"},
+        "config": cfg,
+        "roofline": main["roofline"],
+        "per_projection": main["per_projection"],
+        "step_trials": {"ms_per_step_median": main["ms_per_step"], "trials_us": main["step_trials_us"],
+                        "note": "5 trials of >= 30 ms of the same steps, for comparison with the K-step region"},
+        "warm_l2": main["warm_l2"],
+        "kernel_paths": main["kernel_paths"],
+        "secondary": secondary,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": wb.launches_per_step * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -520,17 +666,6 @@ def run_ours(args):
     if dist:
         dist.destroy_process_group()
     return 0
-
-
-def _profiled_traffic(workload):
-    """DRAM bytes per fused-qkv apply from the committed ncu summary, if present."""
-    path = os.path.join(ROOT, "profiles", "traffic_%s.json" % workload)
-    if os.path.exists(path):
-        try:
-            return json.load(open(path)).get("dram_bytes_per_qkv_apply")
-        except (OSError, ValueError):
-            return None
-    return None
 
 
 def run_e2e(args, sets, lk, torch, stream, dist):
@@ -656,14 +791,13 @@ def main():
                     help="timed steps (0: about one second of work, at least 640)")
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode8b", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--workload", default=MAIN_WORKLOAD, choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the decode8b / prefill8b blocks")
     ap.add_argument("--slot-ranks", action="store_true",
                     help="pass the adapters' true ranks so the kernels skip the rank padding")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--per-set-routing", action="store_true",
-                    help="draw an independent batch (own routing triple) for every input set")
+    ap.add_argument("--cpu-budget", type=float, default=16.0)
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

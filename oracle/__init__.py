@@ -73,6 +73,8 @@ def _bind(L):
                                    ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
                                    ctypes.c_longlong, i32p, i32p, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_void_p]
+    L.oracle_threads.restype = ctypes.c_int
+    L.oracle_threads.argtypes = [ctypes.c_int]
     L.oracle_sgmv_token_slots.restype = ctypes.c_int
     L.oracle_sgmv_token_slots.argtypes = [ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
@@ -97,6 +99,12 @@ def lib(parallel: bool = False):
 
 def omp_available() -> bool:
     return _build.omp_path() is not None
+
+
+def threads(parallel: bool, n: int = 0) -> int:
+    """Threads the (parallel or single-threaded) build runs its row loops on;
+    n > 0 sets the OpenMP build's count first."""
+    return int(lib(parallel).oracle_threads(int(n)))
 
 
 def _i32(a):

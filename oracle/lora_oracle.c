@@ -39,6 +39,21 @@
 #include <limits.h>
 #include <stddef.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the row loops below run on: 1 in the single-threaded build; in the
+ * OpenMP build, n > 0 first sets the count.  No arithmetic depends on it. */
+int oracle_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
 
 /* Status codes of the oracle (independent of the library's own codes). */
 enum {

@@ -8,8 +8,8 @@ library cannot be loaded, every call raises.
 
 Names follow the C ABI: ``lora_build_routing``, ``lora_set_slot``,
 ``lora_shrink``, ``lora_expand``, ``lora_workspace_bytes``,
-``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_get_device_status``,
-``lora_last_call_path``, ``lora_status_string``.
+``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_workspace_init``,
+``lora_get_device_status``, ``lora_last_call_path``, ``lora_status_string``.
 """
 from __future__ import annotations
 
@@ -106,6 +106,10 @@ def lib():
     L.lora_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.lora_status_string.restype = ctypes.c_char_p
     L.lora_status_string.argtypes = [ctypes.c_int]
+    L.lora_workspace_init.restype = ctypes.c_int
+    L.lora_workspace_init.argtypes = [vp, ctypes.c_size_t, vp]
+    L.lora_selftest_handoff.restype = ctypes.c_int
+    L.lora_selftest_handoff.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64, vp]
     L.lora_last_call_path.restype = ctypes.c_uint32
     L.lora_last_call_path.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.lora_selftest_wait_timeout.restype = ctypes.c_int
@@ -323,6 +327,31 @@ def lora_expand(problem: Problem, routing: Routing, u, stream=None) -> None:
 def lora_workspace_bytes(problem: Problem, end: int) -> int:
     c = problem._c()
     return int(lib().lora_workspace_bytes(ctypes.byref(c), int(end)))
+
+
+WORKSPACE_CTRL_BYTES = 4096
+
+
+def lora_workspace_init(workspace, stream=None) -> None:
+    """Zero-fill a workspace tensor (required once before its first
+    lora_sgmv_apply; every call leaves its counter bytes zero again)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().lora_workspace_init(workspace.data_ptr(), nbytes, _stream_handle(stream)), "lora_workspace_init")
+
+
+def new_workspace(problem: Problem, end: int, device="cuda"):
+    """A zero-filled workspace tensor of lora_workspace_bytes(problem, end)."""
+    import torch
+    nbytes = lora_workspace_bytes(problem, end)
+    return torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.float32, device=device)
+
+
+def lora_selftest_handoff(workspace, polls: int, delay_ns: int, stream=None) -> None:
+    """Failure-path self test of the one-launch apply's counter handoff (see
+    include/lora_sgmv.h)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().lora_selftest_handoff(workspace.data_ptr(), nbytes, int(polls), int(delay_ns),
+                                       _stream_handle(stream)), "lora_selftest_handoff")
 
 
 def lora_sgmv_apply(problem: Problem, routing: Routing, workspace, stream=None) -> None:

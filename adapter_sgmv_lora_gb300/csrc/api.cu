@@ -158,7 +158,7 @@ size_t ws_bytes(const lora_problem_t* p, int32_t end) {
                (size_t)p->max_lora_rank * 4;
   const size_t packed = tc_packed_bytes(p->max_num_loras, end, p->num_slices, p->max_lora_rank);
   if (packed > raw) raw = packed;
-  return (raw + 255) & ~(size_t)255;
+  return (size_t)kWorkspaceCtrlBytes + ((raw + 255) & ~(size_t)255);
 }
 
 }  // namespace
@@ -261,10 +261,12 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
   ProblemDesc d = make_desc(problem, routing);
   if (!d.status) return LORA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* u = static_cast<float*>(workspace);
+  unsigned* ctrl = static_cast<unsigned*>(workspace);
+  void* inter = static_cast<uint8_t*>(workspace) + kWorkspaceCtrlBytes;
+  float* u = static_cast<float*>(inter);
   if (fast_path_ok(d, u)) {
     if (tc_expand_ok(d)) {
-      const cudaError_t e = launch_tc_apply_packed(d, workspace, s);
+      const cudaError_t e = launch_tc_apply_packed(d, inter, s);
       if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     if (tc_shrink_ok(d)) {
@@ -277,6 +279,10 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
     }
     const int splits = apply_splits_for(d);
     cudaError_t e = cudaErrorNotSupported;
+    if (dec_apply_ok(d)) {
+      e = launch_dec_apply(d, u, ctrl, s, splits);
+      if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
     if (dec_shrink_ok(d)) e = launch_dec_shrink(d, u, s, splits);
     if (e == cudaErrorNotSupported) e = launch_shrink_partial_bf16(d, u, s);
     if ((st = cuda_status(e)) != LORA_OK) return st;
@@ -307,6 +313,26 @@ extern "C" lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* 
 extern "C" uint32_t lora_last_call_path(uint32_t* num_launches) {
   if (num_launches) *num_launches = t_launches;
   return t_path_bits;
+}
+
+extern "C" lora_status_t lora_workspace_init(void* workspace, size_t workspace_bytes, lora_stream_t stream) {
+  begin_call();
+  if (!workspace) return LORA_ERR_NULL;
+  if (workspace_bytes < (size_t)kWorkspaceCtrlBytes) return LORA_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" lora_status_t lora_selftest_handoff(void* workspace, size_t workspace_bytes, uint32_t polls,
+                                               uint64_t delay_ns, lora_stream_t stream) {
+  begin_call();
+  if (!workspace) return LORA_ERR_NULL;
+  if (workspace_bytes < (size_t)kWorkspaceCtrlBytes) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return LORA_ERR_ALIGN;
+  if (delay_ns > 100000000ull) return LORA_ERR_SHAPE;  // at most 0.1 s
+  unsigned* p = status_ptr();
+  if (!p) return LORA_ERR_CUDA;
+  return cuda_status(launch_selftest_handoff(static_cast<unsigned*>(workspace), p, polls, delay_ns,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" lora_status_t lora_selftest_wait_timeout(uint32_t polls, lora_stream_t stream) {

@@ -98,6 +98,23 @@ int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
 bool dec_shrink_ok(const ProblemDesc& p);
 cudaError_t launch_dec_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int C);
 
+// The workspace of lora_sgmv_apply starts with kWorkspaceCtrlBytes of
+// per-tile counters (zero before the first call, left zero by every call);
+// the intermediate follows.
+constexpr int kWorkspaceCtrlBytes = 4096;
+constexpr int kWorkspaceCtrlWords = kWorkspaceCtrlBytes / 4;
+// The one-launch apply for decode-sized batches (sgmv_decode.cu): plain
+// batches (no token_rows, slot ranks or bias), R = 16 or 32, n*R <= 96,
+// groups of at most 64 routed rows on average.  C K splits write C planes at
+// u, handed to the expand items through the counters at ctrl.  Returns
+// cudaErrorNotSupported, having launched nothing, when the tensor maps cannot
+// be encoded or the grid could not be resident.
+bool dec_apply_ok(const ProblemDesc& p);
+cudaError_t launch_dec_apply(const ProblemDesc& p, float* u, unsigned* ctrl, cudaStream_t s, int C);
+// Failure-path self test of the counter handoff (lora_selftest_handoff).
+cudaError_t launch_selftest_handoff(unsigned* ctrl, unsigned* status, uint32_t polls, uint64_t delay_ns,
+                                    cudaStream_t s);
+
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
 // nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says
 // whether the shape and routing suit it; tc_shrink_splits(end, in, sms) is

@@ -8,7 +8,7 @@ library cannot be loaded, every call raises.
 
 Names follow the C ABI: ``lora_build_routing``, ``lora_set_slot``,
 ``lora_shrink``, ``lora_expand``, ``lora_workspace_bytes``,
-``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_workspace_init``,
+``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_base_gemm_apply``, ``lora_workspace_init``,
 ``lora_get_device_status``, ``lora_last_call_path``, ``lora_status_string``.
 """
 from __future__ import annotations
@@ -55,6 +55,10 @@ class _Problem(ctypes.Structure):
                 ("max_num_loras", ctypes.c_int32), ("max_lora_rank", ctypes.c_int32),
                 ("x", ctypes.c_void_p), ("x_row_stride", ctypes.c_int64),
                 ("num_slices", ctypes.c_int32), ("slices", _Slice * MAX_SLICES), ("slot_ranks", ctypes.c_void_p)]
+
+
+class _BaseWeight(ctypes.Structure):
+    _fields_ = [("W0", ctypes.c_void_p), ("row_stride", ctypes.c_int64)]
 
 
 class _Routing(ctypes.Structure):
@@ -106,6 +110,9 @@ def lib():
     L.lora_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.lora_status_string.restype = ctypes.c_char_p
     L.lora_status_string.argtypes = [ctypes.c_int]
+    L.lora_base_gemm_apply.restype = ctypes.c_int
+    L.lora_base_gemm_apply.argtypes = [ctypes.POINTER(_Problem), ctypes.POINTER(_Routing),
+                                       ctypes.POINTER(_BaseWeight), vp, ctypes.c_size_t, vp]
     L.lora_workspace_init.restype = ctypes.c_int
     L.lora_workspace_init.argtypes = [vp, ctypes.c_size_t, vp]
     L.lora_selftest_handoff.restype = ctypes.c_int
@@ -361,6 +368,30 @@ def lora_sgmv_apply(problem: Problem, routing: Routing, workspace, stream=None) 
     _check(L.lora_sgmv_apply(ctypes.byref(c), ctypes.byref(rr),
                              workspace.data_ptr() if workspace is not None else None, nbytes,
                              _stream_handle(stream)), "lora_sgmv_apply")
+
+
+def lora_base_gemm_apply(problem: Problem, routing: Routing, W0, workspace, stream=None) -> None:
+    """The delta fused into the base projection: every row of each slice's
+    y becomes W0_j x (+ the LoRA delta on routed rows), rounded once; y is
+    written, not read.  W0: one device tensor [out_j, in] per slice (same
+    dtype as x), or (tensor, element offset, row stride) tuples."""
+    L = lib()
+    c, rr = problem._c(), routing._c()
+    arr = (_BaseWeight * MAX_SLICES)()
+    if len(W0) != len(problem.slices):
+        raise ValueError("one base weight per slice")
+    for j, w in enumerate(W0):
+        if isinstance(w, tuple):
+            t, off, stride = w
+        else:
+            t, off, stride = w, 0, w.stride(0)
+        if t.dtype != problem.x.dtype:
+            raise ValueError("W0 must have the dtype of x")
+        arr[j] = _BaseWeight(t.data_ptr() + t.element_size() * int(off), int(stride))
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(L.lora_base_gemm_apply(ctypes.byref(c), ctypes.byref(rr), arr,
+                                  workspace.data_ptr() if workspace is not None else None, nbytes,
+                                  _stream_handle(stream)), "lora_base_gemm_apply")
 
 
 NOALLOC_MAX_WORKSPACE_BYTES = 16 * 1024 * 1024

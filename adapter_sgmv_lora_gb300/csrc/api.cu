@@ -315,6 +315,55 @@ extern "C" uint32_t lora_last_call_path(uint32_t* num_launches) {
   return t_path_bits;
 }
 
+extern "C" lora_status_t lora_base_gemm_apply(const lora_problem_t* problem, const lora_routing_t* routing,
+                                              const lora_base_weight_t* base, void* workspace,
+                                              size_t workspace_bytes, lora_stream_t stream) {
+  begin_call();
+  lora_status_t st = validate_problem(problem);
+  if (st != LORA_OK) return st;
+  if ((st = validate_routing(problem, routing)) != LORA_OK) return st;
+  if (routing->token_rows) return LORA_ERR_SHAPE;  // rows must be in sorted order
+  if (!base) return LORA_ERR_NULL;
+  BaseWeights wts{};
+  for (int j = 0; j < problem->num_slices; ++j) {
+    if (!base[j].W0) return LORA_ERR_NULL;
+    if (base[j].row_stride < problem->in_dim) return LORA_ERR_SHAPE;
+    wts.W0[j] = base[j].W0;
+    wts.row_stride[j] = (long long)base[j].row_stride;
+  }
+  if (problem->num_tokens == 0) return LORA_OK;
+  const bool noop = is_noop(routing);
+  if (!noop && (!workspace || workspace_bytes < ws_bytes(problem, routing->end))) return LORA_ERR_WORKSPACE;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return LORA_ERR_ALIGN;
+  ProblemDesc d = make_desc(problem, routing);
+  if (!d.status) return LORA_ERR_CUDA;
+  if (noop) {  // base rows only: no groups to add
+    d.G = 0;
+    d.end = 0;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* u = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWorkspaceCtrlBytes) : nullptr;
+  if (base_tc_ok(d, wts) && (noop || fast_path_ok(d, u)) && base_maps_ok(d, wts)) {
+    int nsplit = 0;
+    if (!noop) {
+      cudaError_t e = cudaErrorNotSupported;
+      if (tc_shrink_ok(d)) {
+        nsplit = tc_shrink_splits(d.end, d.in_dim, device_sm_count());
+        e = launch_tc_shrink(d, u, s, nsplit);
+      }
+      if (e == cudaErrorNotSupported) {
+        nsplit = apply_splits_for(d);
+        if (dec_shrink_ok(d)) e = launch_dec_shrink(d, u, s, nsplit);
+        if (e == cudaErrorNotSupported) e = launch_shrink_partial_bf16(d, u, s);
+      }
+      if ((st = cuda_status(e)) != LORA_OK) return st;
+    }
+    return cuda_status(launch_base_gemm(d, wts, u, nsplit, !noop, s));
+  }
+  if (!noop && (st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
+  return cuda_status(launch_base_gemm_simple(d, wts, u, !noop, s));
+}
+
 extern "C" lora_status_t lora_workspace_init(void* workspace, size_t workspace_bytes, lora_stream_t stream) {
   begin_call();
   if (!workspace) return LORA_ERR_NULL;

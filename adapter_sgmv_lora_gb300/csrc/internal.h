@@ -111,6 +111,26 @@ constexpr int kWorkspaceCtrlWords = kWorkspaceCtrlBytes / 4;
 // be encoded or the grid could not be resident.
 bool dec_apply_ok(const ProblemDesc& p);
 cudaError_t launch_dec_apply(const ProblemDesc& p, float* u, unsigned* ctrl, cudaStream_t s, int C);
+// The base projection with the delta fused in (sgmv_base.cu).  Per slice,
+// the base weight W0_j [out_j, in] (row stride in elements).
+struct BaseWeights {
+  const void* W0[LORA_MAX_SLICES];
+  long long row_stride[LORA_MAX_SLICES];
+};
+// tcgen05 path: bf16, the fast-path shapes, no token_rows, aligned weights.
+bool base_tc_ok(const ProblemDesc& p, const BaseWeights& wts);
+// Whether the tensor maps of launch_base_gemm can be encoded (checked before
+// anything is launched).
+bool base_maps_ok(const ProblemDesc& p, const BaseWeights& wts);
+// u: nsplit fp32 planes from a shrink launched just before (after_shrink),
+// or unused when end == 0.  Returns cudaErrorNotSupported, having launched
+// nothing, when the tensor maps cannot be encoded.
+cudaError_t launch_base_gemm(const ProblemDesc& p, const BaseWeights& wts, const float* u, int nsplit,
+                             bool after_shrink, cudaStream_t s);
+// Any shape / type: one thread per output, u one fp32 plane (generic shrink).
+cudaError_t launch_base_gemm_simple(const ProblemDesc& p, const BaseWeights& wts, const float* u,
+                                    bool after_shrink, cudaStream_t s);
+
 // Failure-path self test of the counter handoff (lora_selftest_handoff).
 cudaError_t launch_selftest_handoff(unsigned* ctrl, unsigned* status, uint32_t polls, uint64_t delay_ns,
                                     cudaStream_t s);

@@ -326,6 +326,38 @@ lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_
 lora_status_t lora_sgmv_apply_noalloc(const lora_problem_t* problem, const lora_routing_t* routing,
                                       lora_stream_t stream);
 
+/* Base projection weight of one slice: W0 [out_dim, in_dim] in the
+ * problem's storage type, row o at W0 + o * row_stride (elements). */
+typedef struct {
+  const void* W0;
+  int64_t row_stride;
+} lora_base_weight_t;
+
+/*
+ * lora_base_gemm_apply -- the LoRA delta fused into the base projection
+ * ("vLLM LoRA 实现深度解析" section 1: h = W0 x + (alpha/r) B A x, the scale
+ * folded into B):
+ *   y_j[t, o] = rn( sum_i W0_j[o, i] x[t, i]
+ *                   + [t < end] (bias_j[s, o] + sum_k B_j[s, o, k] u[t, j*R + k]) )
+ * for EVERY row t < num_tokens and every slice j (s: the slot of t's group;
+ * base rows get the base product alone), with one rounding to the storage
+ * type.  y is written, never read: the delta joins the base product in the
+ * accumulator instead of a read-modify-write of y.  base[num_slices] gives
+ * each slice's W0 (DEVICE).  The shrink writes u into `workspace` as for
+ * lora_sgmv_apply (same size and first-bytes-zero rule; NULL allowed when
+ * num_groups or end is 0).  Rows must be in sorted order: token_rows is
+ * refused (LORA_ERR_SHAPE).
+ * Kernels: bf16 fast-path shapes (16-byte aligned W0, row stride a multiple
+ * of 8) run a tcgen05 GEMM whose K loop ends with the delta as extra K
+ * steps (u = hi + lo as bf16 terms against the slot's B block, per group
+ * overlapping a 128-row tile); other shapes a generic kernel.
+ * Errors: as lora_sgmv_apply, plus LORA_ERR_NULL (base or a W0 missing),
+ * LORA_ERR_SHAPE (a row stride below in_dim, token_rows given).
+ */
+lora_status_t lora_base_gemm_apply(const lora_problem_t* problem, const lora_routing_t* routing,
+                                   const lora_base_weight_t* base, void* workspace, size_t workspace_bytes,
+                                   lora_stream_t stream);
+
 /*
  * lora_get_device_status -- reads and clears, in one atomic exchange ordered
  * after the work already on `stream`, the device status word of the current

@@ -73,6 +73,9 @@ def _bind(L):
                                    ctypes.c_int, ctypes.POINTER(_Slice), ctypes.c_void_p,
                                    ctypes.c_longlong, i32p, i32p, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_void_p]
+    L.oracle_base_rows.restype = ctypes.c_int
+    L.oracle_base_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_longlong,
+                                   ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_longlong]
     L.oracle_threads.restype = ctypes.c_int
     L.oracle_threads.argtypes = [ctypes.c_int]
     L.oracle_sgmv_token_slots.restype = ctypes.c_int
@@ -302,6 +305,51 @@ def sgmv_rows(rows, x_rows, slices, lora_ids, grouped_offsets, end: int, in_dim:
     if rc != OK:
         raise ValueError("oracle_sgmv_rows failed with code %d" % rc)
     return u, outs
+
+
+def base_rows(W0, x_rows, parallel: bool = False):
+    """The base projection W0 . x of the listed rows in double (plain C;
+    W0 float64 [out, in], x_rows float64 [n, in]) -> float64 [n, out]."""
+    W0 = np.ascontiguousarray(W0, dtype=np.float64)
+    x_rows = np.ascontiguousarray(x_rows, dtype=np.float64)
+    n, k = x_rows.shape
+    out, k2 = W0.shape
+    assert k == k2
+    y = np.empty((n, out), dtype=np.float64)
+    rc = lib(parallel).oracle_base_rows(n, k, out, W0.ctypes.data, k, x_rows.ctypes.data, k, y.ctypes.data, out)
+    if rc != OK:
+        raise ValueError("oracle_base_rows failed with code %d" % rc)
+    return y
+
+
+def prep_w0(W0_raw: np.ndarray, dtype: str) -> np.ndarray:
+    """A base weight [out, in] (fp32) in the storage type (one RNE rounding)."""
+    return from_f32(np.asarray(W0_raw, dtype=np.float32), dtype)
+
+
+def problem_rows_with_base(prob, rows, W0_stored, parallel: bool = False):
+    """The fused result for the listed rows: per slice j,
+    y_j = W0_j . x_t + (t < end ? delta of t : 0)  (unrounded double), the
+    base projection with the LoRA delta added (vLLM page section 1).
+    W0_stored: one storage-type [out_j, in] weight per slice."""
+    rows = _i32(rows)
+    dt = prob["dtype"]
+    x_rows = to_f64(prob["x"][rows], dt)
+    bases = [base_rows(to_f64(w, dt), x_rows, parallel) for w in W0_stored]
+    routed = rows < prob["end"]
+    out = [b.copy() for b in bases]
+    if routed.any():
+        rr = rows[routed]
+        slices = []
+        for sl, b in zip(prob["slices"], bases):
+            d = dict(sl)
+            d["y_in"] = b[routed]
+            slices.append(d)
+        _, ys = sgmv_rows(rr, x_rows[routed], slices, prob["lora_ids"], prob["grouped_offsets"], prob["end"],
+                          prob["in_dim"], prob["R"], prob["S"], parallel=parallel)
+        for o, yj in zip(out, ys):
+            o[routed] = yj
+    return out
 
 
 def problem_rows(prob, rows, parallel: bool = False):

@@ -278,3 +278,30 @@ int oracle_sgmv_token_slots(int n_rows, const int* row_slot, int in_dim, int R, 
   }
   return ORACLE_OK;
 }
+
+/*
+ * oracle_base_rows: the base projection of the listed rows ("vLLM LoRA
+ * 实现深度解析" section 1: h = W0 x + (alpha/r) B A x; this is the W0 x term),
+ *     y[r, o] = sum_i W0[o, i] * x_rows[r, i]        (o < out_dim)
+ * in double, summing over the input index in increasing order.  W0 is the
+ * projection's weight [out_dim, in_dim] (row o at W0 + o * w0_row_stride).
+ * Its result is the y_in that oracle_sgmv_rows adds the delta to when the
+ * delta is fused into the base projection.
+ */
+int oracle_base_rows(int n_rows, int in_dim, int out_dim, const double* W0, long long w0_row_stride,
+                     const double* x_rows, long long x_row_stride, double* y, long long y_row_stride) {
+  if (n_rows < 0 || in_dim <= 0 || out_dim <= 0) return ORACLE_BAD_ARG;
+  if (n_rows > 0 && (!W0 || !x_rows || !y)) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int r = 0; r < n_rows; ++r) {
+    const double* xt = x_rows + (long long)r * x_row_stride;
+    double* yr = y + (long long)r * y_row_stride;
+    for (int o = 0; o < out_dim; ++o) {
+      const double* w = W0 + (long long)o * w0_row_stride;
+      double acc = 0.0;
+      for (int i = 0; i < in_dim; ++i) acc += w[i] * xt[i];
+      yr[o] = acc;
+    }
+  }
+  return ORACLE_OK;
+}

@@ -660,3 +660,94 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(lk.LoraError) as e:
         lk.lora_sgmv_apply(dev["problem"], dev["routing"], dev["workspace"][:10])
     assert e.value.status == 8
+
+
+# --------------------------------------- the delta fused into the base GEMM --
+
+BASE = 0x100
+
+
+def run_base_case(raw, proj="qkv", rows="all", slot_ranks=False, poison=False, path=None, parallel=True,
+                  seed=0):
+    """lora_base_gemm_apply against the oracle's fused definition: every row
+    (routed rows: W0 x + delta; base rows: W0 x), one rounding."""
+    lk, device = _lk(), _dev()
+    dev = device.prepare(raw, proj, slot_ranks=slot_ranks)
+    if poison:
+        _poison_padding(dev, raw)
+    names = dev["names"]
+    dt = raw["dtype"]
+    W0s = [oracle.prep_w0(raw["W0"][nm], dt) for nm in names]
+    W0d = [device.storage_to_torch(w, dt) for w in W0s]
+    dev["y_all"].fill_(float("nan"))  # y is written, never read
+    lk.lora_base_gemm_apply(dev["problem"], dev["routing"], W0d, dev["workspace"])
+    bits, _ = lk.lora_last_call_path()
+    torch.cuda.synchronize()
+    assert lk.lora_get_device_status() == 0
+    if path is not None:
+        assert bits == path, hex(bits)
+    ref = oracle.prepare_problem(raw, proj)
+    T = raw["T"]
+    if rows == "all":
+        rr = np.arange(T, dtype=np.int32)
+    else:
+        rr = np.unique(np.concatenate([_sample_rows(ref["grouped_offsets"], ref["end"], np.random.default_rng(seed)),
+                                       np.arange(ref["end"], T, max(1, (T - ref["end"]) // 40), dtype=np.int32),
+                                       np.array([T - 1], dtype=np.int32)])).astype(np.int32)
+    ys = oracle.problem_rows_with_base(ref, rr, W0s, parallel=parallel)
+    got = oracle.to_f64(device.y_host(dev)[rr], dt)
+    col = 0
+    for yj in ys:
+        g = got[:, col:col + yj.shape[1]]
+        err = np.abs(g - yj) / (1.0 + np.abs(yj))
+        assert err.max() <= TOL_Y[dt], ("y", float(err.max()))
+        col += yj.shape[1]
+    return dev
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_base_gemm_decode8b_every_row(proj):
+    """Decode batch at full size (256 rows, 8 slots, base rows included)."""
+    raw = sy.add_base_weights(sy.draw("decode8b", 90), 90)
+    run_base_case(raw, proj, path=BASE | 0x4)
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_base_gemm_prefill8b_sampled(proj):
+    """Ragged prefill at full size (R = 64): group edges, 64-row boundaries,
+    random routed rows and a spread of base rows."""
+    raw = sy.add_base_weights(sy.draw("prefill8b", 91), 91)
+    run_base_case(raw, proj, rows="sample", path=BASE | 0x10)
+
+
+@pytest.mark.parametrize("R", [16, 32, 64, 128])
+def test_base_gemm_ragged_tiles(R):
+    """Groups straddling the 128-row tiles (several groups per tile), a
+    partial last tile, slices narrower than a column block."""
+    spec = _spec(max_num_loras=7, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
+                 fixed_slots=(0, 1, 2, 3, 4, 5, 6, -1), fixed_lens=(1, 63, 64, 65, 127, 130, 200, 9),
+                 hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
+    raw = sy.add_base_weights(sy.draw(spec, 92 + R), 92 + R)
+    run_base_case(raw, "qkv")
+    run_base_case(raw, "o")
+
+
+def test_base_gemm_bias_ranks_and_delta_dominated():
+    """Bias and true ranks (NaN past them) with a delta of order one."""
+    spec = _spec(max_num_loras=4, max_lora_rank=64, rank_choices=(16, 32, 64), kind="fixed",
+                 fixed_slots=(3, 0, 2, 1, -1), fixed_lens=(150, 300, 29, 260, 9), hidden=512, n_heads=8,
+                 n_kv_heads=2, head_dim=64)
+    raw = sy.add_base_weights(sy.add_bias(sy.emphasize_delta(sy.draw(spec, 96), 40.0), 96, scale=1.0), 96)
+    run_base_case(raw, "qkv", slot_ranks=True, poison=True, path=BASE | 0x10)
+    run_base_case(raw, "o", slot_ranks=True, poison=True)
+
+
+def test_base_gemm_all_base_rows_and_fp32():
+    """No routed rows (the base projection alone), and the generic kernel for fp32."""
+    spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(70, 90), hidden=256, n_heads=8, n_kv_heads=2,
+                 head_dim=32)
+    raw = sy.add_base_weights(sy.draw(spec, 97), 97)
+    run_base_case(raw, "qkv", path=BASE)
+    spec = _spec(dtype="f32", max_lora_rank=32, rank_choices=(8, 32), n_requests=25)
+    raw = sy.add_base_weights(sy.draw(spec, 98), 98)
+    run_base_case(raw, "qkv", path=BASE | 0x1)

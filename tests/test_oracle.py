@@ -486,3 +486,61 @@ def test_openmp_build_matches_single_thread_bitwise():
         _, t2 = oracle.problem_token_rows(prob, allr, slots, parallel=True)
         for a, b in zip(t1, t2):
             assert np.array_equal(a, b)
+
+
+# ------------------------------------- the delta fused into the base projection --
+
+def test_base_rows_identity_and_selection():
+    """W0 = I returns x exactly; a selection matrix (row o picks input p(o))
+    returns the picked inputs exactly: no dropped, shifted or transposed
+    index."""
+    rng = np.random.default_rng(81)
+    k = 12
+    x = rng.standard_normal((5, k))
+    assert np.array_equal(oracle.base_rows(np.eye(k), x), x)
+    perm = rng.permutation(k)[:7]
+    W = np.zeros((7, k))
+    W[np.arange(7), perm] = 1.0
+    assert np.array_equal(oracle.base_rows(W, x), x[:, perm])
+    W2 = 2.0 * W - np.zeros_like(W)
+    assert np.array_equal(oracle.base_rows(W2, x), 2.0 * x[:, perm])
+
+
+def test_base_rows_matches_an_independent_product():
+    """Against numpy's matrix product (another implementation) to 1e-12."""
+    rng = np.random.default_rng(82)
+    W = rng.standard_normal((33, 70))
+    x = rng.standard_normal((9, 70))
+    np.testing.assert_allclose(oracle.base_rows(W, x), x @ W.T, rtol=1e-12, atol=1e-12)
+
+
+def test_fused_base_is_merged_weight():
+    """The base projection with the delta fused in equals the merged-weight
+    product (W0 + B_s A_s) x on routed rows and W0 x on base rows (vLLM page
+    section 1), by numpy brute force on a drawn workload with base rows."""
+    spec = sy.custom_spec(max_num_loras=3, max_lora_rank=16, rank_choices=(4, 16), kind="fixed",
+                          fixed_slots=(2, 0, -1, 1, 0), fixed_lens=(3, 2, 4, 5, 1), hidden=32, n_heads=2,
+                          n_kv_heads=1, head_dim=16)
+    raw = sy.add_base_weights(sy.draw(spec, 83), 83)
+    for proj in ("qkv", "o"):
+        prob = oracle.prepare_problem(raw, proj)
+        names = {"qkv": ["q", "k", "v"], "o": ["o"]}[proj]
+        W0s = [oracle.prep_w0(raw["W0"][nm], raw["dtype"]) for nm in names]
+        T = raw["T"]
+        got = oracle.problem_rows_with_base(prob, np.arange(T, dtype=np.int32), W0s)
+        x = oracle.to_f64(raw["x_" + proj], raw["dtype"])
+        slots = np.full(T, -1)
+        for g in range(len(prob["lora_ids"])):
+            slots[prob["grouped_offsets"][g]:prob["grouped_offsets"][g + 1]] = prob["lora_ids"][g]
+        for j, nm in enumerate(names):
+            W0 = oracle.to_f64(W0s[j], raw["dtype"])
+            sl = prob["slices"][j]
+            R, kin = prob["R"], prob["in_dim"]
+            for t in range(T):
+                W = W0.copy()
+                s = slots[t]
+                if s >= 0:
+                    Af = sl["A"].reshape(-1)[sl["A_offset"] + s * sl["A_slot_stride"]:][:R * kin].reshape(R, kin)
+                    Bf = sl["B"].reshape(-1)[sl["B_offset"] + s * sl["B_slot_stride"]:][:sl["out_dim"] * R]
+                    W = W + Bf.reshape(sl["out_dim"], R) @ Af
+                np.testing.assert_allclose(got[j][t], W @ x[t], rtol=1e-12, atol=1e-12)

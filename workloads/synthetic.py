@@ -240,6 +240,17 @@ def emphasize_delta(raw: dict, b_factor: float = 40.0) -> dict:
     return raw
 
 
+def add_base_weights(raw: dict, seed: int = 0) -> dict:
+    """Draw the base projection weights W0 [out, in] per projection, fp32,
+    N(0, 1) / sqrt(in) (the projection the LoRA delta is added to), from
+    their own stream so the rest of the workload is unchanged."""
+    rng = np.random.default_rng([seed, 104729])
+    spec = raw["spec"]
+    raw["W0"] = {p: rng.standard_normal((spec.out_dims[p], spec.in_dims[p]), dtype=np.float32)
+                 / np.float32(np.sqrt(spec.in_dims[p])) for p in spec.projs}
+    return raw
+
+
 def add_bias(raw: dict, seed: int = 0, scale: float = 0.1) -> dict:
     """Draw a LoRA bias vector per (projection, slot): scale * N(0, 1), fp32.
     Drawn from its own stream so the rest of the workload is unchanged."""

@@ -8,7 +8,7 @@ library cannot be loaded, every call raises.
 
 Names follow the C ABI: ``lora_build_routing``, ``lora_set_slot``,
 ``lora_shrink``, ``lora_expand``, ``lora_workspace_bytes``,
-``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_base_gemm_apply``, ``lora_workspace_init``,
+``lora_sgmv_apply``, ``lora_sgmv_apply_noalloc``, ``lora_base_gemm_apply``,
 ``lora_get_device_status``, ``lora_last_call_path``, ``lora_status_string``.
 """
 from __future__ import annotations
@@ -34,7 +34,7 @@ DEV_BAD_SLOT, DEV_BAD_OFFSETS, DEV_BAD_END, DEV_TIMEOUT, DEV_BAD_ROW = 1, 2, 4, 
 PATH_GENERIC_SHRINK, PATH_GENERIC_EXPAND = 0x1, 0x2
 PATH_MMA_SHRINK, PATH_MMA_EXPAND = 0x4, 0x8
 PATH_TC_SHRINK, PATH_TC_EXPAND = 0x10, 0x20
-PATH_DECODE_FUSED, PATH_PREP, PATH_BASE_GEMM = 0x40, 0x80, 0x100
+PATH_PREP, PATH_BASE_GEMM = 0x80, 0x100
 MAX_SLICES = 3
 
 
@@ -63,7 +63,8 @@ class _BaseWeight(ctypes.Structure):
 
 class _Routing(ctypes.Structure):
     _fields_ = [("lora_ids", ctypes.c_void_p), ("grouped_offsets", ctypes.c_void_p),
-                ("num_groups", ctypes.c_int32), ("end", ctypes.c_int32), ("token_rows", ctypes.c_void_p)]
+                ("num_groups", ctypes.c_int32), ("end", ctypes.c_int32), ("token_rows", ctypes.c_void_p),
+                ("host_grouped_offsets", ctypes.c_void_p)]
 
 
 _lib = None
@@ -113,10 +114,6 @@ def lib():
     L.lora_base_gemm_apply.restype = ctypes.c_int
     L.lora_base_gemm_apply.argtypes = [ctypes.POINTER(_Problem), ctypes.POINTER(_Routing),
                                        ctypes.POINTER(_BaseWeight), vp, ctypes.c_size_t, vp]
-    L.lora_workspace_init.restype = ctypes.c_int
-    L.lora_workspace_init.argtypes = [vp, ctypes.c_size_t, vp]
-    L.lora_selftest_handoff.restype = ctypes.c_int
-    L.lora_selftest_handoff.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64, vp]
     L.lora_last_call_path.restype = ctypes.c_uint32
     L.lora_last_call_path.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.lora_selftest_wait_timeout.restype = ctypes.c_int
@@ -185,26 +182,36 @@ def lora_build_token_rows(req_num_tokens, perm, end: int) -> np.ndarray:
 @dataclass
 class Routing:
     """Routing triple: device lora_ids / grouped_offsets tensors, host num_groups / end,
-    and optionally device token_rows (row of each sorted token, unsorted batches)."""
+    optionally device token_rows (row of each sorted token, unsorted batches)
+    and a host copy of grouped_offsets (int32 numpy array) that lets the
+    library pick the kernels per group."""
     lora_ids: object
     grouped_offsets: object
     num_groups: int
     end: int
     token_rows: object = None
+    host_grouped_offsets: object = None
 
     def _c(self) -> _Routing:
         ptr = lambda t: t.data_ptr() if t is not None and t.numel() > 0 else None
+        h = self.host_grouped_offsets
+        if h is not None:
+            h = np.ascontiguousarray(h, dtype=np.int32)
+            self._host_keep = h  # the pointer below must outlive the call
         return _Routing(ptr(self.lora_ids), ptr(self.grouped_offsets), int(self.num_groups), int(self.end),
-                        ptr(self.token_rows))
+                        ptr(self.token_rows), h.ctypes.data if h is not None and h.size > 0 else None)
 
 
-def routing_to_device(r: dict, device="cuda", non_blocking=False) -> Routing:
-    """Upload the host triple from lora_build_routing (int32 tensors)."""
+def routing_to_device(r: dict, device="cuda", non_blocking=False, host_offsets=True) -> Routing:
+    """Upload the host triple from lora_build_routing (int32 tensors); with
+    host_offsets the host copy of grouped_offsets rides along (per-group
+    kernel choice)."""
     import torch
     ids = torch.from_numpy(np.ascontiguousarray(r["lora_ids"], dtype=np.int32))
-    offs = torch.from_numpy(np.ascontiguousarray(r["grouped_offsets"], dtype=np.int32))
+    offs_h = np.ascontiguousarray(r["grouped_offsets"], dtype=np.int32)
+    offs = torch.from_numpy(offs_h)
     return Routing(ids.to(device, non_blocking=non_blocking), offs.to(device, non_blocking=non_blocking),
-                   int(r["num_groups"]), int(r["end"]))
+                   int(r["num_groups"]), int(r["end"]), None, offs_h.copy() if host_offsets else None)
 
 
 # --------------------------------------------------------------- problems --
@@ -336,29 +343,11 @@ def lora_workspace_bytes(problem: Problem, end: int) -> int:
     return int(lib().lora_workspace_bytes(ctypes.byref(c), int(end)))
 
 
-WORKSPACE_CTRL_BYTES = 4096
-
-
-def lora_workspace_init(workspace, stream=None) -> None:
-    """Zero-fill a workspace tensor (required once before its first
-    lora_sgmv_apply; every call leaves its counter bytes zero again)."""
-    nbytes = workspace.numel() * workspace.element_size()
-    _check(lib().lora_workspace_init(workspace.data_ptr(), nbytes, _stream_handle(stream)), "lora_workspace_init")
-
-
 def new_workspace(problem: Problem, end: int, device="cuda"):
-    """A zero-filled workspace tensor of lora_workspace_bytes(problem, end)."""
+    """A workspace tensor of lora_workspace_bytes(problem, end) bytes."""
     import torch
-    nbytes = lora_workspace_bytes(problem, end)
-    return torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.float32, device=device)
-
-
-def lora_selftest_handoff(workspace, polls: int, delay_ns: int, stream=None) -> None:
-    """Failure-path self test of the one-launch apply's counter handoff (see
-    include/lora_sgmv.h)."""
-    nbytes = workspace.numel() * workspace.element_size()
-    _check(lib().lora_selftest_handoff(workspace.data_ptr(), nbytes, int(polls), int(delay_ns),
-                                       _stream_handle(stream)), "lora_selftest_handoff")
+    nbytes = max(lora_workspace_bytes(problem, end), 256)
+    return torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=device)
 
 
 def lora_sgmv_apply(problem: Problem, routing: Routing, workspace, stream=None) -> None:

@@ -16,7 +16,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblora_sgmv.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "routing.cpp", "simple_kernels.cu", "sgmv_bf16.cu", "sgmv_tc.cu", "sgmv_decode.cu", "sgmv_base.cu"]
+SOURCES = ["api.cu", "routing.cpp", "simple_kernels.cu", "sgmv_bf16.cu", "sgmv_tc.cu", "sgmv_base.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I", CSRC, "-I", INCLUDE]

@@ -133,6 +133,8 @@ ProblemDesc make_desc(const lora_problem_t* p, const lora_routing_t* r) {
     d.token_rows = r->token_rows;
   }
   d.status = status_ptr();
+  d.seg_lo = 0;
+  d.seg_hi = 0x7FFFFFFF;
   return d;
 }
 
@@ -146,19 +148,37 @@ size_t plane_bytes(const lora_problem_t* p, int32_t end) {
   return (raw + 255) & ~(size_t)255;
 }
 
-// lora_sgmv_apply's workspace: its shrink may split the input dimension into
-// up to 16 partial planes (apply_splits), summed by the expand; or, on the
-// tensor-core path for ranks 64 and 128, it holds u packed per 128-row tile
-// (at most max_num_loras + end / 128 tiles).
-size_t ws_bytes(const lora_problem_t* p, int32_t end) {
+// lora_sgmv_apply's workspace holds the intermediate.  Its shrink may split the input dimension into up to 16 partial planes
+// (apply_splits), summed by the expand; on the tensor-core path for ranks 64
+// and 128 it holds u packed per 128-row tile (at most max_num_loras + end /
+// 128 tiles), and when the kernels are picked per group both are live at
+// once: the packed region first, the planes after it.
+size_t planes_bound(const lora_problem_t* p, int32_t end) {
   int splits = apply_splits(end, p->in_dim, p->num_slices * p->max_lora_rank);
   const int tc = tc_shrink_splits(end, p->in_dim, kMaxSmsForWorkspace);
   if (tc > splits) splits = tc;
-  size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
-               (size_t)p->max_lora_rank * 4;
+  const size_t raw = (size_t)splits * (size_t)(end > 0 ? end : 0) * (size_t)p->num_slices *
+                     (size_t)p->max_lora_rank * 4;
+  return (raw + 255) & ~(size_t)255;
+}
+
+size_t packed_region(const lora_problem_t* p, int32_t end) {
   const size_t packed = tc_packed_bytes(p->max_num_loras, end, p->num_slices, p->max_lora_rank);
-  if (packed > raw) raw = packed;
-  return (size_t)kWorkspaceCtrlBytes + ((raw + 255) & ~(size_t)255);
+  return (packed + 255) & ~(size_t)255;
+}
+
+size_t ws_bytes(const lora_problem_t* p, int32_t end) { return packed_region(p, end) + planes_bound(p, end); }
+
+// Long groups (tcgen05 tiles) and short groups of a routing whose host copy
+// of the offsets is given.
+void count_classes(const lora_routing_t* r, int* n_long, int* n_short) {
+  *n_long = *n_short = 0;
+  const int32_t* o = r->host_grouped_offsets;
+  for (int g = 0; g < r->num_groups; ++g) {
+    const int len = o[g + 1] - o[g];
+    if (len >= LORA_TC_MIN_ROWS) ++*n_long;
+    else if (len > 0) ++*n_short;
+  }
 }
 
 }  // namespace
@@ -261,9 +281,27 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
   ProblemDesc d = make_desc(problem, routing);
   if (!d.status) return LORA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  unsigned* ctrl = static_cast<unsigned*>(workspace);
-  void* inter = static_cast<uint8_t*>(workspace) + kWorkspaceCtrlBytes;
+  void* inter = workspace;
   float* u = static_cast<float*>(inter);
+  if (fast_path_ok(d, u) && routing->host_grouped_offsets && tc_expand_shapes_ok(d)) {
+    // Kernels per group: the long groups on tcgen05 (packed u in the first
+    // region), the short ones on mma.sync (planes in the second region).
+    int n_long = 0, n_short = 0;
+    count_classes(routing, &n_long, &n_short);
+    if (n_long > 0 && n_short > 0) {
+      ProblemDesc dl = d, ds = d;
+      dl.seg_lo = LORA_TC_MIN_ROWS;
+      ds.seg_hi = LORA_TC_MIN_ROWS;
+      float* up = reinterpret_cast<float*>(static_cast<uint8_t*>(inter) + packed_region(problem, routing->end));
+      cudaError_t e = launch_tc_apply_packed(dl, inter, s);
+      if (e != cudaErrorNotSupported) {
+        if ((st = cuda_status(e)) != LORA_OK) return st;
+        const int splits = apply_splits_for(ds);
+        if ((st = cuda_status(launch_shrink_partial_bf16(ds, up, s))) != LORA_OK) return st;
+        return cuda_status(launch_expand_bf16(ds, up, s, true, splits));
+      }
+    }
+  }
   if (fast_path_ok(d, u)) {
     if (tc_expand_ok(d)) {
       const cudaError_t e = launch_tc_apply_packed(d, inter, s);
@@ -278,14 +316,7 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
       }
     }
     const int splits = apply_splits_for(d);
-    cudaError_t e = cudaErrorNotSupported;
-    if (dec_apply_ok(d)) {
-      e = launch_dec_apply(d, u, ctrl, s, splits);
-      if (e != cudaErrorNotSupported) return cuda_status(e);
-    }
-    if (dec_shrink_ok(d)) e = launch_dec_shrink(d, u, s, splits);
-    if (e == cudaErrorNotSupported) e = launch_shrink_partial_bf16(d, u, s);
-    if ((st = cuda_status(e)) != LORA_OK) return st;
+    if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s))) != LORA_OK) return st;
     return cuda_status(launch_expand_bf16(d, u, s, true, splits));
   }
   if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
@@ -342,7 +373,7 @@ extern "C" lora_status_t lora_base_gemm_apply(const lora_problem_t* problem, con
     d.end = 0;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* u = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWorkspaceCtrlBytes) : nullptr;
+  float* u = static_cast<float*>(workspace);
   if (base_tc_ok(d, wts) && (noop || fast_path_ok(d, u)) && base_maps_ok(d, wts)) {
     int nsplit = 0;
     if (!noop) {
@@ -353,8 +384,7 @@ extern "C" lora_status_t lora_base_gemm_apply(const lora_problem_t* problem, con
       }
       if (e == cudaErrorNotSupported) {
         nsplit = apply_splits_for(d);
-        if (dec_shrink_ok(d)) e = launch_dec_shrink(d, u, s, nsplit);
-        if (e == cudaErrorNotSupported) e = launch_shrink_partial_bf16(d, u, s);
+        e = launch_shrink_partial_bf16(d, u, s);
       }
       if ((st = cuda_status(e)) != LORA_OK) return st;
     }
@@ -362,26 +392,6 @@ extern "C" lora_status_t lora_base_gemm_apply(const lora_problem_t* problem, con
   }
   if (!noop && (st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
   return cuda_status(launch_base_gemm_simple(d, wts, u, !noop, s));
-}
-
-extern "C" lora_status_t lora_workspace_init(void* workspace, size_t workspace_bytes, lora_stream_t stream) {
-  begin_call();
-  if (!workspace) return LORA_ERR_NULL;
-  if (workspace_bytes < (size_t)kWorkspaceCtrlBytes) return LORA_ERR_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
-}
-
-extern "C" lora_status_t lora_selftest_handoff(void* workspace, size_t workspace_bytes, uint32_t polls,
-                                               uint64_t delay_ns, lora_stream_t stream) {
-  begin_call();
-  if (!workspace) return LORA_ERR_NULL;
-  if (workspace_bytes < (size_t)kWorkspaceCtrlBytes) return LORA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return LORA_ERR_ALIGN;
-  if (delay_ns > 100000000ull) return LORA_ERR_SHAPE;  // at most 0.1 s
-  unsigned* p = status_ptr();
-  if (!p) return LORA_ERR_CUDA;
-  return cuda_status(launch_selftest_handoff(static_cast<unsigned*>(workspace), p, polls, delay_ns,
-                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" lora_status_t lora_selftest_wait_timeout(uint32_t polls, lora_stream_t stream) {

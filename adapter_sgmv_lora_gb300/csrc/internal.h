@@ -40,6 +40,9 @@ struct ProblemDesc {
   const int* token_rows;  // device [end] or nullptr (row i of the sorted order is row i)
   const int* slot_ranks;  // device [S] true ranks, or nullptr (all R)
   unsigned* status;  // device status word (LORA_DEV_* flags)
+  // Groups this launch works on: those of seg_lo <= routed rows < seg_hi
+  // (the others have no tiles).  0 and INT_MAX: every group.
+  int seg_lo, seg_hi;
 };
 
 // Records a successful kernel launch of the current entry-point call
@@ -90,27 +93,6 @@ int apply_splits(int end, int in_dim, int nR);
 // *short_ring tells whether the shrink runs its 4-stage ring.
 int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
 
-// The apply's partial-plane shrink for short groups with TMA-fed stages
-// (sgmv_decode.cu): plain batches (no token_rows, no slot ranks), R = 16 or
-// 32, n*R <= 96.  Writes C planes like launch_shrink_partial_bf16.  Returns
-// cudaErrorNotSupported, having launched nothing, when the tensor maps cannot
-// be encoded.
-bool dec_shrink_ok(const ProblemDesc& p);
-cudaError_t launch_dec_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int C);
-
-// The workspace of lora_sgmv_apply starts with kWorkspaceCtrlBytes of
-// per-tile counters (zero before the first call, left zero by every call);
-// the intermediate follows.
-constexpr int kWorkspaceCtrlBytes = 4096;
-constexpr int kWorkspaceCtrlWords = kWorkspaceCtrlBytes / 4;
-// The one-launch apply for decode-sized batches (sgmv_decode.cu): plain
-// batches (no token_rows, slot ranks or bias), R = 16 or 32, n*R <= 96,
-// groups of at most 64 routed rows on average.  C K splits write C planes at
-// u, handed to the expand items through the counters at ctrl.  Returns
-// cudaErrorNotSupported, having launched nothing, when the tensor maps cannot
-// be encoded or the grid could not be resident.
-bool dec_apply_ok(const ProblemDesc& p);
-cudaError_t launch_dec_apply(const ProblemDesc& p, float* u, unsigned* ctrl, cudaStream_t s, int C);
 // The base projection with the delta fused in (sgmv_base.cu).  Per slice,
 // the base weight W0_j [out_j, in] (row stride in elements).
 struct BaseWeights {
@@ -131,9 +113,6 @@ cudaError_t launch_base_gemm(const ProblemDesc& p, const BaseWeights& wts, const
 cudaError_t launch_base_gemm_simple(const ProblemDesc& p, const BaseWeights& wts, const float* u,
                                     bool after_shrink, cudaStream_t s);
 
-// Failure-path self test of the counter handoff (lora_selftest_handoff).
-cudaError_t launch_selftest_handoff(unsigned* ctrl, unsigned* status, uint32_t polls, uint64_t delay_ns,
-                                    cudaStream_t s);
 
 // tcgen05 shrink for long groups (TMA tensor loads, TMEM accumulator): writes
 // nsplit partial planes like launch_shrink_partial_bf16.  tc_shrink_ok says
@@ -141,6 +120,10 @@ cudaError_t launch_selftest_handoff(unsigned* ctrl, unsigned* status, uint32_t p
 // its plane count for a device of `sms` SMs (shapes and SM count only).  Returns cudaErrorNotSupported when the tensor
 // maps cannot be encoded (nothing launched).
 bool tc_shrink_ok(const ProblemDesc& p);
+// The shape conditions of the tcgen05 kernels without the group-length
+// criterion (for a launch restricted to long groups).
+bool tc_shapes_ok(const ProblemDesc& p);
+bool tc_expand_shapes_ok(const ProblemDesc& p);
 int tc_shrink_splits(int end, int in_dim, int sms);
 cudaError_t launch_tc_shrink(const ProblemDesc& p, float* u, cudaStream_t s, int nsplit);
 // tcgen05 expand for long groups with R = 64 or 128 (sums nsplit planes of u).

@@ -138,21 +138,6 @@ __device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t addr) {
   return v;
 }
 
-// ------------------------------------------- inter-CTA handoff in global memory
-// Load with acquire semantics at GPU scope: later loads of this thread see
-// what the releasing writer made visible before its release.
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Nanoseconds of the GPU's global timer.
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Programmatic dependent launch: let the next grid in the stream start its
 // prologue / wait until the previous grid's memory is visible.
 __device__ __forceinline__ void pdl_launch_dependents() {

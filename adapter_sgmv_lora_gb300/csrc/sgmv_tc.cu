@@ -371,16 +371,19 @@ int tc_shrink_splits(int end, int in_dim, int sms) {
   return n;
 }
 
-bool tc_shrink_ok(const ProblemDesc& p) {
+bool tc_shapes_ok(const ProblemDesc& p) {
   if (p.token_rows) return false;  // TMA boxes need the tile's rows contiguous
   const int nR = p.n_slices * p.R;
   switch (nR) {
     case 16: case 32: case 48: case 64: case 96: case 128: case 192: case 256: case 384: break;
     default: return false;
   }
-  if (p.R % 8 != 0 || p.in_dim % TK != 0) return false;
+  return p.R % 8 == 0 && p.in_dim % TK == 0 && p.G > 0;
+}
+
+bool tc_shrink_ok(const ProblemDesc& p) {
   // Long groups only: on average at least 96 routed rows per group.
-  return p.G > 0 && p.end >= 96LL * p.G;
+  return tc_shapes_ok(p) && p.end >= 96LL * p.G;
 }
 
 namespace {
@@ -543,7 +546,8 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const int o0 = p.offs[g], o1 = p.offs[g + 1];
         rc.offs[g] = o0;
         rc.ids[g] = p.lora_ids[g];
-        nt = (o1 - o0 + TM - 1) / TM;
+        const int len = o1 - o0;
+        nt = (len >= p.seg_lo && len < p.seg_hi) ? (len + TM - 1) / TM : 0;
       }
       int incl = nt;
 #pragma unroll
@@ -975,9 +979,11 @@ bool nr_supported(int n) {
 
 }  // namespace
 
-bool tc_expand_ok(const ProblemDesc& p) {
-  return (p.R == 64 || p.R == 128) && p.G <= RC_MAX_G && tc_shrink_ok(p);
+bool tc_expand_shapes_ok(const ProblemDesc& p) {
+  return (p.R == 64 || p.R == 128) && p.G <= RC_MAX_G && tc_shapes_ok(p);
 }
+
+bool tc_expand_ok(const ProblemDesc& p) { return tc_expand_shapes_ok(p) && tc_shrink_ok(p); }
 
 cudaError_t launch_tc_expand(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
   TxMaps maps;

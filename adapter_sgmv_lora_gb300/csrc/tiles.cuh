@@ -4,9 +4,11 @@
 // Group g covers sorted-batch rows [offs[g], offs[g+1]) and uses slot
 // lora_ids[g] ("max.pipelines.lora.LoRAManagerV3", get_lora_graph_inputs).
 // Each group is cut into ceil(len / tile_rows) tiles; tiles are numbered
-// group by group.  Every CTA scans the whole (small: G <= max_num_loras)
-// triple, so every CTA of a launch reaches the same outcome on validity and
-// an invalid triple makes the whole launch skip its work.
+// group by group.  A launch may work on a class of groups only (lengths in
+// [seg_lo, seg_hi)): the other groups then have no tiles.  Every CTA scans
+// the whole (small: G <= max_num_loras) triple, so every CTA of a launch
+// reaches the same outcome on validity and an invalid triple makes the whole
+// launch skip its work.
 #pragma once
 
 #include "internal.h"
@@ -51,7 +53,7 @@ __device__ __forceinline__ bool warp_locate_tile(const ProblemDesc& p, int tile_
       if (o1 < o0) bad |= LORA_DEV_BAD_OFFSETS;
       if (id < 0 || id >= p.S) bad |= LORA_DEV_BAD_SLOT;
       const long long len = (long long)o1 - (long long)o0;
-      nt = len > 0 ? (len + tile_rows - 1) / tile_rows : 0;
+      nt = (len > 0 && len >= p.seg_lo && len < p.seg_hi) ? (len + tile_rows - 1) / tile_rows : 0;
     }
     long long incl = nt;
 #pragma unroll

@@ -68,6 +68,8 @@ WORKLOAD_DESC = {
     "prefill8b": "ragged prefill, 8B shapes, 4 slots + base, max rank 64, 16 requests of 128-2048 tokens, bf16",
     "mixed70b": "mixed prefill+decode, Llama-3-70B attention (hidden 8192, 64/8 heads; fused qkv 10240 + o 8192), "
                 "16 slots, max rank 128, 8192 tokens, 20% base, bf16",
+    "mixed64": "mixed prefill+decode over many adapters, 8B attention shapes, 64 slots, max rank 64, 3328 tokens "
+               "= 4 prefill requests of 512-768 + 1-token decodes, 10% base, bf16",
     "mlp8b": "decode, Llama-3-8B MLP (hidden 4096, intermediate 14336; fused gate+up 28672 + down 4096), "
              "8 slots, max rank 16, 256 x 1-token requests, 25% base, bf16",
 }
@@ -459,7 +461,7 @@ class WorkloadBench:
         return out
 
 
-def roofline_block(wb, trials_ms, peak, peak_kind, tpeak, tpeak_kind, traffic):
+def roofline_block(wb, trials_ms, peak, peak_kind, tpeak, tpeak_kind, traffic=None):
     med = statistics.median(trials_ms)
     qbytes = statistics.mean(s["b0"] for s in wb.sets)
     qflops = statistics.mean(s["f0"] for s in wb.sets)
@@ -496,6 +498,27 @@ def _profiled_traffic(workload):
     return None
 
 
+def one_path_block(wb, sampler, peaks):
+    """The first problem's apply without the routing's host offsets (one
+    kernel family for the whole call, chosen from the average group length),
+    for comparison with the per-group choice."""
+    lk = wb.lk
+    calls = []
+    for s in wb.sets:
+        d = s["p0"]
+        r = d["routing"]
+        calls.append(lk.CallBuilder(d["problem"], lk.Routing(r.lora_ids, r.grouped_offsets, r.num_groups, r.end),
+                                    d["workspace"]))
+    with wb.torch.cuda.stream(wb.stream):
+        calls[0].apply(wb.stream)
+    wb.stream.synchronize()
+    g = wb._graph(lambda st: [c.apply(st) for c in calls])
+    t = statistics.median(wb.trials(g, wb.NS, sampler=sampler))
+    rb = roofline_block(wb, [t], *peaks, traffic=None)
+    return {"avg_apply_us": rb["avg_launch_us"], "frac": rb["frac"], "kernel_path": hex(calls[0].last_path),
+            "note": "routing without host_grouped_offsets: one kernel family for the whole call"}
+
+
 def workload_summary(wb, sampler, peaks):
     """Secondary block: step and per-projection times, roofline of the first
     problem's apply (median of 5 trials), warm-L2 time."""
@@ -526,6 +549,61 @@ def workload_summary(wb, sampler, peaks):
                             "number" % (wb.P0, wb.nwarm)},
         "kernel_paths": [hex(b) for b in wb.path_bits], "launches_per_step": wb.launches_per_step,
     }
+
+
+def base_fused_block(wb, sampler, peaks):
+    """The delta fused into the base projection (lora_base_gemm_apply) against
+    the base GEMM (cuBLAS through torch.matmul, the library comparison) plus
+    lora_sgmv_apply, on the first problem of every input set; synthetic base
+    weights W0 ~ N(0, 1/in)."""
+    torch, lk, st = wb.torch, wb.lk, wb.stream
+    peak = peaks[0]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    items = []
+    for s in wb.sets:
+        d = s["p0"]
+        x, y = d["x"], d["y_all"]
+        O, k = y.shape[1], x.shape[1]
+        W0 = (torch.randn((O, k), device="cuda", generator=gen, dtype=torch.float32) / k ** 0.5).to(torch.bfloat16)
+        offs = np.cumsum([0] + d["outs"])[:-1]
+        base = [(W0, int(o) * k, k) for o in offs]
+        items.append((d, x, y, W0, base))
+    torch.cuda.synchronize()
+
+    def fused(cs):
+        for d, x, y, W0, base in items:
+            lk.lora_base_gemm_apply(d["problem"], d["routing"], base, d["workspace"], cs)
+
+    def separate(cs):
+        for (d, x, y, W0, base), s in zip(items, wb.sets):
+            torch.matmul(x, W0.t(), out=y)
+            s["call0"].apply(cs)
+
+    with torch.cuda.stream(st):
+        fused(st)
+        path_bits = lk.lora_last_call_path()[0]
+        separate(st)
+    st.synchronize()
+    g_f, g_s = wb._graph(fused), wb._graph(separate)
+    tf = statistics.median(wb.trials(g_f, wb.NS, sampler=sampler))
+    ts = statistics.median(wb.trials(g_s, wb.NS, sampler=sampler))
+    d0 = wb.sets[0]["p0"]
+    T, k = d0["x"].shape
+    O = d0["y_all"].shape[1]
+    lora = statistics.mean(s["b0"] for s in wb.sets)
+    E = statistics.mean(s["E"] for s in wb.sets)
+    e = 2
+    bytes_fused = T * k * e + O * k * e + T * O * e + (lora - E * k * e - 2 * E * O * e)
+    bytes_sep = (T * k * e + O * k * e + T * O * e) + lora
+    return {"unit": "%s projection of one layer: every row's W0 x plus the delta on routed rows" % wb.P0,
+            "fused_us": round(tf * 1e3, 3), "separate_us": round(ts * 1e3, 3),
+            "separate_desc": "torch.matmul (cuBLAS) base GEMM into y, then lora_sgmv_apply",
+            "fused_bytes": int(bytes_fused), "separate_bytes": int(bytes_sep),
+            "fused_GBps": round(bytes_fused / (tf * 1e-3) / 1e9, 1),
+            "fused_frac_of_hbm": round(bytes_fused / (tf * 1e-3) / 1e9 / peak, 4),
+            "fused_tflops": round(2.0 * T * O * k / (tf * 1e-3) / 1e12, 1),
+            "kernel_path": hex(path_bits)}
 
 
 def spawn_replicas(args):
@@ -613,6 +691,8 @@ def run_ours(args):
 
     # ---- roofline and per-projection figures of the main workload
     main = workload_summary(wb, sampler, peaks)
+    if args.workload == "mixed64":
+        main["one_path"] = one_path_block(wb, sampler, peaks)
     (ms,), (tokens,) = reduce_across_ranks([ms], [tokens], dist, "cuda")
 
     # ---- e2e through the public API with host buffers
@@ -626,6 +706,8 @@ def run_ours(args):
                 continue
             sb = WorkloadBench(name, args, rank, lk, torch, stream, l2)
             secondary[name] = workload_summary(sb, sampler, peaks)
+            if not args.no_base_fused:
+                secondary[name]["base_fused"] = base_fused_block(sb, sampler, peaks)
             del sb
             torch.cuda.empty_cache()
     clocks = sampler.stop() if sampler else None
@@ -657,6 +739,7 @@ def run_ours(args):
                         "note": "5 trials of >= 30 ms of the same steps, for comparison with the K-step region"},
         "warm_l2": main["warm_l2"],
         "kernel_paths": main["kernel_paths"],
+        "one_path": main.get("one_path"),
         "secondary": secondary,
         "e2e": e2e,
         "gpu_launches": wb.launches_per_step * args.steps,
@@ -730,7 +813,8 @@ def run_e2e(args, sets, lk, torch, stream, dist):
             prob = d["problem"]
             slices = [dataclasses.replace(sl, y=y_v) for sl in prob.slices]
             prob_v = dataclasses.replace(prob, x=x_v, slices=slices)
-            routing_v = lk.Routing(ids_d, offs_d, d["routing"].num_groups, d["routing"].end)
+            # the host copy of the offsets is the pinned buffer the routing build writes
+            routing_v = lk.Routing(ids_d, offs_d, d["routing"].num_groups, d["routing"].end, None, h["offs_np"])
             h["calls"].append(lk.CallBuilder(prob_v, routing_v, d["workspace"]))
         host.append(h)
 
@@ -797,6 +881,8 @@ def main():
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip the decode8b / prefill8b blocks")
+    ap.add_argument("--no-base-fused", action="store_true",
+                    help="skip the delta-in-base-GEMM comparison in the secondary blocks")
     ap.add_argument("--slot-ranks", action="store_true",
                     help="pass the adapters' true ranks so the kernels skip the rank padding")
     ap.add_argument("--cpu-budget", type=float, default=16.0)

@@ -67,8 +67,7 @@ typedef enum { LORA_DTYPE_F32 = 0, LORA_DTYPE_BF16 = 1 } lora_dtype_t;
 #define LORA_DEV_BAD_SLOT 1u     /* lora_ids[g] outside [0, max_num_loras) */
 #define LORA_DEV_BAD_OFFSETS 2u  /* grouped_offsets[0] != 0 or a decreasing offset */
 #define LORA_DEV_BAD_END 4u      /* grouped_offsets[num_groups] != end */
-#define LORA_DEV_TIMEOUT 8u      /* a kernel gave up (after ~1 s) waiting for its own copies or for
-                                    another CTA's partial result */
+#define LORA_DEV_TIMEOUT 8u      /* a kernel gave up (after ~1 s) waiting for its own copies */
 #define LORA_DEV_BAD_ROW 16u     /* a token_rows entry outside [0, num_tokens) */
 
 #define LORA_MAX_SLICES 3
@@ -158,7 +157,18 @@ typedef struct {
    * tiles containing it and raises LORA_DEV_BAD_ROW.  Gathered batches do not
    * use the tcgen05 kernels. */
   const int32_t* token_rows;
+  /* Optional HOST int32 [num_groups + 1]: the same values as
+   * grouped_offsets, read by the call itself (not by the kernels).  With it
+   * lora_sgmv_apply picks the kernels per group: groups of at least
+   * LORA_TC_MIN_ROWS routed rows on the tensor-core (tcgen05) kernels, the
+   * others on the mma.sync kernels, both in the same call.  NULL: one choice
+   * per call, from the average group length (end / num_groups). */
+  const int32_t* host_grouped_offsets;
 } lora_routing_t;
+
+/* Routed rows from which a group counts as long (tcgen05 tiles) when the
+ * kernels are picked per group. */
+#define LORA_TC_MIN_ROWS 64
 
 /*
  * lora_build_routing -- HOST ONLY.  Sort + group ("max.pipelines.lora.
@@ -254,46 +264,25 @@ lora_status_t lora_expand(const lora_problem_t* problem, const lora_routing_t* r
                           const float* u, lora_stream_t stream);
 
 /*
- * Bytes of device workspace lora_sgmv_apply needs for `end` routed rows:
- * LORA_WORKSPACE_CTRL_BYTES of per-tile counters, then the larger of the fp32
- * intermediate (up to 16 partial planes of end x n*R) and, for max_lora_rank
- * 64 or 128, the packed intermediate of the tensor-core path
- * ((max_num_loras + end / 128) tiles x n*R x 512 bytes).  Depends on shapes
- * only.
+ * Bytes of device workspace lora_sgmv_apply needs for `end` routed rows: for
+ * max_lora_rank 64 or 128 the packed intermediate of the tensor-core path
+ * ((max_num_loras + end / 128) tiles x n*R x 512 bytes), then room for the
+ * fp32 intermediate (up to 16 partial planes of end x n*R); both are live
+ * when the kernels are picked per group.  Depends on shapes only.
  */
-#define LORA_WORKSPACE_CTRL_BYTES 4096u
 size_t lora_workspace_bytes(const lora_problem_t* problem, int32_t end);
-
-/*
- * lora_workspace_init -- zero-fills `workspace_bytes` bytes of a workspace on
- * `stream` (cudaMemsetAsync).  A workspace must start with
- * LORA_WORKSPACE_CTRL_BYTES of zeros the first time lora_sgmv_apply uses it
- * (this call, or any zero fill, does that); every call leaves those bytes
- * zero again, so one initialisation serves every later call, whatever the
- * problem or batch.  No counterpart on the pages.
- * Errors: LORA_ERR_NULL, LORA_ERR_WORKSPACE (fewer than
- * LORA_WORKSPACE_CTRL_BYTES bytes), LORA_ERR_CUDA.
- */
-lora_status_t lora_workspace_init(void* workspace, size_t workspace_bytes, lora_stream_t stream);
 
 /*
  * lora_sgmv_apply -- shrink then expand in one call; the intermediate lives in
  * `workspace` (DEVICE, >= lora_workspace_bytes(problem, end) bytes, 16-byte
- * aligned).  Its first LORA_WORKSPACE_CTRL_BYTES must be zero on entry (see
- * lora_workspace_init) and are zero again when the call's kernels finish;
- * the rest is ignored on entry and holds the intermediate: fp32 partial
- * planes, or, on the tensor-core path (bf16, rank 64 or 128, long groups), u
- * already split into bf16 hi + lo terms and laid out as the expand's operand
- * per 128-row tile.
- * Kernels: decode-sized bf16 batches (rank 16 or 32, at most 64 routed rows
- * per group on average, no token_rows / slot ranks / bias) run shrink and
- * expand in ONE cooperative launch: each tile's K splits hand their partial
- * planes to its expand blocks through a counter in the first bytes of the
- * workspace (waits bounded; a wait that runs out raises LORA_DEV_TIMEOUT and
- * leaves the counters zero).  Other shapes run two kernels, the expand
- * launched as a programmatic dependent of the shrink so its weight and y
- * loads overlap the shrink.  Two calls whose kernels may overlap on the GPU
- * need two workspaces.
+ * aligned, contents on entry ignored): fp32 partial planes, or, on the
+ * tensor-core path (bf16, rank 64 or 128, long groups), u already split into
+ * bf16 hi + lo terms and laid out as the expand's operand per 128-row tile.
+ * The expand is launched as a programmatic dependent of the shrink, so its
+ * weight and y loads overlap the shrink.  With the routing's host copy of
+ * the offsets (host_grouped_offsets), a batch mixing long and short groups
+ * runs both kernel families in the one call, each on its own groups.  Two
+ * calls whose kernels may overlap on the GPU need two workspaces.
  */
 lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lora_routing_t* routing,
                               void* workspace, size_t workspace_bytes, lora_stream_t stream);
@@ -344,7 +333,7 @@ typedef struct {
  * type.  y is written, never read: the delta joins the base product in the
  * accumulator instead of a read-modify-write of y.  base[num_slices] gives
  * each slice's W0 (DEVICE).  The shrink writes u into `workspace` as for
- * lora_sgmv_apply (same size and first-bytes-zero rule; NULL allowed when
+ * lora_sgmv_apply (same size; NULL allowed when
  * num_groups or end is 0).  Rows must be in sorted order: token_rows is
  * refused (LORA_ERR_SHAPE).
  * Kernels: bf16 fast-path shapes (16-byte aligned W0, row stride a multiple
@@ -379,7 +368,6 @@ lora_status_t lora_get_device_status(lora_stream_t stream, uint32_t* flags);
 #define LORA_PATH_MMA_EXPAND 0x8u      /* mma.sync expand (short groups) */
 #define LORA_PATH_TC_SHRINK 0x10u      /* tcgen05 + TMA shrink (long groups) */
 #define LORA_PATH_TC_EXPAND 0x20u      /* persistent tcgen05 + TMA expand (long groups) */
-#define LORA_PATH_DECODE_FUSED 0x40u   /* one-launch shrink + expand (decode-sized batches) */
 #define LORA_PATH_PREP 0x80u           /* load-time slot / bias preparation */
 #define LORA_PATH_BASE_GEMM 0x100u     /* base projection GEMM with the delta as K tail */
 
@@ -402,20 +390,6 @@ uint32_t lora_last_call_path(uint32_t* num_launches);
  * fails.
  */
 lora_status_t lora_selftest_wait_timeout(uint32_t polls, lora_stream_t stream);
-
-/*
- * lora_selftest_handoff -- exercises the failure path of the one-launch
- * apply's counter handoff without faulting the GPU (no counterpart on the
- * pages).  Two resident CTAs use counter 0 of `workspace` (which must be
- * zero, as lora_workspace_init leaves it): the reader gives up after `polls`
- * polls, raises LORA_DEV_TIMEOUT and counts itself; the split arrives after
- * `delay_ns` (at most 0.1 s) and, completing the count, zeroes the counter.
- * Afterwards the workspace serves lora_sgmv_apply as before.
- * Errors: LORA_ERR_NULL, LORA_ERR_WORKSPACE, LORA_ERR_ALIGN, LORA_ERR_SHAPE
- * (delay above 0.1 s), LORA_ERR_CUDA.
- */
-lora_status_t lora_selftest_handoff(void* workspace, size_t workspace_bytes, uint32_t polls,
-                                    uint64_t delay_ns, lora_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* lora_status_string(lora_status_t status);

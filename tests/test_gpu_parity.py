@@ -94,7 +94,6 @@ GEN = 0x1 | 0x2        # generic shrink + expand
 MMA = 0x4 | 0x8        # mma.sync shrink + expand
 TC = 0x10 | 0x20       # tcgen05 shrink + expand
 TC_MMA = 0x10 | 0x8    # tcgen05 shrink, mma.sync expand
-FUSED = 0x40           # one-launch decode apply
 
 
 def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0,
@@ -184,7 +183,7 @@ def test_tiny_fp32(proj, mode):
 @pytest.mark.parametrize("proj", ["qkv", "o"])
 @pytest.mark.parametrize("mode", ["apply", "split"])
 def test_decode8b_full(proj, mode):
-    run_case(sy.draw("decode8b", 0), proj, mode=mode, path=FUSED if mode == "apply" else MMA)
+    run_case(sy.draw("decode8b", 0), proj, mode=mode, path=MMA)
 
 
 @pytest.mark.parametrize("proj", ["qkv", "o"])
@@ -217,10 +216,7 @@ def test_mixed70b_every_row(proj, mode):
 def test_mlp8b_full(proj, mode):
     """MLP projections (gate + up fused as two slices; down over the 14336-wide
     intermediate activations)."""
-    # down (4096 outputs) fits the one-launch apply; gate + up (28672 outputs,
-    # several expand blocks per CTA) takes the two-kernel path.
-    want = FUSED if (mode == "apply" and proj == "down") else MMA
-    run_case(sy.draw("mlp8b", 0), proj, mode=mode, path=want)
+    run_case(sy.draw("mlp8b", 0), proj, mode=mode, path=MMA)
 
 
 # -------------------------------------- checks dominated by the LoRA delta --
@@ -231,9 +227,8 @@ def test_delta_dominated_decode(mode):
     2e-2 (1 + |ref|) bar then measures the delta itself (decode shapes,
     mma.sync path)."""
     raw = sy.emphasize_delta(sy.draw("decode8b", 31), 40.0)
-    want = FUSED if mode == "apply" else MMA
-    run_case(raw, "qkv", mode=mode, path=want)
-    run_case(raw, "o", mode=mode, path=want)
+    run_case(raw, "qkv", mode=mode, path=MMA)
+    run_case(raw, "o", mode=mode, path=MMA)
 
 
 @pytest.mark.parametrize("R", [16, 64, 128])
@@ -431,98 +426,12 @@ def test_short_groups_many_adapters_wide_outputs(mode):
 @pytest.mark.parametrize("R", [16, 32])
 def test_apply_split_planes_ragged_groups(R):
     """The apply's shrink splits K into partial planes for small batches;
-    groups of 1, 31, 32, 33, 64, 70 and 100 rows, input width 1024 (the
-    one-launch apply: tiles of 64 rows with ragged ends, two tiles for the
-    longer groups)."""
+    groups of 1, 31, 32, 33, 64, 70 and 100 rows, input width 1024."""
     spec = _spec(max_num_loras=7, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
                  fixed_slots=(6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 31, 32, 33, 64, 70, 100, 5),
                  hidden=1024, n_heads=16, n_kv_heads=4, head_dim=64)
-    run_case(sy.draw(spec, 5), "qkv", mode="apply", path=FUSED)
-    run_case(sy.draw(spec, 6), "o", mode="apply", path=FUSED)
-
-
-@pytest.mark.parametrize("R", [16, 32])
-@pytest.mark.parametrize("hidden", [512, 2048])
-def test_one_launch_apply_shapes(R, hidden):
-    """The one-launch apply across slice widths narrower and wider than its
-    256-column expand blocks, 1..3 slices (n*R = 16..96), K splits of one or
-    more stages, groups of 1 to 128 rows."""
-    spec = _spec(max_num_loras=9, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
-                 fixed_slots=(8, 7, 6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 2, 15, 16, 17, 63, 64, 65, 128, 3),
-                 hidden=hidden, n_heads=hidden // 64, n_kv_heads=max(1, hidden // 256), head_dim=64)
-    run_case(sy.draw(spec, 50 + R), "qkv", mode="apply", path=FUSED)
-    run_case(sy.draw(spec, 60 + R), "o", mode="apply", path=FUSED)
-
-
-def test_one_launch_apply_leaves_counters_zero_and_reuses_workspace():
-    """The counters at the head of the workspace are zero after every call, so
-    one workspace serves different problems back to back (fused qkv, then
-    o_proj, then qkv again) with correct results each time."""
-    lk, device = _lk(), _dev()
-    raw = sy.draw("decode8b", 70)
-    dq = device.prepare(raw, "qkv")
-    do = device.prepare(raw, "o", shared_routing=(dq["route_host"], dq["routing"]))
-    nbytes = max(lk.lora_workspace_bytes(dq["problem"], dq["route_host"]["end"]),
-                 lk.lora_workspace_bytes(do["problem"], do["route_host"]["end"]))
-    ws = torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.float32, device="cuda")
-    ref_q = oracle.prepare_problem(raw, "qkv")
-    ref_o = oracle.prepare_problem(raw, "o")
-    end = dq["route_host"]["end"]
-    rows = np.arange(end, dtype=np.int32)
-    _, yq = oracle.problem_rows(ref_q, rows)
-    _, yo = oracle.problem_rows(ref_o, rows)
-    y0q, y0o = dq["y_all"].clone(), do["y_all"].clone()
-    for it in range(2):
-        dq["y_all"].copy_(y0q)
-        do["y_all"].copy_(y0o)
-        lk.lora_sgmv_apply(dq["problem"], dq["routing"], ws)
-        assert lk.lora_last_call_path()[0] == FUSED
-        lk.lora_sgmv_apply(do["problem"], do["routing"], ws)
-        assert lk.lora_last_call_path()[0] == FUSED
-        torch.cuda.synchronize()
-        assert lk.lora_get_device_status() == 0
-        assert int(ws[:lk.WORKSPACE_CTRL_BYTES // 4].view(torch.int32).abs().sum().item()) == 0
-        for dev, ys in ((dq, yq), (do, yo)):
-            got = oracle.to_f64(device.y_host(dev), "bf16")
-            col = 0
-            for yj in ys:
-                g = got[:end, col:col + yj.shape[1]]
-                err = np.abs(g - yj) / (1.0 + np.abs(yj))
-                assert err.max() <= TOL_Y["bf16"], float(err.max())
-                col += yj.shape[1]
-
-
-def test_handoff_wait_that_runs_out_leaves_counters_zero():
-    """The one-launch apply's handoff with a wait that runs out (a reader
-    that gives up before its split arrives), no fault: LORA_DEV_TIMEOUT is
-    raised, the late split completes the count and zeroes the counter, and
-    the same workspace then serves a correct apply."""
-    lk, device = _lk(), _dev()
-    raw = sy.draw("decode8b", 71)
-    dev = device.prepare(raw, "qkv")
-    ws = dev["workspace"]
-    assert lk.lora_get_device_status() == 0
-    lk.lora_selftest_handoff(ws, polls=64, delay_ns=2_000_000)
-    torch.cuda.synchronize()
-    assert lk.lora_get_device_status() == lk.DEV_TIMEOUT
-    assert int(ws[:lk.WORKSPACE_CTRL_BYTES // 4].view(torch.int32).abs().sum().item()) == 0
-    lk.lora_selftest_handoff(ws, polls=1 << 22, delay_ns=1000)  # the wait that succeeds
-    torch.cuda.synchronize()
-    assert lk.lora_get_device_status() == 0
-    assert int(ws[:lk.WORKSPACE_CTRL_BYTES // 4].view(torch.int32).abs().sum().item()) == 0
-    lk.lora_sgmv_apply(dev["problem"], dev["routing"], ws)
-    assert lk.lora_last_call_path()[0] == FUSED
-    torch.cuda.synchronize()
-    assert lk.lora_get_device_status() == 0
-    ref = oracle.prepare_problem(raw, "qkv")
-    end = ref["end"]
-    _, ys = oracle.problem_rows(ref, np.arange(end, dtype=np.int32))
-    got = oracle.to_f64(device.y_host(dev), "bf16")
-    col = 0
-    for yj in ys:
-        err = np.abs(got[:end, col:col + yj.shape[1]] - yj) / (1.0 + np.abs(yj))
-        assert err.max() <= TOL_Y["bf16"], float(err.max())
-        col += yj.shape[1]
+    run_case(sy.draw(spec, 5), "qkv", mode="apply", path=MMA)
+    run_case(sy.draw(spec, 6), "o", mode="apply", path=MMA)
 
 
 @pytest.mark.parametrize("R", [16, 32, 64, 128])
@@ -751,3 +660,52 @@ def test_base_gemm_all_base_rows_and_fp32():
     spec = _spec(dtype="f32", max_lora_rank=32, rank_choices=(8, 32), n_requests=25)
     raw = sy.add_base_weights(sy.draw(spec, 98), 98)
     run_base_case(raw, "qkv", path=BASE | 0x1)
+
+
+# --------------------------------------------- kernels picked per group --
+
+SPLIT = 0x10 | 0x20 | 0x4 | 0x8   # tcgen05 shrink + expand for long groups, mma.sync for short ones
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_mixed64_kernels_per_group_every_row(proj):
+    """A few long prefill groups among many one-token groups, with the host
+    copy of the offsets: the long groups run on tcgen05 and the short ones on
+    mma.sync in the same call; every routed row against the oracle."""
+    run_case(sy.draw("mixed64", 0), proj, mode="apply", path=SPLIT, parallel=True)
+
+
+def test_mixed64_without_host_offsets_takes_one_path():
+    """Without the host copy the call picks one path from the average group
+    length (here mma.sync for everything); same results."""
+    lk, device = _lk(), _dev()
+    raw = sy.draw("mixed64", 1)
+    dev = device.prepare(raw, "qkv")
+    r = dev["routing"]
+    plain = lk.Routing(r.lora_ids, r.grouped_offsets, r.num_groups, r.end)
+    lk.lora_sgmv_apply(dev["problem"], plain, dev["workspace"])
+    assert lk.lora_last_call_path()[0] == MMA
+    torch.cuda.synchronize()
+    assert lk.lora_get_device_status() == 0
+    ref = oracle.prepare_problem(raw, "qkv")
+    end = ref["end"]
+    _, ys = oracle.problem_rows(ref, np.arange(end, dtype=np.int32), parallel=True)
+    got = oracle.to_f64(device.y_host(dev), "bf16")
+    col = 0
+    for yj in ys:
+        err = np.abs(got[:end, col:col + yj.shape[1]] - yj) / (1.0 + np.abs(yj))
+        assert err.max() <= TOL_Y["bf16"], float(err.max())
+        col += yj.shape[1]
+
+
+@pytest.mark.parametrize("R", [64, 128])
+def test_kernels_per_group_ragged_and_ranks(R):
+    """Long groups of 64 (the threshold), 65, 129 and 300 rows among groups of
+    1 to 63 rows, with and without true ranks (NaN past them) and a bias."""
+    spec = _spec(max_num_loras=10, max_lora_rank=R, rank_choices=(16, R), kind="fixed",
+                 fixed_slots=(9, 8, 7, 6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 64, 2, 65, 63, 129, 17, 300, 5, 33, 8),
+                 hidden=512, n_heads=8, n_kv_heads=2, head_dim=64)
+    run_case(sy.draw(spec, 100 + R), "qkv", mode="apply", path=SPLIT)
+    run_case(sy.draw(spec, 101 + R), "o", mode="apply", path=SPLIT)
+    raw = sy.add_bias(sy.draw(spec, 102 + R), 102 + R)
+    run_case(raw, "qkv", mode="apply", slot_ranks=True, poison=True, path=SPLIT)

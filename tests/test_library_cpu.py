@@ -168,7 +168,7 @@ def test_host_validation_without_gpu():
     assert L.lora_set_slot(ctypes.byref(prob), 0, 0, 17, 1.0, 0, 16, 16, 0, None) == 3
     assert L.lora_set_slot(ctypes.byref(prob), 0, 2, 4, 1.0, 0, 16, 16, 0, None) == 4
     assert L.lora_set_slot(ctypes.byref(prob), 1, 0, 4, 1.0, 0, 16, 16, 0, None) == 2
-    assert L.lora_workspace_bytes(ctypes.byref(prob), 100) == 4096 + 100 * 16 * 4 + (256 - (6400 % 256)) % 256
+    assert L.lora_workspace_bytes(ctypes.byref(prob), 100) == 100 * 16 * 4 + (256 - (6400 % 256)) % 256
 
 
 def test_token_rows_match_oracle():

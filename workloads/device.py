@@ -102,7 +102,7 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
         routing = lk.routing_to_device(rt, device)
     else:
         rt, routing = shared_routing
-    ws = lk.new_workspace(prob, rt["end"], device=device)  # zero-filled, as the first call requires
+    ws = lk.new_workspace(prob, rt["end"], device=device)
     return {"problem": prob, "routing": routing, "route_host": rt, "x": x, "ys": ys, "y_all": y_all,
             "stacks": stacks, "workspace": ws, "dtype": dt, "names": names, "outs": outs,
             "separate_y": (not fused and separate_y and len(names) > 1)}

@@ -22,6 +22,11 @@ Workload shapes (all attention projections; "hd" = head_dim):
   many64      bf16; 8B shapes; 64 slots, all rank 16; 1024 one-token
               requests, 10% base, else finite Zipf(s=1.1) over the 64 slots;
               per-projection (unfused) q/k/v plus o
+  mixed64     bf16; 8B shapes; 64 slots, max rank 64, ranks from {16,32,64};
+              3328 tokens = 4 prefill requests with lengths uniform in
+              [512, 768] plus one-token decode requests for the rest; each
+              request base with probability 0.1, else uniform over the slots
+              (a few long groups among many short ones)
   mixed70b    bf16; hidden 8192, n_heads 64, n_kv 8, hd 128 (q 8192, k/v 1024);
               16 slots, max rank 128, ranks from {16,64,128}; 8192 tokens =
               6 prefill requests with lengths uniform in [512, 1024] plus
@@ -110,6 +115,11 @@ SPECS = {
     "mixed70b": Spec("mixed70b", "bf16", 64, 8, 128, 8192, 16, 128, (16, 64, 128), kind="mixed",
                      total_tokens=8192, n_prefill=6, base_prob=0.20, slot_dist="uniform",
                      len_range=(512, 1024)),
+    # A mixed batch over many adapters: a few long prefill segments among
+    # many one-token decode groups (the kernels are then picked per group).
+    "mixed64": Spec("mixed64", "bf16", 32, 8, 128, 4096, 64, 64, (16, 32, 64), kind="mixed",
+                    total_tokens=3328, n_prefill=4, base_prob=0.10, slot_dist="uniform",
+                    len_range=(512, 768)),
     # MLP projections of the same 8B shape (intermediate 14336): gate + up
     # fused as a two-slice problem, down separately.
     "mlp8b": Spec("mlp8b", "bf16", 32, 8, 128, 4096, 8, 16, (8, 16), kind="decode",

@@ -202,7 +202,7 @@ class Routing:
                         ptr(self.token_rows), h.ctypes.data if h is not None and h.size > 0 else None)
 
 
-def routing_to_device(r: dict, device="cuda", non_blocking=False, host_offsets=True) -> Routing:
+def routing_to_device(r: dict, device="cuda", non_blocking=False, host_offsets=False) -> Routing:
     """Upload the host triple from lora_build_routing (int32 tensors); with
     host_offsets the host copy of grouped_offsets rides along (per-group
     kernel choice)."""

@@ -264,6 +264,204 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   }
 }
 
+// The apply's shrink with the input dimension split over a cluster of CL
+// CTAs (2 or 4) per 128-row tile, for batches with too few tiles to fill
+// the GPU one CTA per tile.  Each CTA streams its K range of the tile's x rows
+// (so x is read once) and of the slot's A rows for ALL n*R columns; the CL
+// partial accumulators are then exchanged through distributed shared memory:
+// CTA q owns columns [q*NR/CL, (q+1)*NR/CL), receives the other CTAs' partials
+// of those columns into its (then idle) stage ring, sums the CL partials in
+// rank order (the same order on every CTA: deterministic) and stores them
+// packed (pack_u16).  Two cluster barriers: before the exchange (every CTA's
+// MMAs have drained its ring) and after it.
+template <int NR, int CL>
+__global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(const __grid_constant__ ProblemDesc p,
+                                                                           const __grid_constant__ TcMaps maps,
+                                                                           uint8_t* __restrict__ upk) {
+  using Cfg = TcCfg<NR>;
+  constexpr int NSTAGE = Cfg::NSTAGE;
+  constexpr int NRC = NR / CL;  // columns each CTA sums and stores
+  static_assert(NRC % 16 == 0, "column share");
+  static_assert((CL - 1) * TM * NRC * 4 <= NSTAGE * Cfg::STAGE, "exchange buffer must fit in the ring");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[NSTAGE];
+  __shared__ __align__(8) uint64_t empty[NSTAGE];
+  __shared__ __align__(8) uint64_t done;
+  __shared__ uint32_t s_tmem;
+  __shared__ Tile s_tile;
+  __shared__ int s_ok;
+  __shared__ int s_fail;
+  __shared__ int s_kmax;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = (int)(blockIdx.x % (unsigned)CL);  // rank in the cluster (cluster dims CL x 1 x 1)
+  const long long tile = blockIdx.x / (unsigned)CL;
+  if (warp == 0) {
+    Tile t{};
+    const bool ok = warp_locate_tile(p, TM, tile, t);
+    if (lane == 0) {
+      s_tile = t;
+      s_ok = ok;
+      s_fail = 0;
+      s_kmax = ok ? slot_kmax(p, t.slot) : 0;
+      for (int i = 0; i < NSTAGE; ++i) {
+        mbar_init(&full[i], 1);
+        mbar_init(&empty[i], 1);
+      }
+      mbar_init(&done, 1);
+      fence_mbar_init();
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  pdl_launch_dependents();
+  const uint32_t tmem = s_tmem;
+  const Tile t = s_tile;
+  const bool ok = s_ok != 0;  // the same on every CTA of the cluster (same tile)
+  const int R = p.R;
+  const int kmax = s_kmax;
+  const int kc = p.in_dim / CL;
+  const int k0 = crank * kc;
+  const int nst = kc / TK;
+
+  if (ok && warp == 0 && lane == 0) {
+    const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+    uint32_t a_bytes = Cfg::X_BYTES;
+    for (int j = 0; j < p.n_slices; ++j) a_bytes += (uint32_t)(min(R, kmax) * TK * 2);
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % NSTAGE;
+      if (s >= NSTAGE && !mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1))) {
+        atomicOr(&s_fail, 1);
+        break;
+      }
+      uint8_t* xs = smem + slot * Cfg::STAGE;
+      uint8_t* as = xs + Cfg::X_BYTES;
+      mbar_arrive_expect_tx(&full[slot], a_bytes);
+      const int kk = k0 + s * TK;
+      tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
+      for (int j = 0; j < p.n_slices; ++j) {
+        uint8_t* dst = as + j * R * TK * 2;
+        const int khi = min(R, kmax);
+        if (khi == R) {
+          tma_load_3d_hint(dst, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
+        } else {
+          int kb = 0;
+          for (; kb + 64 <= khi; kb += 64)
+            tma_load_3d_hint(dst + kb * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
+          for (; kb < khi; kb += 16)
+            tma_load_3d_hint(dst + kb * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
+        }
+      }
+    }
+  } else if (ok && warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16_f32(TM, Cfg::NB);
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % NSTAGE;
+      if (!mbar_wait(&full[slot], (uint32_t)((s / NSTAGE) & 1))) {
+        atomicOr(&s_fail, 1);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t xs = smem_addr(smem + slot * Cfg::STAGE);
+      const uint32_t as = xs + Cfg::X_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < TK / 16; ++ks) {
+        const uint64_t adesc = sw128_desc(xs + ks * 32);
+#pragma unroll
+        for (int h = 0; h < Cfg::NH; ++h) {
+          const uint64_t bdesc = sw128_desc(as + h * Cfg::NB * 128 + ks * 32);
+          tc_mma_bf16(tmem + h * Cfg::NB, adesc, bdesc, idesc, (s > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      tc_commit(&empty[slot]);
+    }
+    tc_commit(&done);
+  }
+  // Every thread: the accumulator is complete (or the CTA failed), and so is
+  // every other CTA's of the cluster, whose rings are then free.
+  bool got = true;
+  if (ok && warp >= 2) got = __all_sync(0xffffffffu, mbar_wait(&done, 0));
+  if (!got) atomicOr(&s_fail, 1);
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  const int q = warp & 3;
+  const int row = q * 32 + lane;
+  // [CL - 1][TM][NRC]: the other ranks' partials of this CTA's columns, rank
+  // order (a sender of rank c lands in slot c, or c - 1 past the receiver).
+  float* recv = reinterpret_cast<float*>(smem);
+  if (ok && warp >= 2 && got) {
+    // Send the partials of the other ranks' columns.
+    for (int dst = 0; dst < CL; ++dst) {
+      if (dst == crank) continue;
+      const int slot_at_dst = crank < dst ? crank : crank - 1;
+      const uint32_t base = smem_addr(recv + ((size_t)slot_at_dst * TM + row) * NRC);
+      const uint32_t remote = map_shared_rank(base, (uint32_t)dst);
+      for (int c = 0; c < NRC; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(dst * NRC + c), v);
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote + (uint32_t)((c + e) * 4)),
+                       "f"(v[e]), "f"(v[e + 1]), "f"(v[e + 2]), "f"(v[e + 3])
+                       : "memory");
+      }
+    }
+  }
+  tc_fence_before_sync();
+  cluster_sync();  // every partial has landed
+  tc_fence_after_sync();
+  if (ok && warp >= 2 && got && !s_fail) {
+    const bool live = row < t.rows;
+    const int uimg = 4 * R * TM;
+    for (int c = 0; c < NRC; c += 16) {
+      float own[16];
+      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(crank * NRC + c), own);
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      for (int src = 0; src < CL; ++src) {  // rank order
+        if (src == crank) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = src == 0 ? own[e] : v[e] + own[e];
+        } else {
+          const float* rp = recv + ((size_t)(src < crank ? src : src - 1) * TM + row) * NRC + c;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(rp + e);
+            v[e] = src == 0 ? w4.x : v[e] + w4.x;
+            v[e + 1] = src == 0 ? w4.y : v[e + 1] + w4.y;
+            v[e + 2] = src == 0 ? w4.z : v[e + 2] + w4.z;
+            v[e + 3] = src == 0 ? w4.w : v[e + 3] + w4.w;
+          }
+        }
+      }
+      const int col = crank * NRC + c, j = col / R, k = col - j * R;
+      const bool keep = k < kmax;  // columns past the slot's rank read no A rows: 0
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = (keep && live) ? v[e] : 0.f;
+      pack_u16(upk + ((long long)tile * p.n_slices + j) * uimg, R, row, k, v);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    if (s_fail) {
+      (void)mbar_wait(&done, 0);
+      if (lane == 0) atomicOr(p.status, LORA_DEV_TIMEOUT);
+    }
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------ host
 
 namespace {
@@ -1011,13 +1209,75 @@ int tc_pack_splits(const ProblemDesc& p) {
   return n;
 }
 
+template <int NR, int CL>
+cudaError_t launch_ksplit_t(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s) {
+  auto kernel = sgmv_tc_shrink_ksplit_kernel<NR, CL>;
+  static unsigned long long done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(g_tc_mu);
+    if (!(done & (1ull << (dev & 63)))) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<NR>::SMEM);
+      if (e != cudaSuccess) return e;
+      done |= 1ull << (dev & 63);
+    }
+  }
+  const long long tiles = (long long)p.G + p.end / TM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * CL));
+  cfg.blockDim = dim3(TTHREADS);
+  cfg.dynamicSmemBytes = TcCfg<NR>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, maps, upk), LORA_PATH_TC_SHRINK);
+}
+
+// The packed shrink with K split over a cluster of `cl` CTAs per tile (all
+// n*R columns per CTA, x read once); cudaErrorNotSupported for other widths.
+cudaError_t launch_ksplit(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s, int cl) {
+  const int nR = p.n_slices * p.R;
+  if (p.in_dim % (cl * TK) != 0) return cudaErrorNotSupported;
+  if (cl == 2) {
+    switch (nR) {
+      case 64: return launch_ksplit_t<64, 2>(p, maps, upk, s);
+      case 128: return launch_ksplit_t<128, 2>(p, maps, upk, s);
+      case 192: return launch_ksplit_t<192, 2>(p, maps, upk, s);
+      case 256: return launch_ksplit_t<256, 2>(p, maps, upk, s);
+      case 384: return launch_ksplit_t<384, 2>(p, maps, upk, s);
+    }
+  } else if (cl == 4) {
+    switch (nR) {
+      case 64: return launch_ksplit_t<64, 4>(p, maps, upk, s);
+      case 128: return launch_ksplit_t<128, 4>(p, maps, upk, s);
+      case 192: return launch_ksplit_t<192, 4>(p, maps, upk, s);
+      case 256: return launch_ksplit_t<256, 4>(p, maps, upk, s);
+      case 384: return launch_ksplit_t<384, 4>(p, maps, upk, s);
+    }
+  }
+  return cudaErrorNotSupported;
+}
+
 cudaError_t launch_tc_apply_packed(const ProblemDesc& p, void* workspace, cudaStream_t s) {
   TcMaps smaps;
   TxMaps xmaps;
   if (!encode_maps(p, &smaps) || !encode_tx_maps(p, &xmaps)) return cudaErrorNotSupported;
+  // Few tiles: split K over a cluster of CTAs per tile (x read once) rather
+  // than the tile's columns (x read once per column part).
   const int nsn = tc_pack_splits(p);
   uint8_t* upk = static_cast<uint8_t*>(workspace);
-  cudaError_t e = launch_tc_shrink_maps(p, smaps, nullptr, s, 1, nsn, upk);
+  cudaError_t e = cudaErrorNotSupported;
+  if (nsn > 1) e = launch_ksplit(p, smaps, upk, s, nsn);
+  if (e == cudaErrorNotSupported) e = launch_tc_shrink_maps(p, smaps, nullptr, s, 1, nsn, upk);
   if (e != cudaSuccess) return e;
   const TxWork w = make_tx_work(p, 1);
   if (p.R == 64) return launch_tx_t<64, true>(p, xmaps, w, nullptr, upk, s, true);

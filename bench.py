@@ -373,7 +373,7 @@ class WorkloadBench:
                           requests=(sets[0]["raw"]["req_slot"], sets[0]["raw"]["req_len"]) if share else None)
             shared = (sets[0]["p0"]["route_host"], sets[0]["p0"]["routing"]) if share else None
             d0 = device.prepare(raw, self.P0, fused=spec.fused_qkv, slot_ranks=args.slot_ranks,
-                                shared_routing=shared)
+                                shared_routing=shared, host_offsets=args.per_group)
             d1 = device.prepare(raw, self.P1, slot_ranks=args.slot_ranks,
                                 shared_routing=(d0["route_host"], d0["routing"]))
             b0 = algorithmic_bytes(d0["route_host"], raw, self.P0, slot_ranks=args.slot_ranks)
@@ -691,7 +691,7 @@ def run_ours(args):
 
     # ---- roofline and per-projection figures of the main workload
     main = workload_summary(wb, sampler, peaks)
-    if args.workload == "mixed64":
+    if args.per_group:
         main["one_path"] = one_path_block(wb, sampler, peaks)
     (ms,), (tokens,) = reduce_across_ranks([ms], [tokens], dist, "cuda")
 
@@ -813,8 +813,9 @@ def run_e2e(args, sets, lk, torch, stream, dist):
             prob = d["problem"]
             slices = [dataclasses.replace(sl, y=y_v) for sl in prob.slices]
             prob_v = dataclasses.replace(prob, x=x_v, slices=slices)
-            # the host copy of the offsets is the pinned buffer the routing build writes
-            routing_v = lk.Routing(ids_d, offs_d, d["routing"].num_groups, d["routing"].end, None, h["offs_np"])
+            # with --per-group the host copy of the offsets is the pinned buffer the routing build writes
+            routing_v = lk.Routing(ids_d, offs_d, d["routing"].num_groups, d["routing"].end, None,
+                                   h["offs_np"] if args.per_group else None)
             h["calls"].append(lk.CallBuilder(prob_v, routing_v, d["workspace"]))
         host.append(h)
 
@@ -886,6 +887,8 @@ def main():
     ap.add_argument("--slot-ranks", action="store_true",
                     help="pass the adapters' true ranks so the kernels skip the rank padding")
     ap.add_argument("--cpu-budget", type=float, default=16.0)
+    ap.add_argument("--per-group", action="store_true",
+                    help="give the routing its host offsets: kernels picked per group (long groups on tcgen05)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

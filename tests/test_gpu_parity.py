@@ -97,7 +97,7 @@ TC_MMA = 0x10 | 0x8    # tcgen05 shrink, mma.sync expand
 
 
 def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0,
-             slot_ranks=False, poison=False, path=None, parallel=False):
+             slot_ranks=False, poison=False, path=None, parallel=False, host_offsets=False):
     """Prepare on the device, run, compare with the oracle.  Returns the device dict.
 
     path: the exact OR of kernel-family bits the call(s) must have launched
@@ -105,7 +105,8 @@ def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=F
     parallel: check with the OpenMP build of the oracle (same numbers,
     shared out over the host's cores; for full-size workloads)."""
     lk, device = _lk(), _dev()
-    dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y, slot_ranks=slot_ranks)
+    dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y, slot_ranks=slot_ranks,
+                         host_offsets=host_offsets)
     ref = oracle.prepare_problem(raw, proj, fused=fused)
     dt = raw["dtype"]
     # routing: library == oracle, bit-exact
@@ -382,6 +383,8 @@ def test_rank_variants_ragged_tiles(R, mode):
                  hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
     run_case(sy.draw(spec, 3), "qkv", mode=mode, path=MMA)
     run_case(sy.draw(spec, 4), "o", mode=mode, path=MMA)
+    if mode == "apply" and R >= 64:  # the routing's host offsets: long groups on tcgen05
+        run_case(sy.draw(spec, 3), "qkv", mode=mode, path=0x10 | 0x20 | 0x4 | 0x8, host_offsets=True)
 
 
 @pytest.mark.parametrize("mode", ["apply", "split"])
@@ -672,7 +675,7 @@ def test_mixed64_kernels_per_group_every_row(proj):
     """A few long prefill groups among many one-token groups, with the host
     copy of the offsets: the long groups run on tcgen05 and the short ones on
     mma.sync in the same call; every routed row against the oracle."""
-    run_case(sy.draw("mixed64", 0), proj, mode="apply", path=SPLIT, parallel=True)
+    run_case(sy.draw("mixed64", 0), proj, mode="apply", path=SPLIT, parallel=True, host_offsets=True)
 
 
 def test_mixed64_without_host_offsets_takes_one_path():
@@ -680,7 +683,7 @@ def test_mixed64_without_host_offsets_takes_one_path():
     length (here mma.sync for everything); same results."""
     lk, device = _lk(), _dev()
     raw = sy.draw("mixed64", 1)
-    dev = device.prepare(raw, "qkv")
+    dev = device.prepare(raw, "qkv", host_offsets=True)
     r = dev["routing"]
     plain = lk.Routing(r.lora_ids, r.grouped_offsets, r.num_groups, r.end)
     lk.lora_sgmv_apply(dev["problem"], plain, dev["workspace"])
@@ -705,7 +708,7 @@ def test_kernels_per_group_ragged_and_ranks(R):
     spec = _spec(max_num_loras=10, max_lora_rank=R, rank_choices=(16, R), kind="fixed",
                  fixed_slots=(9, 8, 7, 6, 5, 4, 3, 2, 1, 0, -1), fixed_lens=(1, 64, 2, 65, 63, 129, 17, 300, 5, 33, 8),
                  hidden=512, n_heads=8, n_kv_heads=2, head_dim=64)
-    run_case(sy.draw(spec, 100 + R), "qkv", mode="apply", path=SPLIT)
-    run_case(sy.draw(spec, 101 + R), "o", mode="apply", path=SPLIT)
+    run_case(sy.draw(spec, 100 + R), "qkv", mode="apply", path=SPLIT, host_offsets=True)
+    run_case(sy.draw(spec, 101 + R), "o", mode="apply", path=SPLIT, host_offsets=True)
     raw = sy.add_bias(sy.draw(spec, 102 + R), 102 + R)
-    run_case(raw, "qkv", mode="apply", slot_ranks=True, poison=True, path=SPLIT)
+    run_case(raw, "qkv", mode="apply", slot_ranks=True, poison=True, path=SPLIT, host_offsets=True)

@@ -11,12 +11,12 @@
 // disappears.  u (the shrink's fp32 partial planes, summed here) comes from
 // the library's shrink kernels, launched first on the same stream.
 //
-// Tensor cores (tcgen05), one CTA per (128-row tile of the batch, 128-column
-// block of one slice's outputs), 6 warps:
+// Tensor cores (tcgen05), one CTA per (128-row tile of the batch, 128- or
+// 256-column block of one slice's outputs), 6 warps:
 //   warp 0   TMA producer: per 64-wide K stage one box of the tile's x rows
-//            (128 x 64) and one of the block's W0 rows (128 x 64), 128-byte
+//            (128 x 64) and one of the block's W0 rows (N x 64), 128-byte
 //            swizzle, through a ring of stages;
-//   warp 1   TMEM owner and MMA issuer: M=128 N=128, K=16 per instruction,
+//   warp 1   TMEM owner and MMA issuer: M=128 N=128 or 256, K=16 per instruction,
 //            then the LoRA K tail: for every group overlapping the tile, K = 2R
 //            more steps with the masked u image (u's hi part, then its lo part:
 //            u = hi + lo, both bf16, exact split) against the slot's B block;
@@ -43,22 +43,27 @@ namespace lora {
 namespace {
 
 constexpr int BM = 128;        // rows per tile (MMA M)
-constexpr int BN = 128;        // output columns per tile (MMA N)
 constexpr int BK = 64;         // K per stage
 constexpr int BTHREADS = 192;  // 6 warps
 constexpr int MAX_STAGES_B = 4;
 constexpr int MAX_TILE_GROUPS = BM;  // a 128-row tile overlaps at most 128 non-empty groups
 
-template <int R>
+// BN: output columns per tile (MMA N): 128, or 256 for batches of many
+// rows (twice the MMA work per byte staged).
+template <int R, int BN_>
 struct BaseCfg {
-  static constexpr int BSTAGES = R >= 128 ? 3 : 4;        // ring depth within ~227 KB
+  static constexpr int BN = BN_;
   static constexpr int X_BYTES = BM * BK * 2;                // 16 KB
-  static constexpr int W_BYTES = BN * BK * 2;                // 16 KB
+  static constexpr int W_BYTES = BN * BK * 2;                // 16 or 32 KB
   static constexpr int STAGE = X_BYTES + W_BYTES;
   static constexpr int UB = (2 * R + 63) / 64;               // 64-wide K blocks of u's hi | lo
   static constexpr int BB = (R + 63) / 64;                   // 64-wide K blocks of B
   static constexpr int U_BYTES = UB * BM * 128;
   static constexpr int B_BYTES = BB * BN * 128;
+  // Ring depth: as many stages as ~224 KB hold next to the K-tail operands.
+  static constexpr int BSTAGES_RAW = (224 * 1024 - U_BYTES - B_BYTES - 1024) / STAGE;
+  static constexpr int BSTAGES = BSTAGES_RAW > 4 ? 4 : BSTAGES_RAW;
+  static_assert(BSTAGES >= 2, "ring too shallow");
   static constexpr int SMEM = BSTAGES * STAGE + U_BYTES + B_BYTES + 1024;
 };
 
@@ -83,18 +88,18 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// Byte offset of bf16 element (row r, k) in a K-major operand of [128 x 64]
+// Byte offset of bf16 element (row r, k) in a K-major operand of [rows x 64]
 // blocks with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)).
-__device__ __forceinline__ uint32_t bsw(int r, int k) {
+__device__ __forceinline__ uint32_t bsw(int r, int k, int rows) {
   const int kb = k >> 6, kk = k & 63;
-  return (uint32_t)(kb * BM * 128 + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + ((kk & 7) << 1));
+  return (uint32_t)(kb * rows * 128 + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + ((kk & 7) << 1));
 }
 
 }  // namespace
 
 struct BaseMaps {
   CUtensorMap x;                    // [T rows, in] bf16, box 64 x 128
-  CUtensorMap w[LORA_MAX_SLICES];   // per slice W0 [out_j rows, in] bf16, box 64 x 128
+  CUtensorMap w[LORA_MAX_SLICES];   // per slice W0 [out_j rows, in] bf16, box 64 x BN
 };
 
 struct BaseWork {
@@ -105,12 +110,12 @@ struct BaseWork {
   int wait_first;                      // 1: no shrink precedes; every role waits for the previous kernel
 };
 
-template <int R>
+template <int R, int BN>
 __global__ void __launch_bounds__(BTHREADS, 1) sgmv_base_gemm_kernel(const __grid_constant__ ProblemDesc p,
                                                                      const __grid_constant__ BaseMaps maps,
                                                                      const __grid_constant__ BaseWork w,
                                                                      const float* __restrict__ u) {
-  using Cfg = BaseCfg<R>;
+  using Cfg = BaseCfg<R, BN>;
   constexpr int BSTAGES = Cfg::BSTAGES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[MAX_STAGES_B], empty[MAX_STAGES_B], uready, ufree, done;
@@ -255,13 +260,15 @@ __global__ void __launch_bounds__(BTHREADS, 1) sgmv_base_gemm_kernel(const __gri
       if (g > 0 && !bad && !mbar_wait(&ufree, (uint32_t)((g - 1) & 1))) bad = true;
       bad = __any_sync(0xffffffffu, bad);
       if (!bad) {
-        // B rows: output o0 + r of the slot, K columns [0, min(R, kmax)).
+        // B rows: outputs o0 + r (+ 128, ...) of the slot, K columns [0, min(R, kmax)).
         const int slot = s_gslot[g];
         const int kmax = slot_kmax(p, slot);
-        if (o0 + r < sl.out_dim) {
-          const __nv_bfloat16* brow = static_cast<const __nv_bfloat16*>(sl.B) + (long long)slot * sl.B_slot_stride +
-                                      (long long)(o0 + r) * R;
-          for (int c = 0; c * 8 < kmax; ++c) cp_async16(Bs + bsw(r, 8 * c), brow + 8 * c);
+        for (int br = r; br < BN; br += BM) {
+          if (o0 + br < sl.out_dim) {
+            const __nv_bfloat16* brow = static_cast<const __nv_bfloat16*>(sl.B) +
+                                        (long long)slot * sl.B_slot_stride + (long long)(o0 + br) * R;
+            for (int c = 0; c * 8 < kmax; ++c) cp_async16(Bs + bsw(br, 8 * c, BN), brow + 8 * c);
+          }
         }
         cp_async_commit();
         // u rows of the group (sum of the planes, plane order), hi | lo; zero elsewhere.
@@ -281,8 +288,8 @@ __global__ void __launch_bounds__(BTHREADS, 1) sgmv_base_gemm_kernel(const __gri
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) split_hi_lo_bf16x2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
-          *reinterpret_cast<uint4*>(Us + bsw(r, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(Us + bsw(r, R + k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(Us + bsw(r, k, BM)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(Us + bsw(r, R + k, BM)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         cp_async_wait<0>();
       }
@@ -406,11 +413,19 @@ PFN_cuTensorMapEncodeTiled_v12000 base_encode_fn() {
   return fn;
 }
 
+// Tile width: 256 output columns for batches of at least this many rows
+// (long K loops at full MMA rate need twice the work per staged byte), 128
+// otherwise (more CTAs for small batches).  Ranks above 64 keep 128 (the
+// K-tail operands would leave too shallow a ring).
+constexpr int kWideTileRows = 1024;
+int base_bn(const ProblemDesc& p) { return (p.num_tokens >= kWideTileRows && p.R <= 64) ? 256 : 128; }
+
 bool encode_base_maps(const ProblemDesc& p, const BaseWeights& wts, BaseMaps* m) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = base_encode_fn();
   if (!enc) return false;
   const cuuint32_t es[2] = {1, 1};
   const cuuint32_t box[2] = {(cuuint32_t)BK, 128};
+  const cuuint32_t wbox[2] = {(cuuint32_t)BK, (cuuint32_t)base_bn(p)};
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.in_dim, (cuuint64_t)p.num_tokens};
     const cuuint64_t strides[1] = {(cuuint64_t)p.x_row_stride * 2};
@@ -422,7 +437,7 @@ bool encode_base_maps(const ProblemDesc& p, const BaseWeights& wts, BaseMaps* m)
   for (int j = 0; j < p.n_slices; ++j) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.in_dim, (cuuint64_t)p.sl[j].out_dim};
     const cuuint64_t strides[1] = {(cuuint64_t)wts.row_stride[j] * 2};
-    if (enc(&m->w[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(wts.W0[j]), dims, strides, box, es,
+    if (enc(&m->w[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(wts.W0[j]), dims, strides, wbox, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
@@ -430,10 +445,10 @@ bool encode_base_maps(const ProblemDesc& p, const BaseWeights& wts, BaseMaps* m)
   return true;
 }
 
-template <int R>
+template <int R, int BN>
 cudaError_t launch_base_t(const ProblemDesc& p, const BaseMaps& maps, const BaseWork& w, const float* u,
                           cudaStream_t s) {
-  auto kernel = sgmv_base_gemm_kernel<R>;
+  auto kernel = sgmv_base_gemm_kernel<R, BN>;
   static unsigned long long done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -441,7 +456,7 @@ cudaError_t launch_base_t(const ProblemDesc& p, const BaseMaps& maps, const Base
   {
     std::lock_guard<std::mutex> lk(g_base_mu);
     if (!(done & (1ull << (dev & 63)))) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BaseCfg<R>::SMEM);
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BaseCfg<R, BN>::SMEM);
       if (e != cudaSuccess) return e;
       done |= 1ull << (dev & 63);
     }
@@ -449,7 +464,7 @@ cudaError_t launch_base_t(const ProblemDesc& p, const BaseMaps& maps, const Base
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)w.nbt, (unsigned)((p.num_tokens + BM - 1) / BM));
   cfg.blockDim = dim3(BTHREADS);
-  cfg.dynamicSmemBytes = BaseCfg<R>::SMEM;
+  cfg.dynamicSmemBytes = BaseCfg<R, BN>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -481,6 +496,7 @@ cudaError_t launch_base_gemm(const ProblemDesc& p, const BaseWeights& wts, const
   BaseMaps maps;
   if (!encode_base_maps(p, wts, &maps)) return cudaErrorNotSupported;
   BaseWork w{};
+  const int BN = base_bn(p);
   int acc = 0;
   for (int j = 0; j < p.n_slices; ++j) {
     w.blk_begin[j] = acc;
@@ -491,11 +507,19 @@ cudaError_t launch_base_gemm(const ProblemDesc& p, const BaseWeights& wts, const
   w.nsplit = nsplit;
   w.plane_stride = (long long)p.end * p.n_slices * p.R;
   w.wait_first = after_shrink ? 0 : 1;
+  if (BN == 256) {
+    switch (p.R) {
+      case 16: return launch_base_t<16, 256>(p, maps, w, u, s);
+      case 32: return launch_base_t<32, 256>(p, maps, w, u, s);
+      case 64: return launch_base_t<64, 256>(p, maps, w, u, s);
+    }
+    return cudaErrorNotSupported;
+  }
   switch (p.R) {
-    case 16: return launch_base_t<16>(p, maps, w, u, s);
-    case 32: return launch_base_t<32>(p, maps, w, u, s);
-    case 64: return launch_base_t<64>(p, maps, w, u, s);
-    case 128: return launch_base_t<128>(p, maps, w, u, s);
+    case 16: return launch_base_t<16, 128>(p, maps, w, u, s);
+    case 32: return launch_base_t<32, 128>(p, maps, w, u, s);
+    case 64: return launch_base_t<64, 128>(p, maps, w, u, s);
+    case 128: return launch_base_t<128, 128>(p, maps, w, u, s);
   }
   return cudaErrorNotSupported;
 }

@@ -84,6 +84,28 @@ __device__ __forceinline__ void pack_u16(uint8_t* blk, int R, int r, int k0, con
 
 }  // namespace
 
+// Gathered batches (token_rows): the x / y row of every position of tile t;
+// positions past the tile's rows repeat its first row (their results are
+// never stored).  Executed by one full warp; false on every lane (and
+// LORA_DEV_BAD_ROW recorded) if an entry is out of range.
+__device__ __forceinline__ bool warp_tile_rows(const ProblemDesc& p, const Tile& t, int* rows) {
+  const int lane = threadIdx.x & 31;
+  int bad = 0;
+  const int first = p.token_rows[t.row0];
+  for (int r = lane; r < TM; r += 32) {
+    const int v = r < t.rows ? p.token_rows[t.row0 + r] : first;
+    if (v < 0 || v >= p.num_tokens) bad = 1;
+    rows[r] = v;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (bad && lane == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
+  return !bad;
+}
+
+// Copies in flight of a gathered x stream (stages whose 16-byte copies the
+// producer warp has issued but not yet signalled).
+constexpr int kGatherDepth = 3;
+
 struct TcMaps {
   CUtensorMap x;                     // [T rows, in] bf16, box 64 x 128
   CUtensorMap a[LORA_MAX_SLICES];    // per slice [S, R, in] bf16, box 64 x R x 1 (full rank)
@@ -112,6 +134,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   __shared__ int s_ok;
   __shared__ int s_fail;
   __shared__ int s_kmax;
+  __shared__ int s_rows[TM];  // gathered batches: the x row of each tile position
 
   // 1024-byte aligned ring (the 128-byte swizzle repeats every 1024 bytes).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -124,16 +147,20 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   const int cn = (int)((blockIdx.x / (unsigned)nsplit) % (unsigned)nsn);
   const long long tile = blockIdx.x / (unsigned)(nsplit * nsn);
   const int n_base = cn * NR;  // first u column of this CTA
+  const bool gathered = p.token_rows != nullptr;
   if (warp == 0) {
     Tile t{};
-    const bool ok = warp_locate_tile(p, TM, tile, t);
+    bool ok = warp_locate_tile(p, TM, tile, t);
+    if (ok && gathered) ok = warp_tile_rows(p, t, s_rows);  // a bad entry skips the tile
     if (lane == 0) {
       s_tile = t;
       s_ok = ok;
       s_fail = 0;
       s_kmax = ok ? slot_kmax(p, t.slot) : 0;
       for (int i = 0; i < NSTAGE; ++i) {
-        mbar_init(&full[i], 1);
+        // gathered: one arrival for the A boxes' bytes, one when the warp's
+        // copies of the stage's x rows have landed
+        mbar_init(&full[i], gathered ? 2 : 1);
         mbar_init(&empty[i], 1);
       }
       mbar_init(&done, 1);
@@ -159,7 +186,67 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   const int k0 = split * kc;
   const int nst = kc / TK;
 
-  if (ok && warp == 0 && lane == 0) {
+  if (ok && warp == 0 && gathered) {
+    // ---- producer, gathered batch: the whole warp copies the tile's x rows
+    // (scattered through token_rows) with 16-byte async copies into the
+    // stage's 128-byte-swizzled layout, kGatherDepth stages deep, and lane 0
+    // signals each stage once its copies have landed; the A rows come by TMA
+    // as below.
+    const uint64_t pol_keep = policy_evict_last();
+    uint32_t a_bytes = 0;
+    for (int j = 0; j < p.n_slices; ++j) {
+      const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+      if (khi > klo) a_bytes += (uint32_t)((khi - klo) * TK * 2);
+    }
+    const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+    int signalled = 0;  // stages whose x copies have been signalled
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % NSTAGE;
+      bool free_ok = true;
+      if (s >= NSTAGE && lane == 0) free_ok = mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1));
+      if (!__shfl_sync(0xffffffffu, (int)free_ok, 0)) {
+        if (lane == 0) atomicOr(&s_fail, 1);
+        break;
+      }
+      uint8_t* xs = smem + slot * Cfg::STAGE;
+      uint8_t* as = xs + Cfg::X_BYTES;
+      const int kk = k0 + s * TK;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[slot], a_bytes);
+        for (int j = 0; j < p.n_slices; ++j) {
+          const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+          if (khi <= klo) continue;
+          uint8_t* dst = as + (j * R - n_base) * TK * 2;
+          if (klo == 0 && khi == R) {
+            tma_load_3d_hint(dst, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
+          } else {
+            int kb = klo;
+            for (; kb + 64 <= khi; kb += 64)
+              tma_load_3d_hint(dst + kb * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
+            for (; kb < khi; kb += 16)
+              tma_load_3d_hint(dst + kb * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
+          }
+        }
+      }
+      for (int e = lane; e < TM * (TK / 8); e += 32) {  // row r, 16-byte chunk c
+        const int r = e >> 3, c = e & 7;
+        cp_async16(xs + r * 128 + ((c ^ (r & 7)) << 4), xg + (long long)s_rows[r] * p.x_row_stride + kk + c * 8);
+      }
+      cp_async_commit();
+      if (s - signalled >= kGatherDepth - 1) {  // the oldest stage in flight has landed
+        cp_async_wait<kGatherDepth - 1>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[signalled % NSTAGE]);
+        ++signalled;
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0)
+      for (; signalled < nst; ++signalled) mbar_arrive(&full[signalled % NSTAGE]);
+  } else if (ok && warp == 0 && lane == 0) {
     // ---- producer (x streams through L2 once; the slot's A rows are re-read
     // by every tile of the group, so they are kept)
     const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
@@ -570,7 +657,6 @@ int tc_shrink_splits(int end, int in_dim, int sms) {
 }
 
 bool tc_shapes_ok(const ProblemDesc& p) {
-  if (p.token_rows) return false;  // TMA boxes need the tile's rows contiguous
   const int nR = p.n_slices * p.R;
   switch (nR) {
     case 16: case 32: case 48: case 64: case 96: case 128: case 192: case 256: case 384: break;
@@ -807,9 +893,11 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       const int slot = i % NSLOT;
       uint8_t* ys = slots + slot * Cfg::SLOT;
       uint8_t* bs = ys + Cfg::Y_BYTES;
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)(Cfg::Y_BYTES + nbbox * XB * 128));
-      for (int yb = 0; yb < XB / 64; ++yb)
-        tma_load_2d_hint(ys + yb * TM * 128, &maps.y[x.j], x.o0 + yb * 64, t.row0, &full[slot], pol_stream);
+      // Gathered batches: the epilogue reads its y rows itself (scattered).
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)((p.token_rows ? 0 : Cfg::Y_BYTES) + nbbox * XB * 128));
+      if (!p.token_rows)
+        for (int yb = 0; yb < XB / 64; ++yb)
+          tma_load_2d_hint(ys + yb * TM * 128, &maps.y[x.j], x.o0 + yb * 64, t.row0, &full[slot], pol_stream);
       for (int kb = 0; kb < nbbox; ++kb)
         tma_load_3d_hint(bs + kb * XB * 128, &maps.b[x.j], kb * 64, x.o0, t.slot, &full[slot], pol_keep);
     };
@@ -954,7 +1042,10 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       };
 
       const uint64_t pol_stream = policy_evict_first();
+      const bool gathered = p.token_rows != nullptr;
       int cur_tile = -1, cur_j = -1, seg = -1, kmax = 0;
+      int yrow = 0;            // gathered: the y row of this thread's tile position
+      bool tile_skip = false;  // gathered: the tile has an out-of-range entry
       Tile t{};
       int i = 0;
       for (long long un = u0; un < u1; ++un, ++i) {
@@ -964,7 +1055,19 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
           // (its TMEM results were all consumed), so the u buffer it read is
           // free: fill this segment's buffer if it was not prefetched, then
           // prefetch the next segment's into the freed one.
-          if (x.tile != cur_tile) t = rc_tile(rc, G, x.tile);
+          if (x.tile != cur_tile) {
+            t = rc_tile(rc, G, x.tile);
+            if (gathered) {  // every warp checks the whole tile: the same outcome everywhere
+              int badrow = 0;
+              for (int r = lane; r < t.rows; r += 32) {
+                const int v = p.token_rows[t.row0 + r];
+                if (v < 0 || v >= p.num_tokens) badrow = 1;
+              }
+              tile_skip = __any_sync(0xffffffffu, badrow) != 0;
+              if (tile_skip && lane == 0) atomicOr(p.status, LORA_DEV_BAD_ROW);
+              yrow = (!tile_skip && row < t.rows) ? p.token_rows[t.row0 + row] : 0;
+            }
+          }
           cur_tile = x.tile;
           cur_j = x.j;
           ++seg;
@@ -999,7 +1102,8 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
         // 32 columns per TMEM load: two 16-column groups.
-        for (int c32 = hf * XB / (32 * XNH); !bad && c32 < (hf + 1) * XB / (32 * XNH); ++c32) {
+        const bool work = !bad && !tile_skip;
+        for (int c32 = hf * XB / (32 * XNH); work && c32 < (hf + 1) * XB / (32 * XNH); ++c32) {
           float dd[32];
           if (kmax > 0) {
             tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c32 * 32), dd);
@@ -1023,7 +1127,26 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
                 d[2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
               }
             }
-            if (live && c16 * 16 < ovalid) {
+            if (gathered && live && c16 * 16 < ovalid) {
+              // Gathered: y + delta for this thread's own (scattered) row,
+              // read and written straight in global memory, rounded once.
+              uint4* gy = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
+                                                   (long long)yrow * sl.y_row_stride + o0 + c16 * 16);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                if (c16 * 16 + h * 8 >= ovalid) continue;
+                const uint4 yv = gy[h];
+                const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+                uint32_t out[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 yy = make_float2(__uint_as_float(yw[e] << 16), __uint_as_float(yw[e] & 0xFFFF0000u));
+                  const float2 r = add_f32x2(yy, make_float2(d[h * 8 + 2 * e], d[h * 8 + 2 * e + 1]));
+                  out[e] = round_pack_bf16x2(r.x, r.y);
+                }
+                gy[h] = make_uint4(out[0], out[1], out[2], out[3]);
+              }
+            } else if (live && c16 * 16 < ovalid) {
               // y + delta, rounded once, written back over y in the slot.
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
@@ -1046,7 +1169,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         __syncwarp();
         // This warp's 32 rows x XB / XNH columns to y: eight lanes per row,
         // so each store instruction writes whole 128-byte row segments.
-        if (!bad) {
+        if (work && !gathered) {
           constexpr int CPR = XB / XNH / 8;   // 16-byte chunks per row
           constexpr int RPI = 32 / CPR;       // rows per store instruction
           const int cch = hf * CPR + lane % CPR;  // this lane's chunk of the 128-column block
@@ -1276,7 +1399,7 @@ cudaError_t launch_tc_apply_packed(const ProblemDesc& p, void* workspace, cudaSt
   const int nsn = tc_pack_splits(p);
   uint8_t* upk = static_cast<uint8_t*>(workspace);
   cudaError_t e = cudaErrorNotSupported;
-  if (nsn > 1) e = launch_ksplit(p, smaps, upk, s, nsn);
+  if (nsn > 1 && !p.token_rows) e = launch_ksplit(p, smaps, upk, s, nsn);
   if (e == cudaErrorNotSupported) e = launch_tc_shrink_maps(p, smaps, nullptr, s, 1, nsn, upk);
   if (e != cudaSuccess) return e;
   const TxWork w = make_tx_work(p, 1);

@@ -498,6 +498,33 @@ def _profiled_traffic(workload):
     return None
 
 
+def unsorted_block(wb, sampler, peaks):
+    """The first problem's apply on the same batch given in ARRIVAL order:
+    x and y rows as the requests arrived, token_rows (lora_build_token_rows)
+    mapping the sorted positions to them (the per-token routing of the vLLM
+    page, section 6), timed like the sorted apply."""
+    lk, torch = wb.lk, wb.torch
+    calls = []
+    for s in wb.sets:
+        d = s["p0"]
+        r, rt, raw = d["routing"], d["route_host"], s["raw"]
+        rows = lk.lora_build_token_rows(raw["req_len"], rt["perm"], rt["end"])
+        tr = torch.from_numpy(rows).to("cuda")
+        s["_token_rows"] = tr
+        calls.append(lk.CallBuilder(d["problem"], lk.Routing(r.lora_ids, r.grouped_offsets, r.num_groups, r.end, tr),
+                                    d["workspace"]))
+    with torch.cuda.stream(wb.stream):
+        calls[0].apply(wb.stream)
+    wb.stream.synchronize()
+    g = wb._graph(lambda st: [c.apply(st) for c in calls])
+    t = statistics.median(wb.trials(g, wb.NS, sampler=sampler))
+    rb = roofline_block(wb, [t], *peaks, traffic=None)
+    return {"avg_apply_us": rb["avg_launch_us"], "frac": rb["frac"], "achieved_GBps": rb["achieved"],
+            "kernel_path": hex(calls[0].last_path),
+            "note": "same batch with rows in arrival order and token_rows: x rows gathered by the shrink, y rows "
+                    "read and written in place by the expand"}
+
+
 def one_path_block(wb, sampler, peaks):
     """The first problem's apply without the routing's host offsets (one
     kernel family for the whole call, chosen from the average group length),
@@ -706,6 +733,8 @@ def run_ours(args):
                 continue
             sb = WorkloadBench(name, args, rank, lk, torch, stream, l2)
             secondary[name] = workload_summary(sb, sampler, peaks)
+            if name == "prefill8b":
+                secondary[name]["unsorted"] = unsorted_block(sb, sampler, peaks)
             if not args.no_base_fused:
                 secondary[name]["base_fused"] = base_fused_block(sb, sampler, peaks)
             del sb

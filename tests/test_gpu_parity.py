@@ -263,9 +263,10 @@ def test_mlp_long_groups_tensor_core_path(mode):
     run_case(sy.draw(spec, 10), "down", mode=mode, path=TC)
 
 
-def run_unsorted(raw, proj="qkv", mode="apply"):
+def run_unsorted(raw, proj="qkv", mode="apply", path=None, parallel=False):
     """x and y rows in ARRIVAL order; token_rows maps the sorted order to rows.
-    Compared with the per-token oracle (slot of each row, no routing triple)."""
+    Compared with the per-token oracle (slot of each row, no routing triple).
+    path: the exact kernel families the call(s) must take (None: no check)."""
     lk, device = _lk(), _dev()
     dev = device.prepare(raw, proj)
     rt = dev["route_host"]
@@ -276,18 +277,23 @@ def run_unsorted(raw, proj="qkv", mode="apply"):
     y_before = device.y_host(dev)
     if mode == "apply":
         lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
+        taken = lk.lora_last_call_path()[0]
     else:
         nR = len(dev["names"]) * raw["max_lora_rank"]
         u = torch.empty((max(rt["end"], 1), nR), dtype=torch.float32, device="cuda")
         lk.lora_shrink(dev["problem"], routing, u)
+        taken = lk.lora_last_call_path()[0]
         lk.lora_expand(dev["problem"], routing, u)
+        taken |= lk.lora_last_call_path()[0]
     torch.cuda.synchronize()
     assert lk.lora_get_device_status() == 0
+    if path is not None:
+        assert taken == path, ("kernel path", hex(taken), hex(path))
     y_after = device.y_host(dev)
     ref = oracle.prepare_problem(raw, proj)
     slots = oracle.row_slots(raw["req_slot"], raw["req_len"])
     all_rows = np.arange(raw["T"], dtype=np.int32)
-    _, ys = oracle.problem_token_rows(ref, all_rows, slots)
+    _, ys = oracle.problem_token_rows(ref, all_rows, slots, parallel=parallel)
     got = oracle.to_f64(y_after, raw["dtype"])
     base = slots < 0
     assert np.array_equal(_bits(y_after[base]), _bits(y_before[base]))
@@ -312,6 +318,48 @@ def test_unsorted_multi_token_requests(mode):
                  head_dim=64)
     run_unsorted(sy.draw(spec, 11), "qkv", mode)
     run_unsorted(sy.draw(_spec(dtype="f32", n_requests=20), 12), "qkv", mode)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+@pytest.mark.parametrize("R", [16, 64, 128])
+def test_unsorted_long_groups_tensor_core(mode, R):
+    """Unsorted (arrival-order) batches of long groups on the tcgen05 path:
+    the shrink gathers x rows through token_rows (16-byte async copies into
+    the swizzled stages), the expand reads and writes its scattered y rows
+    itself.  Ragged 128-row tiles; per-token oracle on every row."""
+    spec = _spec(max_num_loras=5, max_lora_rank=R, rank_choices=(R // 2, R), kind="fixed",
+                 fixed_slots=(2, -1, 0, 4, 1, 3, 0, 2), fixed_lens=(130, 17, 255, 128, 97, 300, 64, 90),
+                 hidden=512, n_heads=8, n_kv_heads=2, head_dim=64)
+    want = TC if R >= 64 else TC_MMA
+    run_unsorted(sy.draw(spec, 110 + R), "qkv", mode, path=want)
+    run_unsorted(sy.draw(spec, 111 + R), "o", mode, path=want)
+
+
+@pytest.mark.parametrize("mode", ["apply", "split"])
+def test_unsorted_prefill8b_tensor_core(mode):
+    """The full-size prefill batch in arrival order (token_rows), on tcgen05,
+    every row against the per-token oracle."""
+    run_unsorted(sy.draw("prefill8b", 7), "qkv", mode, path=TC, parallel=True)
+
+
+def test_unsorted_long_groups_bad_row_is_flagged():
+    """An out-of-range token_rows entry on the tcgen05 path raises
+    LORA_DEV_BAD_ROW (the tile holding it is skipped)."""
+    lk, device = _lk(), _dev()
+    spec = _spec(max_num_loras=3, max_lora_rank=64, rank_choices=(64,), kind="fixed",
+                 fixed_slots=(1, 0, 2), fixed_lens=(200, 300, 150), hidden=256, n_heads=4, n_kv_heads=2,
+                 head_dim=64)
+    raw = sy.draw(spec, 120)
+    dev = device.prepare(raw, "qkv")
+    rt = dev["route_host"]
+    rows = lk.lora_build_token_rows(raw["req_len"], rt["perm"], rt["end"])
+    rows[5] = raw["T"] + 7
+    routing = lk.Routing(dev["routing"].lora_ids, dev["routing"].grouped_offsets, rt["num_groups"], rt["end"],
+                         torch.from_numpy(rows).cuda())
+    assert lk.lora_get_device_status() == 0
+    lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
+    assert lk.lora_last_call_path()[0] == TC
+    assert lk.lora_get_device_status() & lk.DEV_BAD_ROW
 
 
 def test_token_rows_out_of_range_is_flagged_and_skipped():

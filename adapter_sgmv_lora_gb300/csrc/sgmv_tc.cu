@@ -102,10 +102,6 @@ __device__ __forceinline__ bool warp_tile_rows(const ProblemDesc& p, const Tile&
   return !bad;
 }
 
-// Copies in flight of a gathered x stream (stages whose 16-byte copies the
-// producer warp has issued but not yet signalled).
-constexpr int kGatherDepth = 3;
-
 struct TcMaps {
   CUtensorMap x;                     // [T rows, in] bf16, box 64 x 128
   CUtensorMap a[LORA_MAX_SLICES];    // per slice [S, R, in] bf16, box 64 x R x 1 (full rank)
@@ -189,9 +185,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   if (ok && warp == 0 && gathered) {
     // ---- producer, gathered batch: the whole warp copies the tile's x rows
     // (scattered through token_rows) with 16-byte async copies into the
-    // stage's 128-byte-swizzled layout, kGatherDepth stages deep, and lane 0
-    // signals each stage once its copies have landed; the A rows come by TMA
-    // as below.
+    // stage's 128-byte-swizzled layout, as many stages deep as the ring, and
+    // lane 0 signals each stage once its copies have landed; the A rows come
+    // by TMA as below.
+    constexpr int kGatherDepth = NSTAGE;
     const uint64_t pol_keep = policy_evict_last();
     uint32_t a_bytes = 0;
     for (int j = 0; j < p.n_slices; ++j) {
@@ -354,19 +351,21 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
 // The apply's shrink with the input dimension split over a cluster of CL
 // CTAs (2 or 4) per 128-row tile, for batches with too few tiles to fill
 // the GPU one CTA per tile.  Each CTA streams its K range of the tile's x rows
-// (so x is read once) and of the slot's A rows for ALL n*R columns; the CL
-// partial accumulators are then exchanged through distributed shared memory:
-// CTA q owns columns [q*NR/CL, (q+1)*NR/CL), receives the other CTAs' partials
-// of those columns into its (then idle) stage ring, sums the CL partials in
-// rank order (the same order on every CTA: deterministic) and stores them
-// packed (pack_u16).  Two cluster barriers: before the exchange (every CTA's
-// MMAs have drained its ring) and after it.
-template <int NR, int CL>
+// (so each column part reads x once) and of the slot's A rows for its NR
+// columns (all n*R, or one of nsn column parts); the CL partial accumulators
+// are then exchanged through distributed shared memory: CTA q owns columns
+// [q*NR/CL, (q+1)*NR/CL) of the part, receives the other CTAs' partials of
+// those columns into its (then idle) stage ring, sums the CL partials in rank
+// order (the same order on every CTA: deterministic) and stores them packed
+// (pack_u16).  Two cluster barriers: before the exchange (every CTA's MMAs
+// have drained its ring) and after it.  NST: ring depth -- a shallow ring
+// lets two CTAs share an SM when the grid has more CTAs than SMs.
+template <int NR, int CL, int NST>
 __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(const __grid_constant__ ProblemDesc p,
                                                                            const __grid_constant__ TcMaps maps,
-                                                                           uint8_t* __restrict__ upk) {
+                                                                           uint8_t* __restrict__ upk, int nsn) {
   using Cfg = TcCfg<NR>;
-  constexpr int NSTAGE = Cfg::NSTAGE;
+  constexpr int NSTAGE = NST;
   constexpr int NRC = NR / CL;  // columns each CTA sums and stores
   static_assert(NRC % 16 == 0, "column share");
   static_assert((CL - 1) * TM * NRC * 4 <= NSTAGE * Cfg::STAGE, "exchange buffer must fit in the ring");
@@ -384,7 +383,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)(blockIdx.x % (unsigned)CL);  // rank in the cluster (cluster dims CL x 1 x 1)
-  const long long tile = blockIdx.x / (unsigned)CL;
+  const int cn = (int)((blockIdx.x / (unsigned)CL) % (unsigned)nsn);
+  const long long tile = blockIdx.x / (unsigned)(CL * nsn);
+  const int n_base = cn * NR;  // first u column of this cluster's part
   if (warp == 0) {
     Tile t{};
     const bool ok = warp_locate_tile(p, TM, tile, t);
@@ -421,7 +422,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
   if (ok && warp == 0 && lane == 0) {
     const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
     uint32_t a_bytes = Cfg::X_BYTES;
-    for (int j = 0; j < p.n_slices; ++j) a_bytes += (uint32_t)(min(R, kmax) * TK * 2);
+    for (int j = 0; j < p.n_slices; ++j) {
+      const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+      if (khi > klo) a_bytes += (uint32_t)((khi - klo) * TK * 2);
+    }
     for (int s = 0; s < nst; ++s) {
       const int slot = s % NSTAGE;
       if (s >= NSTAGE && !mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1))) {
@@ -434,12 +438,14 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
       const int kk = k0 + s * TK;
       tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
       for (int j = 0; j < p.n_slices; ++j) {
-        uint8_t* dst = as + j * R * TK * 2;
-        const int khi = min(R, kmax);
-        if (khi == R) {
+        // Rows [klo, khi) of slice j fall in this part's columns (and the rank).
+        const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+        if (khi <= klo) continue;
+        uint8_t* dst = as + (j * R - n_base) * TK * 2;
+        if (klo == 0 && khi == R) {
           tma_load_3d_hint(dst, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
         } else {
-          int kb = 0;
+          int kb = klo;
           for (; kb + 64 <= khi; kb += 64)
             tma_load_3d_hint(dst + kb * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
           for (; kb < khi; kb += 16)
@@ -530,7 +536,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
           }
         }
       }
-      const int col = crank * NRC + c, j = col / R, k = col - j * R;
+      const int col = n_base + crank * NRC + c, j = col / R, k = col - j * R;
       const bool keep = k < kmax;  // columns past the slot's rank read no A rows: 0
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] = (keep && live) ? v[e] : 0.f;
@@ -1092,6 +1098,17 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const SliceDesc& sl = p.sl[x.j];
         const bool live = row < t.rows;
         const int slot = i % NSLOT, buf = i & 1;
+        // Gathered: this thread's y row segment (XB / XNH columns) is loaded
+        // before the wait for the unit's MMAs, so the loads overlap them.
+        constexpr int GCH = XB / XNH / 8;  // 16-byte chunks of the segment
+        uint4 yseg[GCH];
+        if (gathered && !tile_skip && live) {
+          const uint4* gy = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(sl.y) +
+                                                           (long long)yrow * sl.y_row_stride + x.o0 + hf * (XB / XNH));
+          const int nvalid = min(XB, sl.out_dim - x.o0) - hf * (XB / XNH);
+#pragma unroll
+          for (int c = 0; c < GCH; ++c) yseg[c] = c * 8 < nvalid ? gy[c] : make_uint4(0, 0, 0, 0);
+        }
         if (!bad && !mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
           atomicOr(&s_fail, 1);
           bad = true;
@@ -1103,7 +1120,10 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const int ovalid = min(XB, sl.out_dim - o0);
         // 32 columns per TMEM load: two 16-column groups.
         const bool work = !bad && !tile_skip;
-        for (int c32 = hf * XB / (32 * XNH); work && c32 < (hf + 1) * XB / (32 * XNH); ++c32) {
+#pragma unroll
+        for (int cc = 0; cc < XB / (32 * XNH); ++cc) {
+          if (!work) break;
+          const int c32 = hf * (XB / (32 * XNH)) + cc;
           float dd[32];
           if (kmax > 0) {
             tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * XB + c32 * 32), dd);
@@ -1129,13 +1149,13 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
             }
             if (gathered && live && c16 * 16 < ovalid) {
               // Gathered: y + delta for this thread's own (scattered) row,
-              // read and written straight in global memory, rounded once.
+              // written straight to global memory, rounded once.
               uint4* gy = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
                                                    (long long)yrow * sl.y_row_stride + o0 + c16 * 16);
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 if (c16 * 16 + h * 8 >= ovalid) continue;
-                const uint4 yv = gy[h];
+                const uint4 yv = yseg[cc * 4 + g16 * 2 + h];
                 const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
                 uint32_t out[4];
 #pragma unroll
@@ -1332,9 +1352,17 @@ int tc_pack_splits(const ProblemDesc& p) {
   return n;
 }
 
-template <int NR, int CL>
-cudaError_t launch_ksplit_t(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s) {
-  auto kernel = sgmv_tc_shrink_ksplit_kernel<NR, CL>;
+// Ring of a K-split CTA: the full-depth ring (one CTA per SM), or a shallow
+// one that two CTAs per SM hold (~112 KB each).
+template <int NR>
+constexpr int shallow_stages() {
+  return (112 * 1024 - 1024) / TcCfg<NR>::STAGE;
+}
+
+template <int NR, int CL, int NST>
+cudaError_t launch_ksplit_t(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s, int nsn) {
+  auto kernel = sgmv_tc_shrink_ksplit_kernel<NR, CL, NST>;
+  constexpr int SMEM = NST * TcCfg<NR>::STAGE + 1024;
   static unsigned long long done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1342,16 +1370,16 @@ cudaError_t launch_ksplit_t(const ProblemDesc& p, const TcMaps& maps, uint8_t* u
   {
     std::lock_guard<std::mutex> lk(g_tc_mu);
     if (!(done & (1ull << (dev & 63)))) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<NR>::SMEM);
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
       if (e != cudaSuccess) return e;
       done |= 1ull << (dev & 63);
     }
   }
   const long long tiles = (long long)p.G + p.end / TM;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * CL));
+  cfg.gridDim = dim3((unsigned)(tiles * CL * nsn));
   cfg.blockDim = dim3(TTHREADS);
-  cfg.dynamicSmemBytes = TcCfg<NR>::SMEM;
+  cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1362,29 +1390,41 @@ cudaError_t launch_ksplit_t(const ProblemDesc& p, const TcMaps& maps, uint8_t* u
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return noted(cudaLaunchKernelEx(&cfg, kernel, p, maps, upk), LORA_PATH_TC_SHRINK);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, maps, upk, nsn), LORA_PATH_TC_SHRINK);
 }
 
-// The packed shrink with K split over a cluster of `cl` CTAs per tile (all
-// n*R columns per CTA, x read once); cudaErrorNotSupported for other widths.
-cudaError_t launch_ksplit(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s, int cl) {
-  const int nR = p.n_slices * p.R;
-  if (p.in_dim % (cl * TK) != 0) return cudaErrorNotSupported;
+template <int NR, int CL>
+cudaError_t launch_ksplit_nr(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s, int nsn,
+                             bool shallow) {
+  if constexpr (shallow_stages<NR>() >= 2 && (CL - 1) * TM * (NR / CL) * 4 <= shallow_stages<NR>() * TcCfg<NR>::STAGE) {
+    if (shallow) return launch_ksplit_t<NR, CL, shallow_stages<NR>()>(p, maps, upk, s, nsn);
+  }
+  if (shallow) return cudaErrorNotSupported;
+  return launch_ksplit_t<NR, CL, TcCfg<NR>::NSTAGE>(p, maps, upk, s, nsn);
+}
+
+// The packed shrink with K split over a cluster of `cl` CTAs per tile and
+// the n*R columns in `nsn` parts (NR = n*R / nsn per CTA); `shallow` picks
+// the two-CTAs-per-SM ring.  cudaErrorNotSupported for other shapes.
+cudaError_t launch_ksplit(const ProblemDesc& p, const TcMaps& maps, uint8_t* upk, cudaStream_t s, int cl, int nsn,
+                          bool shallow) {
+  const int nR = p.n_slices * p.R / nsn;
+  if (p.in_dim % (cl * TK) != 0 || (p.n_slices * p.R) % nsn != 0) return cudaErrorNotSupported;
   if (cl == 2) {
     switch (nR) {
-      case 64: return launch_ksplit_t<64, 2>(p, maps, upk, s);
-      case 128: return launch_ksplit_t<128, 2>(p, maps, upk, s);
-      case 192: return launch_ksplit_t<192, 2>(p, maps, upk, s);
-      case 256: return launch_ksplit_t<256, 2>(p, maps, upk, s);
-      case 384: return launch_ksplit_t<384, 2>(p, maps, upk, s);
+      case 64: return launch_ksplit_nr<64, 2>(p, maps, upk, s, nsn, shallow);
+      case 128: return launch_ksplit_nr<128, 2>(p, maps, upk, s, nsn, shallow);
+      case 192: return launch_ksplit_nr<192, 2>(p, maps, upk, s, nsn, shallow);
+      case 256: return launch_ksplit_nr<256, 2>(p, maps, upk, s, nsn, shallow);
+      case 384: return launch_ksplit_nr<384, 2>(p, maps, upk, s, nsn, shallow);
     }
   } else if (cl == 4) {
     switch (nR) {
-      case 64: return launch_ksplit_t<64, 4>(p, maps, upk, s);
-      case 128: return launch_ksplit_t<128, 4>(p, maps, upk, s);
-      case 192: return launch_ksplit_t<192, 4>(p, maps, upk, s);
-      case 256: return launch_ksplit_t<256, 4>(p, maps, upk, s);
-      case 384: return launch_ksplit_t<384, 4>(p, maps, upk, s);
+      case 64: return launch_ksplit_nr<64, 4>(p, maps, upk, s, nsn, shallow);
+      case 128: return launch_ksplit_nr<128, 4>(p, maps, upk, s, nsn, shallow);
+      case 192: return launch_ksplit_nr<192, 4>(p, maps, upk, s, nsn, shallow);
+      case 256: return launch_ksplit_nr<256, 4>(p, maps, upk, s, nsn, shallow);
+      case 384: return launch_ksplit_nr<384, 4>(p, maps, upk, s, nsn, shallow);
     }
   }
   return cudaErrorNotSupported;
@@ -1394,12 +1434,18 @@ cudaError_t launch_tc_apply_packed(const ProblemDesc& p, void* workspace, cudaSt
   TcMaps smaps;
   TxMaps xmaps;
   if (!encode_maps(p, &smaps) || !encode_tx_maps(p, &xmaps)) return cudaErrorNotSupported;
-  // Few tiles: split K over a cluster of CTAs per tile (x read once) rather
-  // than the tile's columns (x read once per column part).
+  // Fill the SMs.  Few tiles: split K over a cluster of CTAs per tile (x read
+  // once) rather than the tile's columns (x read once per column part), one
+  // CTA per SM.  Up to two tiles per SM: K split over CTA pairs with shallow
+  // rings, two CTAs per SM.  Otherwise one CTA per tile.
   const int nsn = tc_pack_splits(p);
   uint8_t* upk = static_cast<uint8_t*>(workspace);
   cudaError_t e = cudaErrorNotSupported;
-  if (nsn > 1 && !p.token_rows) e = launch_ksplit(p, smaps, upk, s, nsn);
+  if (!p.token_rows) {
+    const long long tiles_lb = (p.end + TM - 1) / TM;
+    if (nsn > 1) e = launch_ksplit(p, smaps, upk, s, nsn, 1, false);
+    else if (tiles_lb * 2 <= 2LL * device_sm_count()) e = launch_ksplit(p, smaps, upk, s, 2, 1, true);
+  }
   if (e == cudaErrorNotSupported) e = launch_tc_shrink_maps(p, smaps, nullptr, s, 1, nsn, upk);
   if (e != cudaSuccess) return e;
   const TxWork w = make_tx_work(p, 1);

@@ -64,7 +64,7 @@ class _BaseWeight(ctypes.Structure):
 class _Routing(ctypes.Structure):
     _fields_ = [("lora_ids", ctypes.c_void_p), ("grouped_offsets", ctypes.c_void_p),
                 ("num_groups", ctypes.c_int32), ("end", ctypes.c_int32), ("token_rows", ctypes.c_void_p),
-                ("host_grouped_offsets", ctypes.c_void_p)]
+                ("host_grouped_offsets", ctypes.c_void_p), ("host_lora_ids", ctypes.c_void_p)]
 
 
 _lib = None
@@ -182,36 +182,47 @@ def lora_build_token_rows(req_num_tokens, perm, end: int) -> np.ndarray:
 @dataclass
 class Routing:
     """Routing triple: device lora_ids / grouped_offsets tensors, host num_groups / end,
-    optionally device token_rows (row of each sorted token, unsorted batches)
-    and a host copy of grouped_offsets (int32 numpy array) that lets the
-    library pick the kernels per group."""
+    optionally device token_rows (row of each sorted token, unsorted batches),
+    a host copy of grouped_offsets (int32 numpy array) that lets the library
+    pick the kernels per group, and a host copy of lora_ids (with the host
+    offsets: the mma.sync kernels take the triple as launch parameters)."""
     lora_ids: object
     grouped_offsets: object
     num_groups: int
     end: int
     token_rows: object = None
     host_grouped_offsets: object = None
+    host_lora_ids: object = None
 
     def _c(self) -> _Routing:
         ptr = lambda t: t.data_ptr() if t is not None and t.numel() > 0 else None
-        h = self.host_grouped_offsets
-        if h is not None:
-            h = np.ascontiguousarray(h, dtype=np.int32)
-            self._host_keep = h  # the pointer below must outlive the call
+
+        def host(a):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a, dtype=np.int32)
+            self._host_keep.append(a)  # the pointer must outlive the call
+            return a.ctypes.data if a.size > 0 else None
+
+        self._host_keep = []
         return _Routing(ptr(self.lora_ids), ptr(self.grouped_offsets), int(self.num_groups), int(self.end),
-                        ptr(self.token_rows), h.ctypes.data if h is not None and h.size > 0 else None)
+                        ptr(self.token_rows), host(self.host_grouped_offsets), host(self.host_lora_ids))
 
 
-def routing_to_device(r: dict, device="cuda", non_blocking=False, host_offsets=False) -> Routing:
+def routing_to_device(r: dict, device="cuda", non_blocking=False, host_offsets=False,
+                      host_ids=False) -> Routing:
     """Upload the host triple from lora_build_routing (int32 tensors); with
     host_offsets the host copy of grouped_offsets rides along (per-group
-    kernel choice)."""
+    kernel choice), with host_ids also the host copy of lora_ids (the
+    mma.sync kernels then take the triple as launch parameters)."""
     import torch
+    ids_h = np.ascontiguousarray(r["lora_ids"], dtype=np.int32)[: int(r["num_groups"])]
     ids = torch.from_numpy(np.ascontiguousarray(r["lora_ids"], dtype=np.int32))
     offs_h = np.ascontiguousarray(r["grouped_offsets"], dtype=np.int32)
     offs = torch.from_numpy(offs_h)
     return Routing(ids.to(device, non_blocking=non_blocking), offs.to(device, non_blocking=non_blocking),
-                   int(r["num_groups"]), int(r["end"]), None, offs_h.copy() if host_offsets else None)
+                   int(r["num_groups"]), int(r["end"]), None,
+                   offs_h.copy() if host_offsets or host_ids else None, ids_h.copy() if host_ids else None)
 
 
 # --------------------------------------------------------------- problems --

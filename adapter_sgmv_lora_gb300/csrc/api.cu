@@ -106,7 +106,28 @@ lora_status_t validate_routing(const lora_problem_t* p, const lora_routing_t* r)
   if (r->end < 0 || r->end > p->num_tokens) return LORA_ERR_ROUTING;
   if (r->num_groups == 0 && r->end != 0) return LORA_ERR_ROUTING;
   if (r->num_groups > 0 && (!r->lora_ids || !r->grouped_offsets)) return LORA_ERR_NULL;
+  if (r->host_lora_ids && !r->host_grouped_offsets) return LORA_ERR_NULL;
+  if (const int32_t* o = r->host_grouped_offsets) {
+    if (r->num_groups > 0 && o[0] != 0) return LORA_ERR_ROUTING;
+    for (int g = 0; g < r->num_groups; ++g)
+      if (o[g + 1] < o[g]) return LORA_ERR_ROUTING;
+    if (r->num_groups > 0 && o[r->num_groups] != r->end) return LORA_ERR_ROUTING;
+  }
+  if (const int32_t* ids = r->host_lora_ids)
+    for (int g = 0; g < r->num_groups; ++g)
+      if (ids[g] < 0 || ids[g] >= p->max_num_loras) return LORA_ERR_SLOT_RANGE;
   return LORA_OK;
+}
+
+// The launch-parameter summary of a validated routing's host triple (G = 0:
+// no host copy of both arrays).
+HostRouting host_routing(const lora_routing_t* r) {
+  HostRouting h{};
+  if (!r->host_grouped_offsets || !r->host_lora_ids) return h;
+  h.G = r->num_groups;
+  for (int g = 0; g < r->num_groups; ++g)
+    h.digest += routing_digest_term(g, r->host_grouped_offsets[g], r->host_lora_ids[g]);
+  return h;
 }
 
 ProblemDesc make_desc(const lora_problem_t* p, const lora_routing_t* r) {
@@ -296,9 +317,10 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
       cudaError_t e = launch_tc_apply_packed(dl, inter, s);
       if (e != cudaErrorNotSupported) {
         if ((st = cuda_status(e)) != LORA_OK) return st;
-        const int splits = apply_splits_for(ds);
-        if ((st = cuda_status(launch_shrink_partial_bf16(ds, up, s))) != LORA_OK) return st;
-        return cuda_status(launch_expand_bf16(ds, up, s, true, splits));
+        int splits = 1;
+        const HostRouting hr = host_routing(routing);
+        if ((st = cuda_status(launch_shrink_partial_bf16(ds, up, s, routing, &splits))) != LORA_OK) return st;
+        return cuda_status(launch_expand_bf16(ds, up, s, true, splits, &hr));
       }
     }
   }
@@ -315,9 +337,10 @@ extern "C" lora_status_t lora_sgmv_apply(const lora_problem_t* problem, const lo
         return cuda_status(launch_expand_bf16(d, u, s, true, tcs));
       }
     }
-    const int splits = apply_splits_for(d);
-    if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s))) != LORA_OK) return st;
-    return cuda_status(launch_expand_bf16(d, u, s, true, splits));
+    int splits = 1;
+    const HostRouting hr = host_routing(routing);
+    if ((st = cuda_status(launch_shrink_partial_bf16(d, u, s, routing, &splits))) != LORA_OK) return st;
+    return cuda_status(launch_expand_bf16(d, u, s, true, splits, &hr));
   }
   if ((st = cuda_status(launch_shrink_simple(d, u, s))) != LORA_OK) return st;
   return cuda_status(launch_expand_simple(d, u, s, true));

@@ -62,6 +62,38 @@ int device_sm_count();
 // many SMs; launches use the device's own count, which is at most this.
 constexpr int kMaxSmsForWorkspace = 256;
 
+// One group's term of the routing digest: SplitMix64's finalizer (Steele,
+// Lea and Flood, "Fast splittable pseudorandom number generators", 2014)
+// applied to (offset, slot) offset by a Weyl step per group index.  The
+// digest of a triple is the sum of its groups' terms modulo 2^64; the host
+// computes it from its copy, the kernels from the device arrays.
+__host__ __device__ __forceinline__ unsigned long long routing_digest_term(int g, int offset, int slot) {
+  unsigned long long z = ((unsigned long long)(unsigned)slot << 32 | (unsigned)offset) +
+                         (unsigned long long)(g + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// What a launch knows of the routing triple's host copy (G == 0: nothing):
+// the group count and the digest of (grouped_offsets[g], lora_ids[g]) over
+// its groups.  Two uniform kernel parameters, so checking the device triple
+// against the host copy costs each lane its own groups' terms and a warp sum.
+struct HostRouting {
+  int G;
+  unsigned long long digest;
+};
+
+// The tiles of one launch, made on the host from a HostRouting: tile i is
+// t[i] = {first row, slot << 8 | rows}.  A CTA reads its own entry, one
+// address for all its threads (a constant-bank broadcast), so it knows its
+// tile without any global load.  n == 0: none.
+constexpr int kHostTilesMax = 128;
+struct HostTiles {
+  int n;
+  int2 t[kHostTilesMax];
+};
+
 // Token rows per tile of the bf16 SGMV kernels.
 constexpr int kTileRows = 64;
 
@@ -82,16 +114,24 @@ bool fast_path_ok(const ProblemDesc& p, const void* u);
 // launch_shrink_bf16 writes the final u (cluster reduction);
 // launch_shrink_partial_bf16 writes apply_splits(...) partial planes of u,
 // plane c at u + c * end * n * R, which launch_expand_bf16 sums (nsplit).
+// r (optional): a routing whose host copies of the triple were validated.
+// The shrink then takes a table of its tiles made from them (no read of the
+// device triple before its loads).  hr (optional): the expand checks the
+// device triple's digest against the host copy's (a difference:
+// LORA_DEV_BAD_OFFSETS, the launch skips its work).
 cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
-cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s);
-cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit);
+// *splits (if given) receives the partial planes written (the expand's nsplit).
+cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s,
+                                       const lora_routing_t* r = nullptr, int* splits = nullptr);
+cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit,
+                               const HostRouting* hr = nullptr);
 // Upper bound on the partial planes the apply's shrink uses for this shape
 // (1..16); shapes only (it sizes the workspace).
 int apply_splits(int end, int in_dim, int nR);
 // The split the apply's partial-plane shrink actually uses (and its expand
 // sums): from the group count and CTA occupancy, at most apply_splits(...);
 // *short_ring tells whether the shrink runs its 4-stage ring.
-int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr);
+int apply_splits_for(const ProblemDesc& p, bool* short_ring = nullptr, long long exact_tiles = -1);
 
 // The base projection with the delta fused in (sgmv_base.cu).  Per slice,
 // the base weight W0_j [out_j, in] (row stride in elements).

@@ -70,17 +70,13 @@ struct ShrinkCfg {
 template <int NB, bool GEN, int NSO>
 __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                float* __restrict__ u, int C,
-                                                               int nblk, int Kc, long long plane_stride) {
+                                                               int nblk, int Kc, long long plane_stride,
+                                                               const __grid_constant__ HostTiles ht) {
   using Cfg = ShrinkCfg<NB, NSO>;
   constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Tile s_tile;
   __shared__ int s_ok;
-
-  // Launched as a programmatic dependent of whatever kernel precedes it: no
-  // global memory is touched before that kernel has completed.
-  pdl_wait();
-  pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)(blockIdx.x % (unsigned)C);
@@ -88,17 +84,36 @@ __global__ void __launch_bounds__(128) sgmv_shrink_bf16_kernel(const __grid_cons
   const int nb = rest % nblk;
   const long long tile = rest / nblk;
 
-  if (warp == 0) {
-    Tile t{};
-    const bool ok = warp_locate_tile(p, MT, tile, t);
-    if (lane == 0) {
-      s_tile = t;
-      s_ok = ok;
-    }
+  Tile t{};
+  if (ht.n > 0) {
+    // Tiles made on the host: every thread reads its CTA's entry from the
+    // launch parameters, so the first global reads after the wait below are
+    // the x / A stages.
+    if (tile >= ht.n) return;
+    const int2 e = ht.t[tile];
+    t.row0 = e.x;
+    t.slot = e.y >> 8;
+    t.rows = e.y & 0xff;
   }
-  __syncthreads();
-  if (!s_ok) return;  // the whole cluster sees the same tile and the same outcome
-  const Tile t = s_tile;
+
+  // Launched as a programmatic dependent of whatever kernel precedes it: no
+  // global memory is touched before that kernel has completed.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (ht.n == 0) {
+    if (warp == 0) {
+      Tile w{};
+      const bool ok = warp_locate_tile(p, MT, tile, w);
+      if (lane == 0) {
+        s_tile = w;
+        s_ok = ok;
+      }
+    }
+    __syncthreads();
+    if (!s_ok) return;  // the whole cluster sees the same tile and the same outcome
+    t = s_tile;
+  }
 
   const int R = p.R;
   const int nR = p.n_slices * R;
@@ -303,7 +318,7 @@ struct ExpandMap {
 // GEN as for the shrink: token_rows, slot ranks or a bias in use.
 template <int R, int OB, int MR, bool GEN>
 __device__ __forceinline__ void expand_bf16_body(const ProblemDesc& p, const float* __restrict__ u,
-                                                 const ExpandMap& map) {
+                                                 const ExpandMap& map, const HostRouting& hr) {
   using Cfg = ExpandCfg<R, OB, MR>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Tile s_tile;
@@ -321,7 +336,7 @@ __device__ __forceinline__ void expand_bf16_body(const ProblemDesc& p, const flo
 
   if (warp == 0) {
     Tile t{};
-    const bool ok = warp_locate_tile(p, MR, tile, t);
+    const bool ok = warp_locate_tile(p, MR, tile, t, &hr);  // also checks the host copy, if any
     if (lane == 0) {
       s_tile = t;
       s_ok = ok;
@@ -519,16 +534,18 @@ __device__ __forceinline__ void expand_bf16_body(const ProblemDesc& p, const flo
 template <int R, int OB, int MR, bool GEN>
 __global__ void __launch_bounds__(256) sgmv_expand_bf16_kernel(const __grid_constant__ ProblemDesc p,
                                                                const float* __restrict__ u,
-                                                               const __grid_constant__ ExpandMap map) {
-  expand_bf16_body<R, OB, MR, GEN>(p, u, map);
+                                                               const __grid_constant__ ExpandMap map,
+                                                               const __grid_constant__ HostRouting hr) {
+  expand_bf16_body<R, OB, MR, GEN>(p, u, map, hr);
 }
 
 // The plain 32 x 512 rank-16 tile (short groups over wide outputs, grids of
 // several waves) held to 64 registers, so four CTAs share an SM.
 __global__ void __launch_bounds__(256, 4) sgmv_expand_bf16_w4_kernel(const __grid_constant__ ProblemDesc p,
                                                                      const float* __restrict__ u,
-                                                                     const __grid_constant__ ExpandMap map) {
-  expand_bf16_body<16, 512, 32, false>(p, u, map);
+                                                                     const __grid_constant__ ExpandMap map,
+                                                                     const __grid_constant__ HostRouting hr) {
+  expand_bf16_body<16, 512, 32, false>(p, u, map, hr);
 }
 
 // ------------------------------------------------------------------ host
@@ -582,31 +599,36 @@ static int cluster_splits(const ProblemDesc& p, int nblk) {
 }
 
 template <int NB, bool GEN, int NSO>
-cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial);
+cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial,
+                             const HostTiles& ht);
 
 template <int NB, bool GEN>
-cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
+cudaError_t launch_shrink_nb(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial,
+                             const HostTiles& ht) {
   bool short_ring = false;
   if (partial)
-    (void)apply_splits_for(p, &short_ring);
+    (void)apply_splits_for(p, &short_ring, ht.n > 0 ? ht.n : -1);
   else
     short_ring = cluster_splits(p, nblk) == 16;  // smaller CTAs: a 16-CTA cluster packs into a GPC
-  if (short_ring) return launch_shrink_ns<NB, GEN, 4>(p, u, s, nblk, partial);
-  return launch_shrink_ns<NB, GEN, 0>(p, u, s, nblk, partial);
+  if (short_ring) return launch_shrink_ns<NB, GEN, 4>(p, u, s, nblk, partial, ht);
+  return launch_shrink_ns<NB, GEN, 0>(p, u, s, nblk, partial, ht);
 }
 
 template <int NB, bool GEN, int NSO>
-cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial) {
+cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int nblk, bool partial,
+                             const HostTiles& ht) {
   auto kernel = sgmv_shrink_bf16_kernel<NB, GEN, NSO>;
   const int smem = ShrinkCfg<NB, NSO>::SMEM;
   static unsigned long long done = 0;
   cudaError_t e = ensure_smem(kernel, smem, &done);
   if (e != cudaSuccess) return e;
-  const long long tiles = (long long)p.G + p.end / MT;
+  // A tile table gives the exact count; else an upper bound (CTAs past the
+  // last tile return).
+  const long long tiles = ht.n > 0 ? ht.n : (long long)p.G + p.end / MT;
   int C = 1;
   long long plane_stride = 0;
   if (partial) {
-    C = apply_splits_for(p);
+    C = apply_splits_for(p, nullptr, ht.n > 0 ? ht.n : -1);
     if (C > 1) plane_stride = (long long)p.end * p.n_slices * p.R;
   } else {
     C = cluster_splits(p, nblk);
@@ -662,7 +684,7 @@ cudaError_t launch_shrink_ns(const ProblemDesc& p, float* u, cudaStream_t s, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return noted(cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride), LORA_PATH_MMA_SHRINK);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, u, C, nblk, Kc, plane_stride, ht), LORA_PATH_MMA_SHRINK);
 }
 
 // The kernel of an expand tile shape (only the one that runs is instantiated).
@@ -675,7 +697,8 @@ constexpr auto expand_kernel() {
 }
 
 template <int R, int OB, int MR, bool GEN>
-cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
+cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit,
+                            const HostRouting& hr) {
   auto kernel = expand_kernel<R, OB, MR, GEN>();
   const int smem = ExpandCfg<R, OB, MR>::SMEM;
   static unsigned long long done = 0;
@@ -704,7 +727,7 @@ cudaError_t launch_expand_r(const ProblemDesc& p, const float* u, cudaStream_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return noted(cudaLaunchKernelEx(&cfg, kernel, p, u, map), LORA_PATH_MMA_EXPAND);
+  return noted(cudaLaunchKernelEx(&cfg, kernel, p, u, map, hr), LORA_PATH_MMA_EXPAND);
 }
 
 }  // namespace
@@ -725,9 +748,10 @@ bool fast_path_ok(const ProblemDesc& p, const void* u) {
   return true;
 }
 
-int apply_splits_for(const ProblemDesc& p, bool* short_ring) {
-  // At launch the group count is known: size the split on the upper bound
-  // of the tiles (G + end/64) and on how many of these CTAs share an SM, to
+int apply_splits_for(const ProblemDesc& p, bool* short_ring, long long exact_tiles) {
+  // At launch the group count is known: size the split on the tiles (their
+  // count when a host-made table gives it, else the upper bound G + end/64)
+  // and on how many of these CTAs share an SM, to
   // about two waves, never above the shape-only bound the workspace holds.
   // With the 4-stage ring three times as many CTAs share an SM: it is taken
   // when that allows more splits, or when a split is at most 4 stages long.
@@ -742,7 +766,7 @@ int apply_splits_for(const ProblemDesc& p, bool* short_ring) {
     case 64: smem = ShrinkCfg<64>::SMEM; smem4 = ShrinkCfg<64, 4>::SMEM; break;
     case 96: smem = ShrinkCfg<96>::SMEM; smem4 = ShrinkCfg<96, 4>::SMEM; break;
   }
-  const long long tiles = (long long)p.G + p.end / MT;
+  const long long tiles = exact_tiles >= 0 ? exact_tiles : (long long)p.G + p.end / MT;
   const int ksteps = p.in_dim / KS;
   auto pick = [&](int sm_bytes) {
     const long long per_sm = std::max(1, (228 * 1024) / (sm_bytes + 1024));
@@ -792,25 +816,29 @@ static bool needs_general(const ProblemDesc& p) {
 }
 
 template <bool GEN>
-static cudaError_t dispatch_shrink_g(const ProblemDesc& p, float* u, cudaStream_t s, bool partial) {
+static cudaError_t dispatch_shrink_g(const ProblemDesc& p, float* u, cudaStream_t s, bool partial,
+                                     const HostTiles& ht) {
   int nblk = 1;
   const int nb = pick_nb(p.n_slices * p.R, &nblk);
   switch (nb) {
-    case 16: return launch_shrink_nb<16, GEN>(p, u, s, nblk, partial);
-    case 32: return launch_shrink_nb<32, GEN>(p, u, s, nblk, partial);
-    case 48: return launch_shrink_nb<48, GEN>(p, u, s, nblk, partial);
-    case 64: return launch_shrink_nb<64, GEN>(p, u, s, nblk, partial);
-    case 96: return launch_shrink_nb<96, GEN>(p, u, s, nblk, partial);
-    default: return launch_shrink_nb<128, GEN>(p, u, s, nblk, partial);
+    case 16: return launch_shrink_nb<16, GEN>(p, u, s, nblk, partial, ht);
+    case 32: return launch_shrink_nb<32, GEN>(p, u, s, nblk, partial, ht);
+    case 48: return launch_shrink_nb<48, GEN>(p, u, s, nblk, partial, ht);
+    case 64: return launch_shrink_nb<64, GEN>(p, u, s, nblk, partial, ht);
+    case 96: return launch_shrink_nb<96, GEN>(p, u, s, nblk, partial, ht);
+    default: return launch_shrink_nb<128, GEN>(p, u, s, nblk, partial, ht);
   }
 }
 
-static cudaError_t dispatch_shrink(const ProblemDesc& p, float* u, cudaStream_t s, bool partial) {
-  return needs_general(p) ? dispatch_shrink_g<true>(p, u, s, partial) : dispatch_shrink_g<false>(p, u, s, partial);
+static cudaError_t dispatch_shrink(const ProblemDesc& p, float* u, cudaStream_t s, bool partial,
+                                   const HostTiles& ht) {
+  return needs_general(p) ? dispatch_shrink_g<true>(p, u, s, partial, ht)
+                          : dispatch_shrink_g<false>(p, u, s, partial, ht);
 }
 
 template <bool GEN>
-static cudaError_t dispatch_expand_g(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
+static cudaError_t dispatch_expand_g(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit,
+                                     const HostRouting& hr) {
   // Short groups (at most 32 routed rows each on average): 32-row tiles twice
   // as wide, so a tile's fixed costs (routing lookup, u, B block) cover twice
   // the outputs and the grid has half the CTAs -- unless that leaves fewer
@@ -824,27 +852,54 @@ static cudaError_t dispatch_expand_g(const ProblemDesc& p, const float* u, cudaS
         long long blocks = 0;
         for (int j = 0; j < p.n_slices; ++j) blocks += (p.sl[j].out_dim + 511) / 512;
         const long long tiles = (long long)p.G + p.end / 32;
-        return tiles * blocks < 2LL * num_sms() ? launch_expand_r<16, 256, 32, GEN>(p, u, s, pdl, nsplit)
-                                                : launch_expand_r<16, 512, 32, GEN>(p, u, s, pdl, nsplit);
+        return tiles * blocks < 2LL * num_sms() ? launch_expand_r<16, 256, 32, GEN>(p, u, s, pdl, nsplit, hr)
+                                                : launch_expand_r<16, 512, 32, GEN>(p, u, s, pdl, nsplit, hr);
       }
-      return launch_expand_r<16, 256, 64, GEN>(p, u, s, pdl, nsplit);
-    case 32: return launch_expand_r<32, 256, 64, GEN>(p, u, s, pdl, nsplit);
-    case 64: return launch_expand_r<64, 128, 64, GEN>(p, u, s, pdl, nsplit);
-    default: return launch_expand_r<128, 64, 64, GEN>(p, u, s, pdl, nsplit);
+      return launch_expand_r<16, 256, 64, GEN>(p, u, s, pdl, nsplit, hr);
+    case 32: return launch_expand_r<32, 256, 64, GEN>(p, u, s, pdl, nsplit, hr);
+    case 64: return launch_expand_r<64, 128, 64, GEN>(p, u, s, pdl, nsplit, hr);
+    default: return launch_expand_r<128, 64, 64, GEN>(p, u, s, pdl, nsplit, hr);
   }
 }
 
+// The shrink's MT-row tiles of the groups the launch works on (lengths in
+// [seg_lo, seg_hi)), numbered as warp_locate_tile numbers them, from the
+// routing's (validated) host copies.  n = 0 when there are none or the tiles
+// do not fit the table.
+static HostTiles make_host_tiles(const ProblemDesc& p, const lora_routing_t* r) {
+  HostTiles ht{};
+  if (!r || !r->host_grouped_offsets || !r->host_lora_ids || r->num_groups <= 0 || p.S > (1 << 22)) return ht;
+  const int32_t* offs = r->host_grouped_offsets;
+  int n = 0;
+  for (int g = 0; g < r->num_groups; ++g) {
+    const int o0 = offs[g], o1 = offs[g + 1];
+    const int len = o1 - o0;
+    if (len <= 0 || len < p.seg_lo || len >= p.seg_hi) continue;
+    for (int row = o0; row < o1; row += MT) {
+      if (n == kHostTilesMax) return HostTiles{};
+      ht.t[n++] = make_int2(row, (r->host_lora_ids[g] << 8) | std::min(MT, o1 - row));
+    }
+  }
+  ht.n = n;
+  return ht;
+}
+
 cudaError_t launch_shrink_bf16(const ProblemDesc& p, float* u, cudaStream_t s) {
-  return dispatch_shrink(p, u, s, false);
+  return dispatch_shrink(p, u, s, false, HostTiles{});
 }
 
-cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s) {
-  return dispatch_shrink(p, u, s, true);
+cudaError_t launch_shrink_partial_bf16(const ProblemDesc& p, float* u, cudaStream_t s, const lora_routing_t* r,
+                                       int* splits) {
+  const HostTiles ht = make_host_tiles(p, r);
+  if (splits) *splits = apply_splits_for(p, nullptr, ht.n > 0 ? ht.n : -1);  // what the launch below takes
+  return dispatch_shrink(p, u, s, true, ht);
 }
 
-cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit) {
-  return needs_general(p) ? dispatch_expand_g<true>(p, u, s, pdl, nsplit)
-                          : dispatch_expand_g<false>(p, u, s, pdl, nsplit);
+cudaError_t launch_expand_bf16(const ProblemDesc& p, const float* u, cudaStream_t s, bool pdl, int nsplit,
+                               const HostRouting* hr) {
+  const HostRouting h = hr ? *hr : HostRouting{};
+  return needs_general(p) ? dispatch_expand_g<true>(p, u, s, pdl, nsplit, h)
+                          : dispatch_expand_g<false>(p, u, s, pdl, nsplit, h);
 }
 
 }  // namespace lora

@@ -804,8 +804,10 @@ __device__ __forceinline__ Unit tx_unit(const TxWork& w, int n_slices, long long
 // PACKED: u arrives packed (the tcgen05 shrink's image per (tile, slice),
 // see pack_u16) and warp 0 copies each segment's image into its u buffer;
 // otherwise u is fp32 [end, n*R] (nsplit planes) and the epilogue warps
-// convert it.
-template <int R, bool PACKED>
+// convert it.  GATHER: the batch has token_rows (the epilogue reads and
+// writes its scattered y rows itself); the sorted instantiation compiles
+// none of that.
+template <int R, bool PACKED, bool GATHER>
 __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __grid_constant__ ProblemDesc p,
                                                                     const __grid_constant__ TxMaps maps,
                                                                     const __grid_constant__ TxWork w,
@@ -1048,7 +1050,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       };
 
       const uint64_t pol_stream = policy_evict_first();
-      const bool gathered = p.token_rows != nullptr;
+      constexpr bool gathered = GATHER;
       int cur_tile = -1, cur_j = -1, seg = -1, kmax = 0;
       int yrow = 0;            // gathered: the y row of this thread's tile position
       bool tile_skip = false;  // gathered: the tile has an out-of-range entry
@@ -1063,7 +1065,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
           // prefetch the next segment's into the freed one.
           if (x.tile != cur_tile) {
             t = rc_tile(rc, G, x.tile);
-            if (gathered) {  // every warp checks the whole tile: the same outcome everywhere
+            if constexpr (gathered) {  // every warp checks the whole tile: the same outcome everywhere
               int badrow = 0;
               for (int r = lane; r < t.rows; r += 32) {
                 const int v = p.token_rows[t.row0 + r];
@@ -1118,9 +1120,10 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         uint8_t* ys = slots + slot * Cfg::SLOT;
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
-        // 32 columns per TMEM load: two 16-column groups.
+        // 32 columns per TMEM load: two 16-column groups.  Gathered: unrolled,
+        // so yseg is indexed with constants (kept in registers).
         const bool work = !bad && !tile_skip;
-#pragma unroll
+#pragma unroll(GATHER ? XB / (32 * XNH) : 1)
         for (int cc = 0; cc < XB / (32 * XNH); ++cc) {
           if (!work) break;
           const int c32 = hf * (XB / (32 * XNH)) + cc;
@@ -1261,10 +1264,10 @@ bool encode_tx_maps(const ProblemDesc& p, TxMaps* m) {
   return true;
 }
 
-template <int R, bool PACKED>
-cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& w, const float* u,
+template <int R, bool PACKED, bool GATHER>
+cudaError_t launch_tx_g(const ProblemDesc& p, const TxMaps& maps, const TxWork& w, const float* u,
                         const uint8_t* upk, cudaStream_t s, bool pdl) {
-  auto kernel = sgmv_tc_expand_kernel<R, PACKED>;
+  auto kernel = sgmv_tc_expand_kernel<R, PACKED, GATHER>;
   static unsigned long long done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1295,6 +1298,13 @@ cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& 
     cfg.numAttrs = 1;
   }
   return noted(cudaLaunchKernelEx(&cfg, kernel, p, maps, w, u, upk), LORA_PATH_TC_EXPAND);
+}
+
+template <int R, bool PACKED>
+cudaError_t launch_tx_t(const ProblemDesc& p, const TxMaps& maps, const TxWork& w, const float* u,
+                        const uint8_t* upk, cudaStream_t s, bool pdl) {
+  return p.token_rows ? launch_tx_g<R, PACKED, true>(p, maps, w, u, upk, s, pdl)
+                      : launch_tx_g<R, PACKED, false>(p, maps, w, u, upk, s, pdl);
 }
 
 TxWork make_tx_work(const ProblemDesc& p, int nsplit) {

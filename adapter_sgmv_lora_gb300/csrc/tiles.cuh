@@ -30,9 +30,11 @@ __device__ __forceinline__ unsigned warp_or(unsigned v) {
 
 // Executed by one full warp.  Returns true on every lane iff the routing is
 // valid and `tile` exists; `out` is then valid on every lane.  Records
-// LORA_DEV_* flags in p.status on a violation.
+// LORA_DEV_* flags in p.status on a violation.  With what the launch knows of
+// a host copy of the triple (hr, G > 0) the device triple's digest must also
+// equal the host copy's (else LORA_DEV_BAD_OFFSETS).
 __device__ __forceinline__ bool warp_locate_tile(const ProblemDesc& p, int tile_rows, long long tile,
-                                                 Tile& out) {
+                                                 Tile& out, const HostRouting* hr = nullptr) {
   const int lane = threadIdx.x & 31;
   unsigned bad = 0;
   if (lane == 0) {
@@ -42,6 +44,7 @@ __device__ __forceinline__ bool warp_locate_tile(const ProblemDesc& p, int tile_
   long long base = 0;
   int found_lane_data[4] = {0, 0, 0, 0};
   bool found = false;
+  unsigned long long digest = 0;
   for (int c = 0; c < p.G; c += 32) {
     const int g = c + lane;
     long long nt = 0;
@@ -51,6 +54,9 @@ __device__ __forceinline__ bool warp_locate_tile(const ProblemDesc& p, int tile_
       o1 = p.offs[g + 1];
       id = p.lora_ids[g];
       if (o1 < o0) bad |= LORA_DEV_BAD_OFFSETS;
+      // offs[G] is checked against end on both sides, so offsets 0..G-1
+      // and the slots decide equality
+      if (hr && hr->G > 0) digest += routing_digest_term(g, o0, id);
       if (id < 0 || id >= p.S) bad |= LORA_DEV_BAD_SLOT;
       const long long len = (long long)o1 - (long long)o0;
       nt = (len > 0 && len >= p.seg_lo && len < p.seg_hi) ? (len + tile_rows - 1) / tile_rows : 0;
@@ -71,6 +77,11 @@ __device__ __forceinline__ bool warp_locate_tile(const ProblemDesc& p, int tile_
       found = true;
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (hr && hr->G > 0) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) digest += __shfl_xor_sync(0xffffffffu, digest, d);
+    if (hr->G != p.G || digest != hr->digest) bad |= LORA_DEV_BAD_OFFSETS;
   }
   bad = warp_or(bad);
   if (bad) {

@@ -373,7 +373,7 @@ class WorkloadBench:
                           requests=(sets[0]["raw"]["req_slot"], sets[0]["raw"]["req_len"]) if share else None)
             shared = (sets[0]["p0"]["route_host"], sets[0]["p0"]["routing"]) if share else None
             d0 = device.prepare(raw, self.P0, fused=spec.fused_qkv, slot_ranks=args.slot_ranks,
-                                shared_routing=shared, host_offsets=args.per_group)
+                                shared_routing=shared, host_ids=args.routing == "host")
             d1 = device.prepare(raw, self.P1, slot_ranks=args.slot_ranks,
                                 shared_routing=(d0["route_host"], d0["routing"]))
             b0 = algorithmic_bytes(d0["route_host"], raw, self.P0, slot_ranks=args.slot_ranks)
@@ -511,7 +511,8 @@ def unsorted_block(wb, sampler, peaks):
         rows = lk.lora_build_token_rows(raw["req_len"], rt["perm"], rt["end"])
         tr = torch.from_numpy(rows).to("cuda")
         s["_token_rows"] = tr
-        calls.append(lk.CallBuilder(d["problem"], lk.Routing(r.lora_ids, r.grouped_offsets, r.num_groups, r.end, tr),
+        calls.append(lk.CallBuilder(d["problem"], lk.Routing(r.lora_ids, r.grouped_offsets, r.num_groups, r.end, tr,
+                                                             r.host_grouped_offsets, r.host_lora_ids),
                                     d["workspace"]))
     with torch.cuda.stream(wb.stream):
         calls[0].apply(wb.stream)
@@ -525,10 +526,10 @@ def unsorted_block(wb, sampler, peaks):
                     "read and written in place by the expand"}
 
 
-def one_path_block(wb, sampler, peaks):
-    """The first problem's apply without the routing's host offsets (one
-    kernel family for the whole call, chosen from the average group length),
-    for comparison with the per-group choice."""
+def device_routing_block(wb, sampler, peaks):
+    """The first problem's apply with the routing's device arrays only (no
+    host copies: no tile table for the mma.sync shrink, one kernel family for
+    the whole call), for comparison with the default host-copy routing."""
     lk = wb.lk
     calls = []
     for s in wb.sets:
@@ -543,7 +544,7 @@ def one_path_block(wb, sampler, peaks):
     t = statistics.median(wb.trials(g, wb.NS, sampler=sampler))
     rb = roofline_block(wb, [t], *peaks, traffic=None)
     return {"avg_apply_us": rb["avg_launch_us"], "frac": rb["frac"], "kernel_path": hex(calls[0].last_path),
-            "note": "routing without host_grouped_offsets: one kernel family for the whole call"}
+            "note": "routing without host copies (device lora_ids / grouped_offsets only)"}
 
 
 def workload_summary(wb, sampler, peaks):
@@ -718,8 +719,8 @@ def run_ours(args):
 
     # ---- roofline and per-projection figures of the main workload
     main = workload_summary(wb, sampler, peaks)
-    if args.per_group:
-        main["one_path"] = one_path_block(wb, sampler, peaks)
+    if args.routing == "host":
+        main["device_routing"] = device_routing_block(wb, sampler, peaks)
     (ms,), (tokens,) = reduce_across_ranks([ms], [tokens], dist, "cuda")
 
     # ---- e2e through the public API with host buffers
@@ -733,6 +734,8 @@ def run_ours(args):
                 continue
             sb = WorkloadBench(name, args, rank, lk, torch, stream, l2)
             secondary[name] = workload_summary(sb, sampler, peaks)
+            if args.routing == "host":
+                secondary[name]["device_routing"] = device_routing_block(sb, sampler, peaks)
             if name == "prefill8b":
                 secondary[name]["unsorted"] = unsorted_block(sb, sampler, peaks)
             if not args.no_base_fused:
@@ -748,7 +751,9 @@ def run_ours(args):
     cfg = {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload], "input_sets": NS,
            "footprint_MB": round(wb.foot / 1e6, 1), "l2_MB": round(l2 / 2 ** 20, 1),
            "l2_policy": "inputs larger than L2: %d rotated input sets, %.0f MB > 4x L2" % (NS, wb.foot / 1e6),
-           "routing": "one batch: the input sets are its layers (own x, y, A/B each) sharing one routing triple",
+           "routing": "one batch: the input sets are its layers (own x, y, A/B each) sharing one routing triple"
+                      + ("; the routing carries host copies of grouped_offsets and lora_ids" if args.routing == "host"
+                         else "; device arrays only"),
            "parallelism": "replicas" if world > 1 else "single GPU",
            "slot_ranks": "true ranks passed (A/B bytes counted at ceil16(rank))" if args.slot_ranks
            else "padded to max_lora_rank",
@@ -768,7 +773,7 @@ def run_ours(args):
                         "note": "5 trials of >= 30 ms of the same steps, for comparison with the K-step region"},
         "warm_l2": main["warm_l2"],
         "kernel_paths": main["kernel_paths"],
-        "one_path": main.get("one_path"),
+        "device_routing": main.get("device_routing"),
         "secondary": secondary,
         "e2e": e2e,
         "gpu_launches": wb.launches_per_step * args.steps,
@@ -842,9 +847,10 @@ def run_e2e(args, sets, lk, torch, stream, dist):
             prob = d["problem"]
             slices = [dataclasses.replace(sl, y=y_v) for sl in prob.slices]
             prob_v = dataclasses.replace(prob, x=x_v, slices=slices)
-            # with --per-group the host copy of the offsets is the pinned buffer the routing build writes
+            # the host copies are the pinned buffer the step's routing build writes
+            hc = args.routing == "host"
             routing_v = lk.Routing(ids_d, offs_d, d["routing"].num_groups, d["routing"].end, None,
-                                   h["offs_np"] if args.per_group else None)
+                                   h["offs_np"] if hc else None, h["ids_np"] if hc else None)
             h["calls"].append(lk.CallBuilder(prob_v, routing_v, d["workspace"]))
         host.append(h)
 
@@ -916,8 +922,10 @@ def main():
     ap.add_argument("--slot-ranks", action="store_true",
                     help="pass the adapters' true ranks so the kernels skip the rank padding")
     ap.add_argument("--cpu-budget", type=float, default=16.0)
-    ap.add_argument("--per-group", action="store_true",
-                    help="give the routing its host offsets: kernels picked per group (long groups on tcgen05)")
+    ap.add_argument("--routing", default="host", choices=["host", "device"],
+                    help="host: the routing carries host copies of grouped_offsets and lora_ids (as built by "
+                         "lora_build_routing; kernels picked per group in mixed batches, a tile table for the "
+                         "mma.sync shrink); device: the device arrays only")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

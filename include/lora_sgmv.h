@@ -154,16 +154,32 @@ typedef struct {
    * section 6, whose kernels walk tokens sorted by adapter).  NULL: row i is
    * row i (the sorted batch of the MAX page).  Entries must be distinct and in
    * [0, num_tokens); an entry outside that range makes the launch skip the
-   * tiles containing it and raises LORA_DEV_BAD_ROW.  Gathered batches do not
-   * use the tcgen05 kernels. */
+   * tiles containing it and raises LORA_DEV_BAD_ROW.  Long gathered groups
+   * run on the tcgen05 kernels too (x rows gathered with 16-byte copies, y
+   * rows read and written in place); lora_base_gemm_apply refuses token_rows. */
   const int32_t* token_rows;
   /* Optional HOST int32 [num_groups + 1]: the same values as
    * grouped_offsets, read by the call itself (not by the kernels).  With it
    * lora_sgmv_apply picks the kernels per group: groups of at least
    * LORA_TC_MIN_ROWS routed rows on the tensor-core (tcgen05) kernels, the
    * others on the mma.sync kernels, both in the same call.  NULL: one choice
-   * per call, from the average group length (end / num_groups). */
+   * per call, from the average group length (end / num_groups).  When given
+   * it is checked on the host (entry 0 is 0, entries non-decreasing, entry
+   * num_groups equals end; else LORA_ERR_ROUTING). */
   const int32_t* host_grouped_offsets;
+  /* Optional HOST int32 [num_groups]: the same values as lora_ids; used only
+   * together with host_grouped_offsets (alone: LORA_ERR_NULL), each entry in
+   * [0, max_num_loras) (else LORA_ERR_SLOT_RANGE).  With both host copies,
+   * lora_sgmv_apply gives its mma.sync shrink a table of its tiles (up to
+   * 128 tiles of 64 rows) as a launch parameter: each CTA knows its slot and
+   * rows without reading the device triple.  The expand still reads the
+   * device triple and checks it against a 64-bit digest of the host copies
+   * (SplitMix64 terms per group, summed): a difference raises
+   * LORA_DEV_BAD_OFFSETS and the expand skips its work, leaving y as it was
+   * (a difference that leaves the digest unchanged goes unseen; for unequal
+   * triples that is a chance of about 2^-64).  A CUDA graph that captures the
+   * call replays the captured copies: recapture after changing the triple. */
+  const int32_t* host_lora_ids;
 } lora_routing_t;
 
 /* Routed rows from which a group counts as long (tcgen05 tiles) when the

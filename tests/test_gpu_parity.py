@@ -97,7 +97,7 @@ TC_MMA = 0x10 | 0x8    # tcgen05 shrink, mma.sync expand
 
 
 def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=False, seed=0,
-             slot_ranks=False, poison=False, path=None, parallel=False, host_offsets=False):
+             slot_ranks=False, poison=False, path=None, parallel=False, host_offsets=False, host_ids=False):
     """Prepare on the device, run, compare with the oracle.  Returns the device dict.
 
     path: the exact OR of kernel-family bits the call(s) must have launched
@@ -106,7 +106,7 @@ def run_case(raw, proj="qkv", fused=True, mode="apply", rows="all", separate_y=F
     shared out over the host's cores; for full-size workloads)."""
     lk, device = _lk(), _dev()
     dev = device.prepare(raw, proj, fused=fused, separate_y=separate_y, slot_ranks=slot_ranks,
-                         host_offsets=host_offsets)
+                         host_offsets=host_offsets, host_ids=host_ids)
     ref = oracle.prepare_problem(raw, proj, fused=fused)
     dt = raw["dtype"]
     # routing: library == oracle, bit-exact
@@ -263,10 +263,11 @@ def test_mlp_long_groups_tensor_core_path(mode):
     run_case(sy.draw(spec, 10), "down", mode=mode, path=TC)
 
 
-def run_unsorted(raw, proj="qkv", mode="apply", path=None, parallel=False):
+def run_unsorted(raw, proj="qkv", mode="apply", path=None, parallel=False, host_ids=False):
     """x and y rows in ARRIVAL order; token_rows maps the sorted order to rows.
     Compared with the per-token oracle (slot of each row, no routing triple).
-    path: the exact kernel families the call(s) must take (None: no check)."""
+    path: the exact kernel families the call(s) must take (None: no check).
+    host_ids: the routing carries host copies of the offsets and slot ids."""
     lk, device = _lk(), _dev()
     dev = device.prepare(raw, proj)
     rt = dev["route_host"]
@@ -274,6 +275,9 @@ def run_unsorted(raw, proj="qkv", mode="apply", path=None, parallel=False):
     assert np.array_equal(rows, oracle.token_rows(raw["req_len"], rt["perm"], rt["end"]))
     tr = torch.from_numpy(rows).cuda() if rt["end"] > 0 else None
     routing = lk.Routing(dev["routing"].lora_ids, dev["routing"].grouped_offsets, rt["num_groups"], rt["end"], tr)
+    if host_ids:
+        routing.host_grouped_offsets = np.asarray(rt["grouped_offsets"], dtype=np.int32)
+        routing.host_lora_ids = np.asarray(rt["lora_ids"], dtype=np.int32)[: rt["num_groups"]]
     y_before = device.y_host(dev)
     if mode == "apply":
         lk.lora_sgmv_apply(dev["problem"], routing, dev["workspace"])
@@ -612,6 +616,56 @@ def test_invalid_device_routing_is_flagged_and_skipped(bad):
     assert lk.lora_get_device_status() & flag
     assert np.array_equal(_bits(device.y_host(dev)), _bits(before))
     assert lk.lora_get_device_status() == 0  # read-and-clear
+
+
+# ------------------------- the triple's host copy as launch parameters --
+
+@pytest.mark.parametrize("proj", ["qkv", "o"])
+def test_decode8b_host_triple(proj):
+    """With host copies of the offsets and the slot ids the mma.sync shrink
+    locates its tiles from its launch parameters; same results."""
+    run_case(sy.draw("decode8b", 5), proj, mode="apply", path=MMA, host_ids=True)
+
+
+def test_host_triple_64_groups_unfused_ranks_bias():
+    """64 groups (the most a launch carries), per-projection stacks; and a
+    bias with true ranks (general kernels)."""
+    run_case(sy.draw("many64", 6), "qkv", fused=False, mode="apply", path=MMA, host_ids=True)
+    raw = sy.add_bias(sy.emphasize_delta(sy.draw("decode8b", 43), 40.0), 43, scale=1.0)
+    run_case(raw, "qkv", mode="apply", slot_ranks=True, poison=True, path=MMA, host_ids=True)
+
+
+def test_host_triple_unsorted_and_per_group():
+    run_unsorted(sy.draw("decode8b", 7), "qkv", "apply", path=MMA, host_ids=True)
+    run_case(sy.draw("mixed64", 2), "o", mode="apply", path=SPLIT, parallel=True, host_ids=True)
+
+
+@pytest.mark.parametrize("what", ["ids", "offsets"])
+def test_device_triple_differing_from_host_copy_is_flagged(what):
+    """The shrink works from the host copy; the expand compares the device
+    triple with it, and on a difference flags LORA_DEV_BAD_OFFSETS and skips
+    its work: y keeps its old contents."""
+    lk, device = _lk(), _dev()
+    raw = sy.draw("decode8b", 8)
+    dev = device.prepare(raw, "qkv", host_ids=True)
+    rt = dev["route_host"]
+    r = dev["routing"]
+    ids = np.asarray(rt["lora_ids"], dtype=np.int32).copy()
+    offs = np.asarray(rt["grouped_offsets"], dtype=np.int32).copy()
+    if what == "ids":
+        ids[0] = (ids[0] + 1) % raw["max_num_loras"]          # still a valid slot
+    else:
+        assert offs[2] > offs[1] + 1
+        offs[1] += 1                                          # still a valid triple
+    assert not (np.array_equal(ids, rt["lora_ids"]) and np.array_equal(offs, rt["grouped_offsets"]))
+    bad = lk.Routing(torch.from_numpy(ids).cuda(), torch.from_numpy(offs).cuda(), r.num_groups, r.end,
+                     None, r.host_grouped_offsets, r.host_lora_ids)
+    assert lk.lora_get_device_status() == 0
+    before = device.y_host(dev)
+    lk.lora_sgmv_apply(dev["problem"], bad, dev["workspace"])
+    assert lk.lora_last_call_path()[0] == MMA
+    assert lk.lora_get_device_status() & lk.DEV_BAD_OFFSETS
+    assert np.array_equal(_bits(device.y_host(dev)), _bits(before))
 
 
 def test_workspace_too_small_is_rejected():

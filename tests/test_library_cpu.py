@@ -158,6 +158,26 @@ def test_host_validation_without_gpu():
     assert L.lora_sgmv_apply(ctypes.byref(prob), ctypes.byref(rr), None, 0, None) == 0
     rr.num_groups, rr.end, rr.lora_ids, rr.grouped_offsets = 1, 4, 16, 16
     assert L.lora_sgmv_apply(ctypes.byref(prob), ctypes.byref(rr), None, 0, None) == 8
+    # host copies of the triple are checked on the host: offsets must start
+    # at 0, not decrease and end at `end`; ids must name slots; the ids need
+    # the offsets
+    rr.num_groups, rr.end = 2, 4
+    ids_ok = np.array([1, 0], dtype=np.int32)
+    for offs, ids, code in [([0, 2, 4], None, 8),          # valid: reaches the workspace check
+                            ([1, 2, 4], None, 5),          # first offset not 0
+                            ([0, 3, 2], None, 5),          # decreasing
+                            ([0, 2, 3], None, 5),          # last offset != end
+                            ([0, 2, 4], ids_ok, 8),        # valid pair
+                            ([0, 2, 4], [0, 2], 4),        # slot 2 of 2
+                            ([0, 2, 4], [-1, 0], 4),
+                            (None, ids_ok, 1)]:            # ids without offsets
+        oh = None if offs is None else np.asarray(offs, dtype=np.int32)
+        ih = None if ids is None else np.asarray(ids, dtype=np.int32)
+        rr.host_grouped_offsets = None if oh is None else oh.ctypes.data
+        rr.host_lora_ids = None if ih is None else ih.ctypes.data
+        assert L.lora_sgmv_apply(ctypes.byref(prob), ctypes.byref(rr), None, 0, None) == code, (offs, ids)
+    rr.host_grouped_offsets = rr.host_lora_ids = None
+    rr.num_groups, rr.end = 1, 4
     prob.slices[0].A_slot_stride = 10     # slot blocks overlap
     assert L.lora_shrink(ctypes.byref(prob), ctypes.byref(rr), 16, None) == 2
     prob.slices[0].A_slot_stride = 16 * 64

@@ -33,7 +33,8 @@ def torch_to_storage(t: torch.Tensor, dtype: str) -> np.ndarray:
 
 
 def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y: bool = False,
-            slot_ranks: bool = False, shared_routing=None, host_offsets: bool = False) -> dict:
+            slot_ranks: bool = False, shared_routing=None, host_offsets: bool = False,
+            host_ids: bool = False) -> dict:
     """Build one projection problem ("qkv", "o", "gateup" or "down") on the device.
 
     fused=True: one fused stack A [S, n*R, in], B [S, O, R] and y [T, O].
@@ -44,7 +45,9 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
     passes the slots' true ranks so the kernels skip the padding.
     shared_routing=(route_host, routing) reuses another problem's routing (the
     same batch): no new triple is built or uploaded.  host_offsets=True gives
-    the routing its host copy of grouped_offsets (kernels picked per group).
+    the routing its host copy of grouped_offsets (kernels picked per group);
+    host_ids=True adds the host copy of lora_ids too (the mma.sync kernels
+    take the whole triple as launch parameters).
     """
     dt = raw["dtype"]
     tdt = _TORCH_DT[dt]
@@ -100,7 +103,7 @@ def prepare(raw: dict, proj: str, fused: bool = True, device="cuda", separate_y:
                 lk.lora_set_slot_bias(prob, j, s, bias_raw)
     if shared_routing is None:
         rt = lk.lora_build_routing(raw["req_slot"], raw["req_len"], S)
-        routing = lk.routing_to_device(rt, device, host_offsets=host_offsets)
+        routing = lk.routing_to_device(rt, device, host_offsets=host_offsets, host_ids=host_ids)
     else:
         rt, routing = shared_routing
     ws = lk.new_workspace(prob, rt["end"], device=device)

@@ -730,19 +730,30 @@ constexpr int XB = 128;         // output columns per unit (MMA N)
 constexpr int XEPI = 8;         // epilogue warps: XEPI / 4 per TMEM lane quarter
 constexpr int XNH = XEPI / 4;   // ... each taking XB / XNH columns of a unit
 constexpr int XTHREADS = 32 * (2 + XEPI);
-constexpr int RC_MAX_G = 256;   // groups cached in shared memory
+constexpr int RC_MAX_G = 128;   // groups cached in shared memory
 
+// Shared memory of the expand: one u buffer, a ring of y tiles and a ring of
+// B blocks.  The rings are separate because their slots live for different
+// spans: a B block is free once the unit's MMAs complete, a y tile only once
+// the epilogue has stored it.  The y ring (the HBM stream) gets the depth
+// first -- more y loads in flight per SM is what the expand's time follows
+// (a third y/B slot took the R = 64 fused-qkv apply from 108 to 98.6 us) --
+// then the B ring whatever is left.  A second u buffer measured no faster
+// than one.
 template <int R>
 struct TxCfg {
   static constexpr int KB = 2 * R / 64;                 // 64-wide K blocks of the hi|lo operand
   static constexpr int U_BYTES = KB * TM * 128;         // A operand (u hi|lo) of one segment
   static constexpr int Y_BYTES = (XB / 64) * TM * 128;  // 64-column y boxes
   static constexpr int B_BYTES = (R / 64) * XB * 128;   // R/64 boxes of XB rows x 64
-  static constexpr int SLOT = Y_BYTES + B_BYTES;
-  static constexpr int BUDGET = 212 * 1024;             // dynamic smem (static arrays use the rest)
-  static constexpr int NUB = (2 * U_BYTES + 3 * SLOT + 1024 <= BUDGET) ? 2 : 1;   // u buffers
-  static constexpr int NSLOT = (NUB * U_BYTES + 3 * SLOT + 1024 <= BUDGET) ? 3 : 2;  // y/B depth
-  static constexpr int SMEM = NUB * U_BYTES + NSLOT * SLOT + 1024;
+  // Dynamic shared memory, the 1 KB alignment slack included; with the
+  // static arrays (about 1.7 KB) within the 227 KB a CTA may hold.
+  static constexpr int BUDGET = 225 * 1024;
+  static constexpr int NUB = 1;
+  static constexpr int fits(int ny, int nb) { return U_BYTES + ny * Y_BYTES + nb * B_BYTES + 1024 <= BUDGET; }
+  static constexpr int NYS = fits(4, 2) ? 4 : (fits(3, 2) ? 3 : 2);  // y ring depth
+  static constexpr int NBS = fits(NYS, 4) && NYS >= 4 ? 4 : (fits(NYS, 3) && NYS >= 3 ? 3 : 2);  // B ring
+  static constexpr int SMEM = NUB * U_BYTES + NYS * Y_BYTES + NBS * B_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * XB;
   static_assert(SMEM <= BUDGET, "expand pipeline exceeds shared memory");
 };
@@ -814,16 +825,18 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
                                                                     const float* __restrict__ u,
                                                                     const uint8_t* __restrict__ upk) {
   using Cfg = TxCfg<R>;
-  constexpr int NSLOT = Cfg::NSLOT, NUB = Cfg::NUB;
+  constexpr int NYS = Cfg::NYS, NBS = Cfg::NBS, NUB = Cfg::NUB;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], tfull[2], tempty[2], uready[NUB], ufree[NUB];
+  __shared__ __align__(8) uint64_t yfull[NYS], yempty[NYS], bfull[NBS], bempty[NBS], tfull[2], tempty[2],
+      uready[NUB], ufree[NUB];
   __shared__ uint32_t s_tmem;
   __shared__ RouteCache rc;
   __shared__ int s_ok, s_fail;
   __shared__ long long s_u0, s_u1;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* slots = smem + NUB * Cfg::U_BYTES;
+  uint8_t* yring = smem + NUB * Cfg::U_BYTES;
+  uint8_t* bring = yring + NYS * Cfg::Y_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
 
@@ -859,9 +872,13 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       s_u1 = units * (blockIdx.x + 1) / gridDim.x;
       s_ok = valid;
       s_fail = 0;
-      for (int i = 0; i < NSLOT; ++i) {
-        mbar_init(&full[i], 1);
-        mbar_init(&empty[i], XEPI);
+      for (int i = 0; i < NYS; ++i) {
+        mbar_init(&yfull[i], 1);
+        mbar_init(&yempty[i], XEPI);
+      }
+      for (int i = 0; i < NBS; ++i) {
+        mbar_init(&bfull[i], 1);
+        mbar_init(&bempty[i], 1);
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull[i], 1);
@@ -886,44 +903,62 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
   const long long u0 = s_u0, u1 = s_u1;
 
   if (ok && warp == 0 && lane == 0) {
-    // ---- producer: y and B of unit i into slot i % NSLOT (independent of
-    // the shrink, so the first slots are filled before the dependency wait);
-    // with PACKED also each segment's u image into buffer seg % NUB.
+    // ---- producer: unit i's y tile into y slot i % NYS and its B block
+    // into B slot i % NBS (independent of the shrink, so the first slots
+    // are filled before the dependency wait); with PACKED also each
+    // segment's u image into buffer seg % NUB.
     const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
-    int cur = -1, nbbox = 0;
-    Tile t{};
-    auto issue_yb = [&](int i, const Unit& x) {
-      if (x.tile != cur) {
-        cur = x.tile;
-        t = rc_tile(rc, G, x.tile);
-        nbbox = (slot_kmax(p, t.slot) + 63) / 64;
+    int ycur = -1, bcur = -1, nbbox = 0;
+    Tile yt{}, bt{};
+    auto issue_y = [&](int i, const Unit& x) {
+      if (x.tile != ycur) {
+        ycur = x.tile;
+        yt = rc_tile(rc, G, x.tile);
       }
-      const int slot = i % NSLOT;
-      uint8_t* ys = slots + slot * Cfg::SLOT;
-      uint8_t* bs = ys + Cfg::Y_BYTES;
+      uint64_t* bar = &yfull[i % NYS];
+      uint8_t* ys = yring + (i % NYS) * Cfg::Y_BYTES;
       // Gathered batches: the epilogue reads its y rows itself (scattered).
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)((p.token_rows ? 0 : Cfg::Y_BYTES) + nbbox * XB * 128));
-      if (!p.token_rows)
+      mbar_arrive_expect_tx(bar, GATHER ? 0u : (uint32_t)Cfg::Y_BYTES);
+      if (!GATHER)
         for (int yb = 0; yb < XB / 64; ++yb)
-          tma_load_2d_hint(ys + yb * TM * 128, &maps.y[x.j], x.o0 + yb * 64, t.row0, &full[slot], pol_stream);
-      for (int kb = 0; kb < nbbox; ++kb)
-        tma_load_3d_hint(bs + kb * XB * 128, &maps.b[x.j], kb * 64, x.o0, t.slot, &full[slot], pol_keep);
+          tma_load_2d_hint(ys + yb * TM * 128, &maps.y[x.j], x.o0 + yb * 64, yt.row0, bar, pol_stream);
     };
-    const int pre = (int)min((long long)NSLOT, u1 - u0);  // slots free at the start
+    auto issue_b = [&](int i, const Unit& x) {
+      if (x.tile != bcur) {
+        bcur = x.tile;
+        bt = rc_tile(rc, G, x.tile);
+        nbbox = (slot_kmax(p, bt.slot) + 63) / 64;
+      }
+      uint64_t* bar = &bfull[i % NBS];
+      uint8_t* bs = bring + (i % NBS) * Cfg::B_BYTES;
+      mbar_arrive_expect_tx(bar, (uint32_t)(nbbox * XB * 128));
+      for (int kb = 0; kb < nbbox; ++kb)
+        tma_load_3d_hint(bs + kb * XB * 128, &maps.b[x.j], kb * 64, x.o0, bt.slot, bar, pol_keep);
+    };
+    // Slots free at the start.
+    const int pre_y = (int)min((long long)NYS, u1 - u0), pre_b = (int)min((long long)NBS, u1 - u0);
     if (PACKED) {
-      for (int i = 0; i < pre; ++i) issue_yb(i, tx_unit(w, p.n_slices, u0 + i));
+      for (int i = 0; i < pre_y; ++i) issue_y(i, tx_unit(w, p.n_slices, u0 + i));
+      for (int i = 0; i < pre_b; ++i) issue_b(i, tx_unit(w, p.n_slices, u0 + i));
       pdl_wait();  // the packed u comes from the shrink grid
     }
     int seg = -1, seg_tile = -1, seg_j = -1;
     int i = 0;
     for (long long un = u0; un < u1; ++un, ++i) {
       const Unit x = tx_unit(w, p.n_slices, un);
-      if (!PACKED || i >= pre) {
-        if (i >= NSLOT && !mbar_wait(&empty[i % NSLOT], (uint32_t)(((i / NSLOT) - 1) & 1))) {
+      if (!PACKED || i >= pre_y) {  // the slot's previous tile has been stored
+        if (i >= NYS && !mbar_wait(&yempty[i % NYS], (uint32_t)(((i / NYS) - 1) & 1))) {
           atomicOr(&s_fail, 1);
           break;
         }
-        issue_yb(i, x);
+        issue_y(i, x);
+      }
+      if (!PACKED || i >= pre_b) {  // the slot's previous block has been multiplied
+        if (i >= NBS && !mbar_wait(&bempty[i % NBS], (uint32_t)(((i / NBS) - 1) & 1))) {
+          atomicOr(&s_fail, 1);
+          break;
+        }
+        issue_b(i, x);
       }
       if (PACKED && (x.tile != seg_tile || x.j != seg_j)) {
         seg_tile = x.tile;
@@ -958,15 +993,15 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
           break;
         }
       }
-      const int slot = i % NSLOT, buf = i & 1;
-      if (!mbar_wait(&full[slot], (uint32_t)((i / NSLOT) & 1)) ||
+      const int bslot = i % NBS, buf = i & 1;
+      if (!mbar_wait(&bfull[bslot], (uint32_t)((i / NBS) & 1)) ||
           (i >= 2 && !mbar_wait(&tempty[buf], (uint32_t)(((i >> 1) - 1) & 1)))) {
         atomicOr(&s_fail, 1);
         break;
       }
       tc_fence_after_sync();
       const uint32_t ua = smem_addr(smem + (seg % NUB) * Cfg::U_BYTES);
-      const uint32_t bs = smem_addr(slots + slot * Cfg::SLOT + Cfg::Y_BYTES);
+      const uint32_t bs = smem_addr(bring + bslot * Cfg::B_BYTES);
       uint32_t acc = 0;
 #pragma unroll
       for (int ks = 0; ks < 2 * R / 16; ++ks) {
@@ -977,6 +1012,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         tc_mma_bf16(tmem + buf * XB, adesc, bdesc, idesc, acc);
         acc = 1;
       }
+      tc_commit(&bempty[bslot]);  // the B slot is free once these MMAs complete
       tc_commit(&tfull[buf]);
       if (PACKED) {  // last unit of the segment: its u buffer is free once these MMAs finish
         const long long seg_end = x.j + 1 < p.n_slices ? (long long)x.tile * w.nbt + w.blk_begin[x.j + 1]
@@ -1099,7 +1135,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         }
         const SliceDesc& sl = p.sl[x.j];
         const bool live = row < t.rows;
-        const int slot = i % NSLOT, buf = i & 1;
+        const int yslot = i % NYS, buf = i & 1;
         // Gathered: this thread's y row segment (XB / XNH columns) is loaded
         // before the wait for the unit's MMAs, so the loads overlap them.
         constexpr int GCH = XB / XNH / 8;  // 16-byte chunks of the segment
@@ -1111,13 +1147,14 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
 #pragma unroll
           for (int c = 0; c < GCH; ++c) yseg[c] = c * 8 < nvalid ? gy[c] : make_uint4(0, 0, 0, 0);
         }
-        if (!bad && !mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1))) {
+        if (!bad && (!mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1)) ||
+                     !mbar_wait(&yfull[yslot], (uint32_t)((i / NYS) & 1)))) {
           atomicOr(&s_fail, 1);
           bad = true;
         }
         bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below needs the whole warp
         tc_fence_after_sync();
-        uint8_t* ys = slots + slot * Cfg::SLOT;
+        uint8_t* ys = yring + yslot * Cfg::Y_BYTES;
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
         // 32 columns per TMEM load: two 16-column groups.  Gathered: unrolled,
@@ -1215,7 +1252,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&tempty[buf]);
-          mbar_arrive(&empty[slot]);
+          mbar_arrive(&yempty[yslot]);
         }
       }
     }

@@ -881,7 +881,10 @@ def run_e2e(args, sets, lk, torch, stream, dist):
     for i in range(n):
         one(i, stream)
     torch.cuda.synchronize()
-    k = max(min(args.steps // 4, 400), n)
+    # At least 64 steps, so the copy/compute pipeline reaches its steady
+    # state whatever K the value region used (at K = 20 five steps would be
+    # mostly fill and drain).
+    k = max(min(args.steps // 4, 400), 64, n)
     moved["h2d"] = moved["d2h"] = 0
     if dist:
         dist.barrier()

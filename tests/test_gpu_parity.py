@@ -502,16 +502,16 @@ def test_long_groups_tensor_core_shrink(R, mode):
     run_case(sy.draw(spec, 8), "o", mode=mode, path=want)
 
 
-@pytest.mark.parametrize("groups", [256, 260])
+@pytest.mark.parametrize("groups", [128, 132])
 @pytest.mark.parametrize("mode", ["apply", "split"])
 def test_many_long_groups(groups, mode):
-    """256 long groups fill the persistent tcgen05 expand's cached routing
-    exactly; 260 exceed it (the apply then pairs the tcgen05 shrink with the
+    """128 long groups fill the persistent tcgen05 expand's cached routing
+    exactly; 132 exceed it (the apply then pairs the tcgen05 shrink with the
     mma.sync expand).  100 rows per group, rank 64."""
     spec = _spec(max_num_loras=groups, max_lora_rank=64, rank_choices=(32, 64), kind="fixed",
                  fixed_slots=tuple(range(groups - 1, -1, -1)) + (-1,), fixed_lens=(100,) * groups + (5,),
                  hidden=128, n_heads=4, n_kv_heads=4, head_dim=32)
-    run_case(sy.draw(spec, 21), "qkv", mode=mode, path=TC if groups <= 256 else TC_MMA)
+    run_case(sy.draw(spec, 21), "qkv", mode=mode, path=TC if groups <= 128 else TC_MMA)
 
 
 def test_wait_timeout_is_reported_and_context_survives():

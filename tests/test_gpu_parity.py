@@ -640,6 +640,17 @@ def test_host_triple_unsorted_and_per_group():
     run_case(sy.draw("mixed64", 2), "o", mode="apply", path=SPLIT, parallel=True, host_ids=True)
 
 
+def test_host_triple_beyond_the_tile_table():
+    """More 64-row tiles than a launch's tile table holds (100 groups of 90
+    rows: 200 tiles): the shrink locates its tiles in the device triple
+    instead; same results."""
+    spec = _spec(max_num_loras=100, max_lora_rank=16, rank_choices=(16,), kind="fixed",
+                 fixed_slots=tuple(range(99, -1, -1)) + (-1,), fixed_lens=(90,) * 100 + (3,),
+                 hidden=256, n_heads=8, n_kv_heads=2, head_dim=32)
+    run_case(sy.draw(spec, 44), "qkv", mode="apply", path=MMA, host_ids=True)
+    run_case(sy.draw(spec, 45), "o", mode="apply", path=MMA, host_ids=True)
+
+
 @pytest.mark.parametrize("what", ["ids", "offsets"])
 def test_device_triple_differing_from_host_copy_is_flagged(what):
     """The shrink works from the host copy; the expand compares the device

@@ -767,6 +767,29 @@ def test_base_gemm_bias_ranks_and_delta_dominated():
     run_base_case(raw, "o", slot_ranks=True, poison=True)
 
 
+def test_base_gemm_decode_shapes():
+    """Decode-sized batches: bias, true ranks with NaN past them and an
+    order-one delta; rank 32 with a row count that is not a multiple of 16;
+    a single row; a two-stage input; a batch of base rows only."""
+    spec = _spec(max_num_loras=6, max_lora_rank=16, rank_choices=(8, 16), kind="decode", n_requests=200,
+                 base_prob=0.2, slot_dist="uniform", hidden=512, n_heads=8, n_kv_heads=4, head_dim=64)
+    raw = sy.add_base_weights(sy.add_bias(sy.emphasize_delta(sy.draw(spec, 99), 40.0), 99, scale=1.0), 99)
+    run_base_case(raw, "qkv", slot_ranks=True, poison=True, path=BASE | 0x4)
+    run_base_case(raw, "o", slot_ranks=True, poison=True, path=BASE | 0x4)
+    spec = _spec(max_num_loras=3, max_lora_rank=32, rank_choices=(32,), kind="fixed", fixed_slots=(2, 0, 1, -1),
+                 fixed_lens=(9, 17, 5, 6), hidden=256, n_heads=4, n_kv_heads=4, head_dim=64)
+    run_base_case(sy.add_base_weights(sy.draw(spec, 100), 100), "qkv", path=BASE | 0x4)
+    spec = _spec(max_num_loras=2, max_lora_rank=16, rank_choices=(16,), kind="fixed", fixed_slots=(1,),
+                 fixed_lens=(1,), hidden=256, n_heads=4, n_kv_heads=4, head_dim=64)
+    run_base_case(sy.add_base_weights(sy.draw(spec, 101), 101), "o", path=BASE | 0x4)
+    spec = _spec(max_num_loras=2, max_lora_rank=16, rank_choices=(16,), kind="fixed", fixed_slots=(0, 1, -1),
+                 fixed_lens=(30, 40, 20), hidden=128, n_heads=2, n_kv_heads=2, head_dim=128)
+    run_base_case(sy.add_base_weights(sy.draw(spec, 102), 102), "qkv", path=BASE | 0x4)
+    spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(70, 90), hidden=256, n_heads=4, n_kv_heads=4,
+                 head_dim=64)
+    run_base_case(sy.add_base_weights(sy.draw(spec, 103), 103), "qkv", path=BASE)
+
+
 def test_base_gemm_all_base_rows_and_fp32():
     """No routed rows (the base projection alone), and the generic kernel for fp32."""
     spec = _spec(kind="fixed", fixed_slots=(-1, -1), fixed_lens=(70, 90), hidden=256, n_heads=8, n_kv_heads=2,

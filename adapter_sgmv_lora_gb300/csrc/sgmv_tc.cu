@@ -154,9 +154,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
       s_fail = 0;
       s_kmax = ok ? slot_kmax(p, t.slot) : 0;
       for (int i = 0; i < NSTAGE; ++i) {
-        // gathered: one arrival for the A boxes' bytes, one when the warp's
-        // copies of the stage's x rows have landed
-        mbar_init(&full[i], gathered ? 2 : 1);
+        // gathered: one arrival for the A boxes' bytes, one from each of the
+        // four gathering warps once its copies of the stage's x rows landed
+        mbar_init(&full[i], gathered ? 1 + 4 : 1);
         mbar_init(&empty[i], 1);
       }
       mbar_init(&done, 1);
@@ -182,67 +182,39 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
   const int k0 = split * kc;
   const int nst = kc / TK;
 
-  if (ok && warp == 0 && gathered) {
-    // ---- producer, gathered batch: the whole warp copies the tile's x rows
-    // (scattered through token_rows) with 16-byte async copies into the
-    // stage's 128-byte-swizzled layout, as many stages deep as the ring, and
-    // lane 0 signals each stage once its copies have landed; the A rows come
-    // by TMA as below.
-    constexpr int kGatherDepth = NSTAGE;
+  if (ok && warp == 0 && lane == 0 && gathered) {
+    // ---- producer, gathered batch: the A rows by TMA; the x rows are
+    // copied by warps 2-5 (below), which join each stage's full barrier.
     const uint64_t pol_keep = policy_evict_last();
     uint32_t a_bytes = 0;
     for (int j = 0; j < p.n_slices; ++j) {
       const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
       if (khi > klo) a_bytes += (uint32_t)((khi - klo) * TK * 2);
     }
-    const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
-    int signalled = 0;  // stages whose x copies have been signalled
     for (int s = 0; s < nst; ++s) {
       const int slot = s % NSTAGE;
-      bool free_ok = true;
-      if (s >= NSTAGE && lane == 0) free_ok = mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1));
-      if (!__shfl_sync(0xffffffffu, (int)free_ok, 0)) {
-        if (lane == 0) atomicOr(&s_fail, 1);
+      if (s >= NSTAGE && !mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1))) {
+        atomicOr(&s_fail, 1);
         break;
       }
-      uint8_t* xs = smem + slot * Cfg::STAGE;
-      uint8_t* as = xs + Cfg::X_BYTES;
+      uint8_t* as = smem + slot * Cfg::STAGE + Cfg::X_BYTES;
       const int kk = k0 + s * TK;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&full[slot], a_bytes);
-        for (int j = 0; j < p.n_slices; ++j) {
-          const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
-          if (khi <= klo) continue;
-          uint8_t* dst = as + (j * R - n_base) * TK * 2;
-          if (klo == 0 && khi == R) {
-            tma_load_3d_hint(dst, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
-          } else {
-            int kb = klo;
-            for (; kb + 64 <= khi; kb += 64)
-              tma_load_3d_hint(dst + kb * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
-            for (; kb < khi; kb += 16)
-              tma_load_3d_hint(dst + kb * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
-          }
+      mbar_arrive_expect_tx(&full[slot], a_bytes);
+      for (int j = 0; j < p.n_slices; ++j) {
+        const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
+        if (khi <= klo) continue;
+        uint8_t* dst = as + (j * R - n_base) * TK * 2;
+        if (klo == 0 && khi == R) {
+          tma_load_3d_hint(dst, &maps.a[j], kk, 0, t.slot, &full[slot], pol_keep);
+        } else {
+          int kb = klo;
+          for (; kb + 64 <= khi; kb += 64)
+            tma_load_3d_hint(dst + kb * TK * 2, &maps.a64[j], kk, kb, t.slot, &full[slot], pol_keep);
+          for (; kb < khi; kb += 16)
+            tma_load_3d_hint(dst + kb * TK * 2, &maps.a16[j], kk, kb, t.slot, &full[slot], pol_keep);
         }
       }
-      for (int e = lane; e < TM * (TK / 8); e += 32) {  // row r, 16-byte chunk c
-        const int r = e >> 3, c = e & 7;
-        cp_async16(xs + r * 128 + ((c ^ (r & 7)) << 4), xg + (long long)s_rows[r] * p.x_row_stride + kk + c * 8);
-      }
-      cp_async_commit();
-      if (s - signalled >= kGatherDepth - 1) {  // the oldest stage in flight has landed
-        cp_async_wait<kGatherDepth - 1>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[signalled % NSTAGE]);
-        ++signalled;
-      }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0)
-      for (; signalled < nst; ++signalled) mbar_arrive(&full[signalled % NSTAGE]);
   } else if (ok && warp == 0 && lane == 0) {
     // ---- producer (x streams through L2 once; the slot's A rows are re-read
     // by every tile of the group, so they are kept)
@@ -304,6 +276,48 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
     }
     tc_commit(&done);  // accumulator complete
   } else if (ok && warp >= 2) {
+    if (gathered) {
+      // ---- gathered batch: warp w copies x rows 32*(w % 4) .. +31 of every
+      // stage (scattered through token_rows) with 16-byte async copies into
+      // the stage's 128-byte-swizzled layout, eight lanes per row, as many
+      // stages deep as the ring, and arrives on each stage's full barrier
+      // once its copies have landed.
+      const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+      const int rb = (warp & 3) * 32;
+      int signalled = 0;
+      bool gbad = false;
+      for (int s = 0; s < nst; ++s) {
+        const int slot = s % NSTAGE;
+        bool free_ok = true;
+        if (s >= NSTAGE && lane == 0) free_ok = mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1));
+        if (!__shfl_sync(0xffffffffu, (int)free_ok, 0)) {
+          gbad = true;
+          break;
+        }
+        uint8_t* xs = smem + slot * Cfg::STAGE;
+        const int kk = k0 + s * TK;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // row rb + e / 8, 16-byte chunk e % 8
+          const int e = lane + 32 * i, r = rb + (e >> 3), c = e & 7;
+          cp_async16(xs + r * 128 + ((c ^ (r & 7)) << 4), xg + (long long)s_rows[r] * p.x_row_stride + kk + c * 8);
+        }
+        cp_async_commit();
+        if (s - signalled >= NSTAGE - 1) {  // the oldest stage in flight has landed
+          cp_async_wait<NSTAGE - 1>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[signalled % NSTAGE]);
+          ++signalled;
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (gbad) atomicOr(&s_fail, 1);
+        for (; signalled < nst; ++signalled) mbar_arrive(&full[signalled % NSTAGE]);
+      }
+    }
     // ---- epilogue: warp w reads TMEM lanes 32*(w % 4) .. +31 (= tile rows)
     const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0));  // warp-uniform for tcgen05.ld
     tc_fence_after_sync();

@@ -1105,6 +1105,50 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       int yrow = 0;            // gathered: the y row of this thread's tile position
       bool tile_skip = false;  // gathered: the tile has an out-of-range entry
       Tile t{};
+      // Gathered: each warp copies its own block of a unit's y tile (32 rows
+      // x XB / XNH columns, eight lanes per row, 16-byte async copies into
+      // the slot's swizzled layout) two units ahead, one copy group per unit;
+      // rows past the tile or out of range are not copied (such a tile is
+      // skipped below).  The slot's previous unit (NYS >= 3 units back) was
+      // stored by this same warp.
+      // The y rows this lane copies (tile positions 32 q + lane / 8 + 4 it) are
+      // looked up once per tile.
+      int gtile = -1;
+      int grow[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) grow[it] = -1;
+      auto gather_y = [&](int iu, long long un_) {
+        if (un_ < u1 && !bad) {
+          const Unit xu = tx_unit(w, p.n_slices, un_);
+          if (xu.tile != gtile) {
+            gtile = xu.tile;
+            const Tile tu = rc_tile(rc, G, xu.tile);
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int r = q * 32 + (lane >> 3) + 4 * it;
+              const int yr = r < tu.rows ? p.token_rows[tu.row0 + r] : -1;
+              grow[it] = (yr >= 0 && yr < p.num_tokens) ? yr : -1;
+            }
+          }
+          const SliceDesc& su = p.sl[xu.j];
+          uint8_t* yb = yring + (iu % NYS) * Cfg::Y_BYTES + hf * TM * 128;
+          const __nv_bfloat16* yg = static_cast<const __nv_bfloat16*>(su.y);
+          const int c = lane & 7;
+          const int col = xu.o0 + hf * (XB / XNH) + c * 8;
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int r = q * 32 + (lane >> 3) + 4 * it;
+            if (grow[it] >= 0 && col < su.out_dim)
+              cp_async16(yb + r * 128 + ((c ^ (r & 7)) << 4), yg + (long long)grow[it] * su.y_row_stride + col);
+          }
+        }
+        cp_async_commit();
+      };
+      if constexpr (gathered) {
+        static_assert(NYS >= 3, "gathered y tiles are copied two units ahead");
+        gather_y(0, u0);
+        gather_y(1, u0 + 1);
+      }
       int i = 0;
       for (long long un = u0; un < u1; ++un, ++i) {
         const Unit x = tx_unit(w, p.n_slices, un);
@@ -1150,16 +1194,10 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         const SliceDesc& sl = p.sl[x.j];
         const bool live = row < t.rows;
         const int yslot = i % NYS, buf = i & 1;
-        // Gathered: this thread's y row segment (XB / XNH columns) is loaded
-        // before the wait for the unit's MMAs, so the loads overlap them.
-        constexpr int GCH = XB / XNH / 8;  // 16-byte chunks of the segment
-        uint4 yseg[GCH];
-        if (gathered && !tile_skip && live) {
-          const uint4* gy = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(sl.y) +
-                                                           (long long)yrow * sl.y_row_stride + x.o0 + hf * (XB / XNH));
-          const int nvalid = min(XB, sl.out_dim - x.o0) - hf * (XB / XNH);
-#pragma unroll
-          for (int c = 0; c < GCH; ++c) yseg[c] = c * 8 < nvalid ? gy[c] : make_uint4(0, 0, 0, 0);
+        if constexpr (gathered) {  // this unit's y block has landed; unit i + 2's copies start
+          gather_y(i + 2, un + 2);
+          cp_async_wait<2>();
+          __syncwarp();  // the block was copied by the warp's other lanes
         }
         if (!bad && (!mbar_wait(&tfull[buf], (uint32_t)((i >> 1) & 1)) ||
                      !mbar_wait(&yfull[yslot], (uint32_t)((i / NYS) & 1)))) {
@@ -1171,10 +1209,9 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         uint8_t* ys = yring + yslot * Cfg::Y_BYTES;
         const int o0 = x.o0;
         const int ovalid = min(XB, sl.out_dim - o0);
-        // 32 columns per TMEM load: two 16-column groups.  Gathered: unrolled,
-        // so yseg is indexed with constants (kept in registers).
+        // 32 columns per TMEM load: two 16-column groups.
         const bool work = !bad && !tile_skip;
-#pragma unroll(GATHER ? XB / (32 * XNH) : 1)
+#pragma unroll 1
         for (int cc = 0; cc < XB / (32 * XNH); ++cc) {
           if (!work) break;
           const int c32 = hf * (XB / (32 * XNH)) + cc;
@@ -1201,26 +1238,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
                 d[2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
               }
             }
-            if (gathered && live && c16 * 16 < ovalid) {
-              // Gathered: y + delta for this thread's own (scattered) row,
-              // written straight to global memory, rounded once.
-              uint4* gy = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
-                                                   (long long)yrow * sl.y_row_stride + o0 + c16 * 16);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                if (c16 * 16 + h * 8 >= ovalid) continue;
-                const uint4 yv = yseg[cc * 4 + g16 * 2 + h];
-                const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-                uint32_t out[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 yy = make_float2(__uint_as_float(yw[e] << 16), __uint_as_float(yw[e] & 0xFFFF0000u));
-                  const float2 r = add_f32x2(yy, make_float2(d[h * 8 + 2 * e], d[h * 8 + 2 * e + 1]));
-                  out[e] = round_pack_bf16x2(r.x, r.y);
-                }
-                gy[h] = make_uint4(out[0], out[1], out[2], out[3]);
-              }
-            } else if (live && c16 * 16 < ovalid) {
+            if (live && c16 * 16 < ovalid) {
               // y + delta, rounded once, written back over y in the slot.
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
@@ -1243,22 +1261,35 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
         __syncwarp();
         // This warp's 32 rows x XB / XNH columns to y: eight lanes per row,
         // so each store instruction writes whole 128-byte row segments.
-        if (work && !gathered) {
+        if (work) {
           constexpr int CPR = XB / XNH / 8;   // 16-byte chunks per row
           constexpr int RPI = 32 / CPR;       // rows per store instruction
           const int cch = hf * CPR + lane % CPR;  // this lane's chunk of the 128-column block
           const int r0 = q * 32 + lane / CPR;     // this lane's first tile row
           const uint8_t* sbase = ys + (cch >> 3) * TM * 128;
-          uint4* gp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
-                                               (long long)(t.row0 + r0) * sl.y_row_stride + o0 + cch * 8);
-          const long long gstep = (long long)RPI * sl.y_row_stride / 8;  // uint4 per RPI rows
-          if (cch * 8 < ovalid) {
+          if constexpr (gathered) {
+            __nv_bfloat16* ybase = static_cast<__nv_bfloat16*>(sl.y) + o0 + cch * 8;
 #pragma unroll
-            for (int it = 0; it < CPR; ++it, gp += gstep) {
+            for (int it = 0; it < CPR; ++it) {
               const int tr = r0 + it * RPI;
-              if (tr < t.rows)
-                st_global_v4_hint(gp, *reinterpret_cast<const uint4*>(sbase + tr * 128 + (((cch & 7) ^ (tr & 7)) << 4)),
+              const int yr = __shfl_sync(0xffffffffu, yrow, tr - q * 32);  // held by lane tr - 32 q
+              if (tr < t.rows && cch * 8 < ovalid)
+                st_global_v4_hint(reinterpret_cast<uint4*>(ybase + (long long)yr * sl.y_row_stride),
+                                  *reinterpret_cast<const uint4*>(sbase + tr * 128 + (((cch & 7) ^ (tr & 7)) << 4)),
                                   pol_stream);
+            }
+          } else {
+            uint4* gp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sl.y) +
+                                                 (long long)(t.row0 + r0) * sl.y_row_stride + o0 + cch * 8);
+            const long long gstep = (long long)RPI * sl.y_row_stride / 8;  // uint4 per RPI rows
+            if (cch * 8 < ovalid) {
+#pragma unroll
+              for (int it = 0; it < CPR; ++it, gp += gstep) {
+                const int tr = r0 + it * RPI;
+                if (tr < t.rows)
+                  st_global_v4_hint(gp, *reinterpret_cast<const uint4*>(sbase + tr * 128 + (((cch & 7) ^ (tr & 7)) << 4)),
+                                    pol_stream);
+              }
             }
           }
         }

@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
   __shared__ int s_ok;
   __shared__ int s_fail;
   __shared__ int s_kmax;
+  __shared__ int s_rows[TM];  // gathered batches: the x row of each tile position
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   pdl_wait();
@@ -400,16 +401,18 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
   const int cn = (int)((blockIdx.x / (unsigned)CL) % (unsigned)nsn);
   const long long tile = blockIdx.x / (unsigned)(CL * nsn);
   const int n_base = cn * NR;  // first u column of this cluster's part
+  const bool gathered = p.token_rows != nullptr;
   if (warp == 0) {
     Tile t{};
-    const bool ok = warp_locate_tile(p, TM, tile, t);
+    bool ok = warp_locate_tile(p, TM, tile, t);
+    if (ok && gathered) ok = warp_tile_rows(p, t, s_rows);  // the same outcome on every CTA of the cluster
     if (lane == 0) {
       s_tile = t;
       s_ok = ok;
       s_fail = 0;
       s_kmax = ok ? slot_kmax(p, t.slot) : 0;
       for (int i = 0; i < NSTAGE; ++i) {
-        mbar_init(&full[i], 1);
+        mbar_init(&full[i], gathered ? 1 + 4 : 1);  // gathered: + one arrival per x-copying warp
         mbar_init(&empty[i], 1);
       }
       mbar_init(&done, 1);
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
 
   if (ok && warp == 0 && lane == 0) {
     const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
-    uint32_t a_bytes = Cfg::X_BYTES;
+    uint32_t a_bytes = gathered ? 0 : Cfg::X_BYTES;
     for (int j = 0; j < p.n_slices; ++j) {
       const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
       if (khi > klo) a_bytes += (uint32_t)((khi - klo) * TK * 2);
@@ -450,7 +453,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
       uint8_t* as = xs + Cfg::X_BYTES;
       mbar_arrive_expect_tx(&full[slot], a_bytes);
       const int kk = k0 + s * TK;
-      tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
+      if (!gathered) tma_load_2d_hint(xs, &maps.x, kk, t.row0, &full[slot], pol_stream);
       for (int j = 0; j < p.n_slices; ++j) {
         // Rows [klo, khi) of slice j fall in this part's columns (and the rank).
         const int klo = max(0, n_base - j * R), khi = min(min(R, n_base + NR - j * R), kmax);
@@ -490,6 +493,44 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(cons
       tc_commit(&empty[slot]);
     }
     tc_commit(&done);
+  } else if (ok && warp >= 2 && gathered) {
+    // ---- gathered batch: warps 2-5 copy the tile's scattered x rows of
+    // this CTA's K range (32 rows each), as in the one-CTA shrink.
+    const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+    const int rb = (warp & 3) * 32;
+    int signalled = 0;
+    bool gbad = false;
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % NSTAGE;
+      bool free_ok = true;
+      if (s >= NSTAGE && lane == 0) free_ok = mbar_wait(&empty[slot], (uint32_t)(((s / NSTAGE) - 1) & 1));
+      if (!__shfl_sync(0xffffffffu, (int)free_ok, 0)) {
+        gbad = true;
+        break;
+      }
+      uint8_t* xs = smem + slot * Cfg::STAGE;
+      const int kk = k0 + s * TK;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i, r = rb + (e >> 3), c = e & 7;
+        cp_async16(xs + r * 128 + ((c ^ (r & 7)) << 4), xg + (long long)s_rows[r] * p.x_row_stride + kk + c * 8);
+      }
+      cp_async_commit();
+      if (s - signalled >= NSTAGE - 1) {
+        cp_async_wait<NSTAGE - 1>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[signalled % NSTAGE]);
+        ++signalled;
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (gbad) atomicOr(&s_fail, 1);
+      for (; signalled < nst; ++signalled) mbar_arrive(&full[signalled % NSTAGE]);
+    }
   }
   // Every thread: the accumulator is complete (or the CTA failed), and so is
   // every other CTA's of the cluster, whose rings are then free.
@@ -1533,7 +1574,7 @@ cudaError_t launch_tc_apply_packed(const ProblemDesc& p, void* workspace, cudaSt
   const int nsn = tc_pack_splits(p);
   uint8_t* upk = static_cast<uint8_t*>(workspace);
   cudaError_t e = cudaErrorNotSupported;
-  if (!p.token_rows) {
+  {
     const long long tiles_lb = (p.end + TM - 1) / TM;
     if (nsn > 1) e = launch_ksplit(p, smaps, upk, s, nsn, 1, false);
     else if (tiles_lb * 2 <= 2LL * device_sm_count()) e = launch_ksplit(p, smaps, upk, s, 2, 1, true);

@@ -17,7 +17,10 @@
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= rows) and
 //           stores of u: fp32 rows (a K split's plane), or for the apply on
 //           ranks 64/128 the packed intermediate (bf16 hi + lo in the
-//           expand's swizzled operand layout, see pack_u16).
+//           expand's swizzled operand layout, see pack_u16).  For gathered
+//           batches (token_rows) they first copy the tile's scattered x
+//           rows into the stages (16-byte async copies, 32 rows each) in
+//           place of the producer's x boxes.
 // Expand (further down): persistent, one CTA per SM over (tile, slice,
 // 128-column block) units, TMEM accumulators, 8 epilogue warps.
 // Rows of the 128-row box past the group are other groups' rows (read, never
@@ -373,7 +376,9 @@ __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_kernel(const __gri
 // order (the same order on every CTA: deterministic) and stores them packed
 // (pack_u16).  Two cluster barriers: before the exchange (every CTA's MMAs
 // have drained its ring) and after it.  NST: ring depth -- a shallow ring
-// lets two CTAs share an SM when the grid has more CTAs than SMs.
+// lets two CTAs share an SM when the grid has more CTAs than SMs.  Gathered
+// batches: warps 2-5 copy the scattered x rows of the CTA's K range, as in
+// the one-CTA shrink.
 template <int NR, int CL, int NST>
 __global__ void __launch_bounds__(TTHREADS, 1) sgmv_tc_shrink_ksplit_kernel(const __grid_constant__ ProblemDesc p,
                                                                            const __grid_constant__ TcMaps maps,
@@ -870,8 +875,9 @@ __device__ __forceinline__ Unit tx_unit(const TxWork& w, int n_slices, long long
 // PACKED: u arrives packed (the tcgen05 shrink's image per (tile, slice),
 // see pack_u16) and warp 0 copies each segment's image into its u buffer;
 // otherwise u is fp32 [end, n*R] (nsplit planes) and the epilogue warps
-// convert it.  GATHER: the batch has token_rows (the epilogue reads and
-// writes its scattered y rows itself); the sorted instantiation compiles
+// convert it.  GATHER: the batch has token_rows (the epilogue warps copy
+// their blocks of the scattered y rows into the slots themselves and store
+// them back through token_rows); the sorted instantiation compiles
 // none of that.
 template <int R, bool PACKED, bool GATHER>
 __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __grid_constant__ ProblemDesc p,
@@ -972,7 +978,7 @@ __global__ void __launch_bounds__(XTHREADS, 1) sgmv_tc_expand_kernel(const __gri
       }
       uint64_t* bar = &yfull[i % NYS];
       uint8_t* ys = yring + (i % NYS) * Cfg::Y_BYTES;
-      // Gathered batches: the epilogue reads its y rows itself (scattered).
+      // Gathered batches: the epilogue warps copy the y rows (scattered).
       mbar_arrive_expect_tx(bar, GATHER ? 0u : (uint32_t)Cfg::Y_BYTES);
       if (!GATHER)
         for (int yb = 0; yb < XB / 64; ++yb)

@@ -848,3 +848,50 @@ def test_kernels_per_group_ragged_and_ranks(R):
     run_case(sy.draw(spec, 101 + R), "o", mode="apply", path=SPLIT, host_offsets=True)
     raw = sy.add_bias(sy.draw(spec, 102 + R), 102 + R)
     run_case(raw, "qkv", mode="apply", slot_ranks=True, poison=True, path=SPLIT, host_offsets=True)
+
+
+# ------------------------------------- tensor-core apply: grid extremes --
+
+@pytest.mark.parametrize("host_offsets", [False, True])
+def test_tc_apply_few_tiles_long_input(host_offsets):
+    """Eight 128-row tiles (four groups of 200 rows) with in = 4096: the
+    apply's shrink splits K over 4-CTA clusters (n*R = 384 and 128), the
+    partials exchanged through distributed shared memory.  Every row against
+    the oracle with an order-one delta, with and without the routing's host
+    copy."""
+    spec = _spec(max_num_loras=4, max_lora_rank=128, rank_choices=(64, 128), kind="fixed",
+                 fixed_slots=(3, 0, 2, 1, -1), fixed_lens=(200, 200, 200, 200, 11),
+                 hidden=4096, n_heads=32, n_kv_heads=8, head_dim=128)
+    raw = sy.emphasize_delta(sy.draw(spec, 51), 40.0)
+    run_case(raw, "qkv", mode="apply", path=TC, parallel=True, host_offsets=host_offsets)
+    run_case(raw, "o", mode="apply", path=TC, parallel=True, host_offsets=host_offsets)
+
+
+def test_tc_apply_many_tiles_short_input():
+    """448 tiles (eight groups of 7100 rows) with in = 128: one shrink CTA
+    per tile over several waves, and the persistent expand's units spread
+    over every SM.  Ranks 64, every row against the oracle."""
+    spec = _spec(max_num_loras=8, max_lora_rank=64, rank_choices=(32, 64), kind="fixed",
+                 fixed_slots=tuple(range(8)) + (-1,), fixed_lens=(7100,) * 8 + (5,),
+                 hidden=128, n_heads=4, n_kv_heads=2, head_dim=32)
+    raw = sy.draw(spec, 52)
+    run_case(raw, "qkv", mode="apply", path=TC, parallel=True)
+    run_case(raw, "o", mode="apply", path=TC, parallel=True)
+
+
+def test_tc_apply_deterministic():
+    """The K-split shrink sums its CTAs' partials in rank order: repeated
+    applies give bit-identical y."""
+    lk, device = _lk(), _dev()
+    spec = _spec(max_num_loras=4, max_lora_rank=128, rank_choices=(64, 128), kind="fixed",
+                 fixed_slots=(3, 0, 2, 1, -1), fixed_lens=(200, 200, 200, 200, 11),
+                 hidden=4096, n_heads=32, n_kv_heads=8, head_dim=128)
+    raw = sy.emphasize_delta(sy.draw(spec, 54), 40.0)
+    outs = []
+    for _ in range(3):
+        dev = device.prepare(raw, "qkv")
+        lk.lora_sgmv_apply(dev["problem"], dev["routing"], dev["workspace"])
+        torch.cuda.synchronize()
+        assert lk.lora_get_device_status() == 0
+        outs.append(device.y_host(dev))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])

@@ -895,3 +895,56 @@ def test_tc_apply_deterministic():
         assert lk.lora_get_device_status() == 0
         outs.append(device.y_host(dev))
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+# ------------------------------------------------- seeded random batches --
+
+def _random_case(case):
+    """A random small problem for case `case` (seeded): slot count, rank,
+    true ranks, widths, request mix (one-token and long requests, base
+    requests anywhere before sorting), dtype, layout and options.  Returns
+    (raw, kwargs for run_case, projection, run the unsorted form too)."""
+    rng = np.random.default_rng(20000 + case)
+    R = int(rng.choice([16, 32, 64, 128]))
+    S = int(rng.integers(1, 9))
+    ranks = sorted({R, max(1, R // 2), int(rng.integers(1, R + 1))})
+    hd = int(rng.choice([32, 64]))
+    n_heads = int(rng.choice([2, 4, 8]))
+    n_kv = int(rng.choice([1, 2])) if n_heads > 2 else 1
+    hidden = int(rng.choice([64, 128, 256, 512]))
+    n_req = int(rng.integers(1, 11))
+    slots = [int(v) for v in rng.integers(-1, S, size=n_req)]
+    lens = [int(rng.integers(1, 9)) if rng.random() < 0.5 else
+            int(rng.integers(60, 330)) if rng.random() < 0.7 else int(rng.integers(330, 1200)) for _ in range(n_req)]
+    dtype = "f32" if rng.random() < 0.15 else "bf16"
+    spec = _spec(dtype=dtype, max_num_loras=S, max_lora_rank=R, rank_choices=tuple(ranks), kind="fixed",
+                 fixed_slots=tuple(slots), fixed_lens=tuple(lens), hidden=hidden, n_heads=n_heads,
+                 n_kv_heads=n_kv, head_dim=hd, rslora_count=int(rng.integers(0, S + 1)))
+    raw = sy.draw(spec, 30000 + case)
+    if rng.random() < 0.5:
+        raw = sy.emphasize_delta(raw, 40.0)
+    if rng.random() < 0.3:
+        raw = sy.add_bias(raw, case, scale=1.0)
+    proj = "qkv" if rng.random() < 0.6 else "o"
+    kw = dict(mode="apply" if rng.random() < 0.6 else "split",
+              fused=bool(rng.random() < 0.7) or proj == "o")
+    if rng.random() < 0.4:
+        kw.update(slot_ranks=True, poison=True)
+    if rng.random() < 0.3 and kw["mode"] == "apply" and kw["fused"]:
+        kw["host_ids"] = True
+    unsorted = dtype == "bf16" and rng.random() < 0.3
+    return raw, kw, proj, unsorted
+
+
+@pytest.mark.parametrize("case", range(64))
+def test_random_batches(case):
+    """Seeded random batches across the kernel families (generic, mma.sync,
+    tcgen05, kernels per group), layouts (fused, per projection), options
+    (bias, true ranks with NaN in the padding, the routing's host copies,
+    rsLoRA slots) and modes (apply, split): every routed row against the
+    oracle, rows past `end` bit-identical; some also in arrival order through
+    token_rows against the per-token oracle."""
+    raw, kw, proj, unsorted = _random_case(case)
+    run_case(raw, proj, **kw)
+    if unsorted:
+        run_unsorted(raw, proj, kw["mode"])
